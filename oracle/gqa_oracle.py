@@ -1,0 +1,233 @@
+"""Plain, slow fp64 statement of single-query grouped-query decode attention.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): nothing on the product path imports this.
+
+What is computed, for query row ``t`` and query head ``h`` (all arithmetic in float64):
+
+    g      = h // (n_heads // n_kv_heads)                 KV head of the group
+    s      = seq_of[t]                                    which sequence's cache
+    J      = 0 .. kv_len[t]-1                             dense decode, or
+    J      = ids[t][0 : min(kv_len[t], budget)]           selected cells
+    x_j    = scale * sum_d q[t,h,d] * K^[s,j,g,d]         for j in J
+    w_j    = exp(x_j - max x) / sum_j' exp(x_j' - max x)
+    out    = sum_j w_j * V^[s,j,g,:]                      (all zeros when J is empty)
+
+K^ / V^ are the dequantised cache rows: an f16 value widened exactly, or an int8 value times
+the f16 scale of its 64-dim group (both products are exact in float64).
+
+Passages followed (page title, then the part of it):
+  * attention_gqa.metal (cera 0.5.4 sources): one KV head serves all query heads of its group,
+    head -> KV head by integer division by the group size; phase 1 scores scaled q.k, phase 2
+    max / exp(x - max) / sum, phase 3 the probability-weighted sum of V rows.
+  * flash_attention.metal (cera 0.2.0 sources): the same single-query decode as one online pass;
+    a zero-length sequence writes zeros.
+  * qsa2.metal (regolith), qsa_attn2 and qsa_attn3: int8 K/V rows times one f16 scale per 64
+    dims; a row visits the first min(n_kv, budget) entries of its selected-cell id list; the
+    split partials are the unnormalised accumulator with the chunk's max and sum.
+  * qsa2.metal (regolith), qsa_merge2: the log-sum-exp merge of those partials.
+  * flash_attention_tq.metal (cera 0.4.0 sources): a causal row at position p attends to [0, p].
+
+Readings taken where the pages leave a step open are listed in DESIGN.md ("Readings").
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+SCALE_GROUP = 64  # dims sharing one f16 scale in the int8 cache (qsa2.metal, qsa_attn2)
+
+
+# ----------------------------------------------------------------------------- dequantisation
+
+def dequant_f16(x) -> np.ndarray:
+    """f16 cache values widened to float64 (exact)."""
+    return np.asarray(x, dtype=np.float16).astype(np.float64)
+
+
+def dequant_q8(vals, scales) -> np.ndarray:
+    """int8 values times the f16 scale of their 64-dim group, in float64 (exact).
+
+    ``vals[..., D]`` int8 and ``scales[..., D // 64]`` f16, as in qsa2.metal's qsa_attn2, where a
+    K element is float(int8) * float(scale[row*4 + dim/64]).
+    """
+    v = np.asarray(vals, dtype=np.int8).astype(np.float64)
+    s = np.asarray(scales, dtype=np.float16).astype(np.float64)
+    return v * np.repeat(s, SCALE_GROUP, axis=-1)
+
+
+# ----------------------------------------------------------------------------- the definition
+
+def _kv_head_of(h: int, group: int) -> int:
+    """Query head h reads KV head h // group (attention_gqa.metal, q_head_base = kv_head*group)."""
+    return h // group
+
+
+def _width(kv_len: int, budget) -> int:
+    """Number of id-list entries a row visits: min(n_kv, budget) (qsa2.metal, qsa_attn2)."""
+    n = max(int(kv_len), 0)
+    return n if budget is None else min(n, int(budget))
+
+
+def _scores(qg: np.ndarray, K: np.ndarray, scale: float) -> np.ndarray:
+    """x[h, j] = scale * q_h . K_j  (attention_gqa.metal phase 1)."""
+    return scale * (qg @ K.T)
+
+
+def _softmax_rows(x: np.ndarray) -> np.ndarray:
+    """Safe softmax along the last axis: exp(x - max) / sum (attention_gqa.metal phase 2)."""
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _weighted_sum(w: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """out[h, :] = sum_j w[h, j] V_j (attention_gqa.metal phase 3)."""
+    return w @ V
+
+
+def attend_positions(qg, Khat, Vhat, scale) -> np.ndarray:
+    """Attention of the query heads ``qg [G][D]`` over explicit rows ``Khat/Vhat [n][D]``.
+
+    An empty row set gives zeros (flash_attention.metal, the seq_len == 0 guard).
+    """
+    qg = np.asarray(qg, dtype=np.float64)
+    if len(Khat) == 0:
+        return np.zeros((qg.shape[0], qg.shape[1]), dtype=np.float64)
+    x = _scores(qg, np.asarray(Khat, np.float64), float(scale))
+    return _weighted_sum(_softmax_rows(x), np.asarray(Vhat, np.float64))
+
+
+def selected_positions(kv_len: int, ids_row=None, budget=None) -> np.ndarray:
+    """Cache positions a row visits: dense 0..kv_len-1, or the first min(kv_len, budget) ids.
+
+    Ids must lie in [0, kv_len): the selected list names cells of this row's context
+    (qsa2.metal, qsa_topk2 emits only cells below n_kv).  An id outside it raises.
+    """
+    if ids_row is None:
+        return np.arange(max(int(kv_len), 0), dtype=np.int64)
+    if budget is None:
+        raise ValueError("ids need a budget")
+    J = np.asarray(ids_row, dtype=np.int64)[: _width(kv_len, budget)]
+    if len(J) and (J.min() < 0 or J.max() >= kv_len):
+        raise ValueError("an id lies outside [0, kv_len)")
+    return J
+
+
+def _decode(q, kv_rows, n_kv_heads, kv_len, scale, seq_of, ids, budget, rows):
+    q = np.asarray(q)
+    T, H, D = q.shape
+    if H % n_kv_heads:
+        raise ValueError("n_heads must be a multiple of n_kv_heads")
+    G = H // n_kv_heads
+    rows = range(T) if rows is None else list(rows)
+    out = np.zeros((len(rows), H, D), dtype=np.float64)
+    for i, t in enumerate(rows):
+        s = t if seq_of is None else int(seq_of[t])
+        J = selected_positions(int(kv_len[t]), None if ids is None else ids[t], budget)
+        for g in range(n_kv_heads):
+            heads = [h for h in range(H) if _kv_head_of(h, G) == g]
+            Khat, Vhat = kv_rows(s, J, g)
+            out[i, heads] = attend_positions(q[t, heads].astype(np.float64), Khat, Vhat, scale)
+    return out
+
+
+def decode_f16(q, k_cache, v_cache, kv_len, scale, seq_of=None, ids=None, budget=None, rows=None):
+    """Decode attention over an f16 cache ``[n_seq][cap][n_kv_heads][D]``; returns float64.
+
+    ``q [T][H][D]`` (fp32 values, widened exactly), ``kv_len[T]``, ``seq_of[T]`` (None: row t
+    reads sequence t), optional ``ids [T][budget]``.  ``rows`` restricts the output to a subset
+    of query rows (returned in that order).
+    """
+    def kv_rows(s, J, g):
+        return dequant_f16(k_cache[s, J, g, :]), dequant_f16(v_cache[s, J, g, :])
+
+    return _decode(q, kv_rows, k_cache.shape[2], kv_len, scale, seq_of, ids, budget, rows)
+
+
+def decode_q8(q, k_vals, v_vals, k_scales, v_scales, kv_len, scale, seq_of=None, ids=None,
+              budget=None, rows=None):
+    """Decode attention over an int8 cache with one f16 scale per 64 dims; returns float64.
+
+    Values ``[n_seq][cap][n_kv_heads][D]`` int8, scales ``[n_seq][cap][n_kv_heads][D/64]`` f16.
+    """
+    def kv_rows(s, J, g):
+        return (dequant_q8(k_vals[s, J, g, :], k_scales[s, J, g, :]),
+                dequant_q8(v_vals[s, J, g, :], v_scales[s, J, g, :]))
+
+    return _decode(q, kv_rows, k_vals.shape[2], kv_len, scale, seq_of, ids, budget, rows)
+
+
+# ----------------------------------------------------------------------------- split + merge
+
+def _split(q, kv_rows, n_kv_heads, kv_len, scale, seq_of, ids, budget, chunk):
+    """Chunked partials over the visited list: for chunk c (entries [c*chunk, (c+1)*chunk)),
+    m = max_j x_j, p_j = exp(x_j - m), l = sum_j p_j, acc = sum_j p_j V^_j (unnormalised).
+
+    Returns acc [T][S][H][D], m [T][S][H], l [T][S][H], n_valid [T]; chunks at or past
+    n_valid[t] are left as acc = 0, m = -inf, l = 0 (qsa2.metal, qsa_attn2 writes nothing for
+    them and qsa_merge2 reads only the first ceil(width / chunk)).
+    """
+    q = np.asarray(q)
+    T, H, D = q.shape
+    G = H // n_kv_heads
+    J_all = [selected_positions(int(kv_len[t]), None if ids is None else ids[t], budget)
+             for t in range(T)]
+    n_valid = np.array([-(-len(J) // chunk) for J in J_all], dtype=np.int64)
+    S = max(1, int(n_valid.max()) if T else 1)
+    acc = np.zeros((T, S, H, D))
+    m = np.full((T, S, H), -np.inf)
+    l = np.zeros((T, S, H))
+    for t in range(T):
+        s = t if seq_of is None else int(seq_of[t])
+        for g in range(n_kv_heads):
+            heads = [h for h in range(H) if _kv_head_of(h, G) == g]
+            for c in range(int(n_valid[t])):
+                Jc = J_all[t][c * chunk:(c + 1) * chunk]
+                Khat, Vhat = kv_rows(s, Jc, g)
+                x = _scores(q[t, heads].astype(np.float64), Khat, float(scale))
+                mc = x.max(axis=-1)
+                p = np.exp(x - mc[:, None])
+                m[t, c, heads] = mc
+                l[t, c, heads] = p.sum(axis=-1)
+                acc[t, c, heads] = _weighted_sum(p, Vhat)
+    return acc, m, l, n_valid
+
+
+def split_partials_f16(q, k_cache, v_cache, kv_len, scale, chunk, seq_of=None, ids=None,
+                       budget=None):
+    def kv_rows(s, J, g):
+        return dequant_f16(k_cache[s, J, g, :]), dequant_f16(v_cache[s, J, g, :])
+
+    return _split(q, kv_rows, k_cache.shape[2], kv_len, scale, seq_of, ids, budget, chunk)
+
+
+def split_partials_q8(q, k_vals, v_vals, k_scales, v_scales, kv_len, scale, chunk, seq_of=None,
+                      ids=None, budget=None):
+    def kv_rows(s, J, g):
+        return (dequant_q8(k_vals[s, J, g, :], k_scales[s, J, g, :]),
+                dequant_q8(v_vals[s, J, g, :], v_scales[s, J, g, :]))
+
+    return _split(q, kv_rows, k_vals.shape[2], kv_len, scale, seq_of, ids, budget, chunk)
+
+
+def lse_merge(acc, m, l, n_valid) -> np.ndarray:
+    """Log-sum-exp merge of split partials (qsa2.metal, qsa_merge2):
+
+        M = max_c m_c,  e_c = exp(m_c - M),  L = sum_c l_c e_c,  out = sum_c acc_c e_c / L
+
+    over the first ``n_valid[t]`` chunks of row t; a row with no valid chunk gives zeros.
+    ``acc [T][S][H][D]``, ``m, l [T][S][H]`` (natural-log m).
+    """
+    acc = np.asarray(acc, np.float64)
+    m = np.asarray(m, np.float64)
+    l = np.asarray(l, np.float64)
+    T, S, H, D = acc.shape
+    out = np.zeros((T, H, D))
+    for t in range(T):
+        n = int(n_valid[t])
+        if n == 0:
+            continue
+        M = m[t, :n].max(axis=0)                    # [H]
+        e = np.exp(m[t, :n] - M[None, :])           # [n][H]
+        L = (l[t, :n] * e).sum(axis=0)              # [H]
+        out[t] = (acc[t, :n] * e[:, :, None]).sum(axis=0) / L[:, None]
+    return out

@@ -1,0 +1,177 @@
+"""CPU pins of the fp64 oracle (no GPU): closed forms, brute force, invariants, planted mistakes."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.gqa_oracle as OG
+import pins
+from gqa_decode_attention_03_gb300 import workloads as W
+
+
+def test_closed_forms():
+    assert pins.check_closed_forms() == []
+
+
+def test_brute_force_30_digits():
+    assert pins.check_brute_force() == []
+
+
+def test_invariants():
+    assert pins.check_invariants() == []
+
+
+def test_identical_keys_give_mean_of_v():
+    c = W.make_f16_case(21, 1, 4, 1, 64, [33], scale=0.3)
+    c.k[0, :33] = c.k[0, 0]  # every key equal -> uniform weights
+    got = pins.oracle_case(c)
+    mean = c.v[0, :33, 0].astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(got[0], np.broadcast_to(mean, (4, 64)), rtol=1e-13, atol=1e-14)
+
+
+def test_dominant_key_returns_its_row():
+    c = W.make_f16_case(22, 1, 1, 1, 64, [40], scale=1.0)
+    j = 17
+    qn = c.q[0, 0].astype(np.float64)
+    c.k[0, :40] = np.float16(0)
+    c.k[0, j, 0] = (qn / np.linalg.norm(qn) * 8).astype(np.float16)  # x_j ~ 8 |q| ~ 64
+    got = pins.oracle_case(c)[0, 0]
+    xj = float(np.dot(qn, c.k[0, j, 0].astype(np.float64)))
+    bound = 39 * math.exp(-xj) * np.abs(c.v[0, :40, 0].astype(np.float64)).max() * 2
+    assert np.max(np.abs(got - c.v[0, j, 0].astype(np.float64))) <= bound
+
+
+def test_permuting_positions_changes_nothing():
+    c = W.make_f16_case(23, 1, 8, 2, 64, [45], scale=0.2)
+    ref = pins.oracle_case(c)
+    perm = np.random.default_rng(0).permutation(45)
+    c.k[0, :45] = c.k[0, perm]
+    c.v[0, :45] = c.v[0, perm]
+    np.testing.assert_allclose(pins.oracle_case(c), ref, rtol=1e-12, atol=1e-13)
+
+
+def test_empty_context_is_zero():
+    c = W.make_f16_case(24, 2, 4, 2, 64, [0, 0], cache_cap=4)
+    assert np.array_equal(pins.oracle_case(c), np.zeros((2, 4, 64)))
+    acc, m, l, nv = oracle.split_partials_f16(c.q, c.k, c.v, c.kv_len, c.scale, 8)
+    assert np.array_equal(oracle.lse_merge(acc, m, l, nv), np.zeros((2, 4, 64)))
+
+
+def test_nan_past_length_is_never_read():
+    # the generator fills positions >= kv_len with NaN; a finite answer shows none was read
+    c = W.make_f16_case(25, 3, 4, 2, 64, [3, 9, 1], cache_cap=12, seq_of=[0, 0, 1])
+    assert np.isnan(c.k[0, 9:]).all() and np.isfinite(pins.oracle_case(c)).all()
+
+
+def test_selected_ids_equal_dense_over_gathered_cells():
+    c = W.make_q8_case(26, 1, 12, 1, 128, [300], budget=40, scale=0.0625)
+    ref = pins.oracle_case(c)
+    J = c.ids[0, :40]
+    g = W.make_q8_case(26, 1, 12, 1, 128, [40], scale=0.0625)
+    g.kq[0, :40], g.vq[0, :40] = c.kq[0, J], c.vq[0, J]
+    g.ksc[0, :40], g.vsc[0, :40] = c.ksc[0, J], c.vsc[0, J]
+    g.q = c.q
+    assert np.array_equal(pins.oracle_case(g), ref)
+
+
+def test_selected_width_is_min_of_length_and_budget():
+    c = W.make_q8_case(27, 2, 4, 1, 64, [5, 100], budget=8, scale=0.1)
+    assert list(c.ids[0, :5]) == [0, 1, 2, 3, 4] and (c.ids[0, 5:] == -1).all()
+    assert len(oracle.selected_positions(5, c.ids[0], 8)) == 5
+    assert len(oracle.selected_positions(100, c.ids[1], 8)) == 8
+    with pytest.raises(ValueError):
+        oracle.selected_positions(3, np.array([0, 1, 5, 6]), 4)  # id 5 >= kv_len 3
+
+
+def test_causal_rows_equal_truncated_decode():
+    # flash_attention_tq.metal (cera 0.4.0): causal row r at position start+r sees [0, start+r]
+    start, R = 20, 4
+    c = W.make_f16_case(28, R, 4, 2, 64, [start + r + 1 for r in range(R)], cache_cap=start + R,
+                        seq_of=[0] * R, n_seq=1)
+    got = pins.oracle_case(c)
+    for r in range(R):
+        one = oracle.decode_f16(c.q[r:r + 1], c.k[:, :start + r + 1], c.v[:, :start + r + 1],
+                                [start + r + 1], c.scale, seq_of=[0])
+        assert np.array_equal(got[r], one[0])
+
+
+def test_q8_dequant_cells_exact():
+    vals = np.array([[-127, 1, 64, 0] * 16 + [5] * 64], dtype=np.int8)  # D = 128
+    sc = np.array([[0.0125, 0.007]], dtype=np.float16)
+    d = oracle.dequant_q8(vals, sc)
+    s0, s1 = float(np.float16(0.0125)), float(np.float16(0.007))
+    assert s0 == 0.0124969482421875  # 1638 / 1024 * 2**-7
+    assert d[0, 0] == -127 * s0 and d[0, 2] == 64 * s0 and d[0, 64] == 5 * s1
+    assert d[0, 63] == 0.0
+
+
+def test_scale_folds_into_q():
+    c = W.make_f16_case(29, 1, 4, 1, 64, [30], scale=0.25)
+    ref = pins.oracle_case(c)
+    c.q = c.q * 2  # exact in fp32
+    c.scale = 0.125
+    np.testing.assert_allclose(pins.oracle_case(c), ref, rtol=1e-14, atol=1e-15)
+
+
+def test_merge_of_one_chunk_is_acc_over_l():
+    rng = np.random.default_rng(3)
+    acc = rng.standard_normal((1, 1, 2, 64))
+    m = rng.standard_normal((1, 1, 2))
+    l = rng.uniform(0.5, 4, (1, 1, 2))
+    got = oracle.lse_merge(acc, m, l, [1])
+    np.testing.assert_allclose(got[0], acc[0, 0] / l[0, 0][:, None], rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+def _mutants():
+    """Plausible mistakes planted in the oracle; the battery must catch every one."""
+    return {
+        "kv head by modulo": ("_kv_head_of", lambda h, group: h % group),
+        "scale dropped": ("_scores", lambda qg, K, scale: qg @ K.T),
+        "scale squared": ("_scores", lambda qg, K, scale: scale * scale * (qg @ K.T)),
+        "max sign flipped": ("_softmax_rows",
+                             lambda x: (lambda e: e / e.sum(-1, keepdims=True))(
+                                 np.exp(x.max(-1, keepdims=True) - x))),
+        "not normalised": ("_softmax_rows", lambda x: np.exp(x - x.max(-1, keepdims=True))),
+        "v rows reversed": ("_weighted_sum", lambda w, V: w @ V[::-1]),
+        "k used for v": None,  # handled below via attend_positions
+        "budget ignored": ("_width", lambda n, budget: max(int(n), 0)),
+        "width off by one": ("_width",
+                             lambda n, budget: max(int(n), 0) if budget is None
+                             else max(0, min(max(int(n), 0), int(budget)) - 1)),
+        "scale group of 32": ("SCALE_GROUP", 32),
+    }
+
+
+@pytest.mark.parametrize("name", [k for k in _mutants()])
+def test_planted_mistake_is_caught(name, monkeypatch):
+    assert pins.battery() == []
+    spec = _mutants()[name]
+    if spec is None:
+        orig = OG.attend_positions
+
+        def wrong(qg, Khat, Vhat, scale):
+            return orig(qg, Khat, Khat, scale)
+        monkeypatch.setattr(OG, "attend_positions", wrong)
+    else:
+        monkeypatch.setattr(OG, spec[0], spec[1])
+    assert pins.battery() != [], f"planted mistake '{name}' went unnoticed"
+
+
+def test_planted_merge_mistakes_are_caught(monkeypatch):
+    import numpy as _np
+
+    def merge_without_weights(acc, m, l, n_valid):
+        acc = _np.asarray(acc, _np.float64)
+        T, S, H, D = acc.shape
+        out = _np.zeros((T, H, D))
+        for t in range(T):
+            n = int(n_valid[t])
+            if n:
+                out[t] = acc[t, :n].sum(0) / _np.asarray(l)[t, :n].sum(0)[:, None]
+        return out
+    monkeypatch.setattr(oracle, "lse_merge", merge_without_weights)
+    assert pins.check_closed_forms() != [] or pins.check_invariants() != []
