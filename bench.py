@@ -1,0 +1,393 @@
+"""Decode-attention benchmark: µs per decode step and KV-read GB/s on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_ctx] [--impl gb300|reference]
+
+One step = one call of the whole path (split-KV partial kernel + log-sum-exp merge) over the
+workload's batch.  Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (weak scaling; the path needs no exchange).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
+stream, with a 512 MiB device write between steps (outside the events) so every step starts with
+a cold L2; the KV read of the default workload (1.1 GB) is also far larger than the 129 MB L2.
+``value`` = algorithmic bytes per step (KV rows read once per KV head + q + out) / mean step time.
+``e2e`` repeats the step through host buffers: pinned q and kv_len copied in, out copied back.
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded sample per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_decode_attention_03_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attention µs/step and KV-read GB/s (% of GB300 HBM peak), 1 GPU"
+FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _config(case, extra=None):
+    cfg = {"workload": case.name, "n_tok": int(case.n_tok), "n_heads": int(case.n_heads),
+           "n_kv_heads": int(case.n_kv_heads), "head_dim": int(case.head_dim),
+           "cache_cap": int(case.cache_cap), "kv_kind": case.kind,
+           "visited_positions": int(sum(case.visited(t) for t in range(case.n_tok))),
+           "seed": int(case.seed),
+           "l2": "flushed between steps (512 MiB device write outside the events); "
+                 "KV read per step larger than L2"}
+    if case.ids is not None:
+        cfg["budget"] = int(case.budget)
+    cfg.update(extra or {})
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, f in enumerate(fl)
+                          if f.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])),
+                "sm_max_mhz": float(max(r[1] for r in rows)), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _source_hash():
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "gqa_decode_attention_03_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload):
+    """DRAM bytes per launch of the partial kernel from the committed ncu summary, when it was
+    taken on the current kernel sources; otherwise None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        ent = d.get(workload)
+        if ent and ent.get("source_hash") == _source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def _device_inputs(case, torch):
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    t = {"q": d(case.q), "kv_len": d(case.kv_len), "seq_of": d(case.seq_of)}
+    if case.kind == "f16":
+        t.update(k=d(case.k), v=d(case.v))
+    else:
+        t.update(kq=d(case.kq), vq=d(case.vq), ksc=d(case.ksc), vsc=d(case.vsc),
+                 ids=None if case.ids is None else d(case.ids))
+    return t
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+
+    case = W.NAMED[args.workload]()
+    x = _device_inputs(case, torch)
+    T, H, D, Hk = case.n_tok, case.n_heads, case.head_dim, case.n_kv_heads
+    max_len = int(min(case.cache_cap, case.kv_len.max()))
+    kind = gd.KIND_F16 if case.kind == "f16" else gd.KIND_Q8
+    budget = -1 if case.ids is None else int(case.budget)
+    plan = gd.plan(T, H, Hk, D, max_len, budget, kind)
+    ws = gd.alloc_workspace(T, H, Hk, D, max_len, budget, kind)
+    out = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(q=None, kv=None):
+        q = x["q"] if q is None else q
+        kv = x["kv_len"] if kv is None else kv
+        if case.kind == "f16":
+            gd.attn_decode_f16(q, x["k"], x["v"], kv, scale=case.scale, seq_of=x["seq_of"],
+                               max_kv_len=max_len, out=out, ws=ws, stream=stream)
+        else:
+            gd.attn_decode_q8_sel(q, x["kq"], x["vq"], x["ksc"], x["vsc"], kv, ids=x["ids"],
+                                  budget=None if x["ids"] is None else case.budget,
+                                  scale=case.scale, seq_of=x["seq_of"], max_kv_len=max_len,
+                                  out=out, ws=ws, stream=stream)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    if world > 1:
+        torch.distributed.barrier()
+
+    # the merge kernel alone (same partials, L2 as the step leaves it), to isolate the partial
+    # kernel's duration for the roofline
+    merge_ms = 0.0
+    if plan.merge:
+        part = ws[: T * plan.n_split * H * (D + 2) * 4].view(torch.float32).view(
+            T, plan.n_split, H, D + 2)
+        off = -(-part.numel() * 4 // 256) * 256
+        n_valid = ws[off: off + 4 * T].view(torch.int32)
+        evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(K, 500))]
+        for a, b in evm:
+            flush.zero_()
+            step()
+            a.record(stream)
+            gd.attn_merge(part, n_valid, out=out, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        merge_ms = float(np.mean([a.elapsed_time(b) for a, b in evm]))
+
+    # end to end through host buffers: pinned q / kv_len in, out back, every step
+    q_h = torch.from_numpy(case.q).pin_memory()
+    kv_h = torch.from_numpy(case.kv_len).pin_memory()
+    out_h = torch.empty((T, H, D), dtype=torch.float32).pin_memory()
+    q_d, kv_d = torch.empty_like(x["q"]), torch.empty_like(x["kv_len"])
+    Ke = min(K, 500)
+    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ke)]
+    for a, b in eve:
+        flush.zero_()
+        a.record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        kv_d.copy_(kv_h, non_blocking=True)
+        step(q_d, kv_d)
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eve]))
+
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+    alg = case.algorithmic_bytes()
+    peak, peak_src = _peaks()
+    part_ms = ms - merge_ms
+    achieved = alg / (part_ms * 1e-3) / 1e9
+    traffic = _ncu_traffic(case.name)
+    gbs = world * alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s",
+        "us_per_step": round(ms * 1e3, 3), "frac_of_hbm_peak": round(gbs / world / peak, 4),
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded N(0,1) q and f16 K/V, NaN past each sequence's length",
+        "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
+                                 "n_split": plan.n_split, "parallelism": f"replicas x{world}"}),
+        "roofline": {"bound": "hbm", "kernel": "partial_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "partial_us": round(part_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3)},
+        "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_ms * 1e3, 3),
+                "h2d_bytes_per_step": int(case.q.nbytes + case.kv_len.nbytes),
+                "d2h_bytes_per_step": int(T * H * D * 4)},
+        "gpu_launches": int(K * (2 if plan.merge else 1)),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle arms
+
+_CHILD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def _oracle_pair(case, t, g):
+    """The oracle on one (row, KV head) of the case: the G query heads of KV head g."""
+    import oracle
+    G = case.n_heads // case.n_kv_heads
+    q = case.q[t:t + 1, g * G:(g + 1) * G]
+    s = int(case.seq_of[t])
+    L = case.kv_len[t:t + 1]
+    if case.kind == "f16":
+        return oracle.decode_f16(q, case.k[s:s + 1, :, g:g + 1], case.v[s:s + 1, :, g:g + 1], L,
+                                 case.scale, seq_of=[0])
+    ids = None if case.ids is None else case.ids[t:t + 1]
+    return oracle.decode_q8(q, case.kq[s:s + 1, :, g:g + 1], case.vq[s:s + 1, :, g:g + 1],
+                            case.ksc[s:s + 1, :, g:g + 1], case.vsc[s:s + 1, :, g:g + 1], L,
+                            case.scale, seq_of=[0], ids=ids, budget=case.budget)
+
+
+def _pair_bytes(case, t):
+    D = case.head_dim
+    per_pos = 2 * D * 2 if case.kind == "f16" else 2 * (D + 2 * (D // 64))
+    return case.visited(t) * per_pos
+
+
+def _baseline_child(workload, budget_s):
+    """Runs in a single-threaded child process: the oracle over (row, KV head) pairs until about
+    budget_s seconds of work, returning GB/s of KV processed."""
+    case = W.NAMED[workload]()
+    pairs = [(t, g) for t in range(case.n_tok) for g in range(case.n_kv_heads)]
+    done, nbytes, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done < len(pairs):
+        t, g = pairs[done]
+        _oracle_pair(case, t, g)
+        nbytes += _pair_bytes(case, t)
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {len(pairs)} (row, KV head) pairs of {case.name}, "
+                      f"{nbytes / 1e6:.1f} MB of KV in {dt:.1f} s, fp64 numpy, 1 thread"}
+
+
+def cpu_baseline(workload, budget_s=15.0):
+    env = dict(os.environ, **_CHILD_ENV)
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench._baseline_child({workload!r}, {budget_s})))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # the baseline is reported, never required
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {e!r}"[:200]}
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm: each step is one (row, KV head) pair of the
+    workload, cycling through the pairs; rank 0 only."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    for k, v in _CHILD_ENV.items():
+        os.environ.setdefault(k, v)
+    case = W.NAMED[args.workload]()
+    pairs = [(t, g) for t in range(case.n_tok) for g in range(case.n_kv_heads)]
+    for i in range(args.warmup):
+        _oracle_pair(case, *pairs[i % len(pairs)])
+    nbytes, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        t, g = pairs[i % len(pairs)]
+        _oracle_pair(case, t, g)
+        nbytes += _pair_bytes(case, t)
+    dt = time.perf_counter() - t0
+    gbs = nbytes / dt / 1e9
+    sample = (f"{args.steps} steps, each one (row, KV head) pair of {case.name} cycling through "
+              f"{len(pairs)} pairs; fp64 numpy oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded workload as the GPU arm)",
+            "config": _config(case),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="long_ctx", choices=sorted(W.NAMED))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

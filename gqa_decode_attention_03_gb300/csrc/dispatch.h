@@ -1,0 +1,53 @@
+// dispatch.h -- host-side entry points into the kernel instantiations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "gqa_decode.h"
+#include "partial_kernel.cuh"
+
+namespace gqa {
+
+struct Variant {
+  int gw;   // query heads per consumer warp (1, 2 or 4)
+  int nps;  // row slices of a stage (consumer warps per head group)
+};
+
+Variant pick_variant(int group);
+int stage_rows(int kind, int head_dim);
+
+// Defined in the inst_*.cu files, one per (cache kind, head_dim).
+cudaError_t launch_partial_f16_d64(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                   const PartialParams&, dim3, int, cudaStream_t);
+cudaError_t launch_partial_f16_d128(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                    const PartialParams&, dim3, int, cudaStream_t);
+cudaError_t launch_partial_f16_d256(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                    const PartialParams&, dim3, int, cudaStream_t);
+cudaError_t launch_partial_q8_d64(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                  const PartialParams&, dim3, int, cudaStream_t);
+cudaError_t launch_partial_q8_d128(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                   const PartialParams&, dim3, int, cudaStream_t);
+cudaError_t launch_partial_q8_d256(Variant v, const CUtensorMap&, const CUtensorMap&,
+                                   const PartialParams&, dim3, int, cudaStream_t);
+
+inline cudaError_t launch_partial(int kind, int head_dim, Variant v, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const PartialParams& p, dim3 grid,
+                                  int threads, cudaStream_t s) {
+  if (kind == GQA_KIND_F16) {
+    if (head_dim == 64) return launch_partial_f16_d64(v, tk, tv, p, grid, threads, s);
+    if (head_dim == 128) return launch_partial_f16_d128(v, tk, tv, p, grid, threads, s);
+    return launch_partial_f16_d256(v, tk, tv, p, grid, threads, s);
+  }
+  if (head_dim == 64) return launch_partial_q8_d64(v, tk, tv, p, grid, threads, s);
+  if (head_dim == 128) return launch_partial_q8_d128(v, tk, tv, p, grid, threads, s);
+  return launch_partial_q8_d256(v, tk, tv, p, grid, threads, s);
+}
+
+cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,
+                         int n_tok, int n_heads, float* out, cudaStream_t s);
+
+// Raises the function's dynamic shared-memory limit once per (function, device).
+cudaError_t ensure_smem(const void* fn, int bytes);
+
+}  // namespace gqa

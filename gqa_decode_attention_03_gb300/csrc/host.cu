@@ -1,0 +1,321 @@
+// host.cu -- the C ABI of libgqadecode.so: argument checks, the split planner, TMA descriptors,
+// and kernel dispatch.  Nothing here allocates device memory or synchronises; every launch goes
+// to the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <string>
+#include <utility>
+
+#include "dispatch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gqa_status fail(gqa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+gqa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GQA_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// SM count of the current device, cached per device id.
+int current_sm_count(gqa_status* st) {
+  static std::mutex mu;
+  static int cache[128] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *st = cuda_fail(e, "cudaGetDevice");
+    return -1;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    *st = cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+    return -1;
+  }
+  if (dev >= 0 && dev < 128) cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+constexpr int kCtasPerSmTarget = 8;  // partial-kernel CTAs per SM the planner aims for
+
+// Shapes that do not depend on the device.
+gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
+                       int kind) {
+  if (kind != GQA_KIND_F16 && kind != GQA_KIND_Q8) return fail(GQA_EINVAL, "kind must be 0 or 1");
+  if (n_tok < 0 || n_tok > 65535) return fail(GQA_EINVAL, "n_tok %d outside [0, 65535]", n_tok);
+  if (n_heads <= 0 || n_kv_heads <= 0 || n_kv_heads > 65535)
+    return fail(GQA_EINVAL, "n_heads %d / n_kv_heads %d", n_heads, n_kv_heads);
+  if (n_heads % n_kv_heads)
+    return fail(GQA_EINVAL, "n_heads %d is not a multiple of n_kv_heads %d", n_heads, n_kv_heads);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(GQA_EINVAL, "head_dim %d not in {64, 128, 256}", head_dim);
+  if (max_kv_len < 0) return fail(GQA_EINVAL, "max_kv_len %d < 0", max_kv_len);
+  if (n_heads / n_kv_heads > 16)
+    return fail(GQA_EUNSUPPORTED, "group size %d > 16", n_heads / n_kv_heads);
+  return GQA_OK;
+}
+
+}  // namespace
+
+namespace gqa {
+
+Variant pick_variant(int group) {
+  if (group <= 4) return Variant{group <= 1 ? 1 : (group <= 2 ? 2 : 4), 4};
+  return Variant{4, 2};
+}
+
+int stage_rows(int kind, int head_dim) {
+  if (kind == GQA_KIND_F16) return head_dim == 64 ? 128 : (head_dim == 128 ? 64 : 32);
+  return head_dim == 256 ? 64 : 128;
+}
+
+}  // namespace gqa
+
+extern "C" {
+
+int gqa_abi_version(void) { return GQA_ABI_VERSION; }
+
+const char* gqa_last_error(void) { return g_last_error.c_str(); }
+
+const char* gqa_status_string(gqa_status s) {
+  switch (s) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_EINVAL: return "GQA_EINVAL";
+    case GQA_EWORKSPACE: return "GQA_EWORKSPACE";
+    case GQA_EUNSUPPORTED: return "GQA_EUNSUPPORTED";
+    case GQA_ECUDA: return "GQA_ECUDA";
+  }
+  return "GQA_UNKNOWN";
+}
+
+gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
+                            int budget, int kind, int num_sms, gqa_plan* plan) {
+  if (!plan) return fail(GQA_EINVAL, "plan is NULL");
+  std::memset(plan, 0, sizeof *plan);
+  gqa_status st = check_shape(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, kind);
+  if (st != GQA_OK) return st;
+  if (kind == GQA_KIND_F16) budget = -1;
+  if (budget == 0 || budget < -1) return fail(GQA_EINVAL, "budget %d (use -1 for dense)", budget);
+  if (num_sms <= 0) {
+    st = GQA_OK;
+    num_sms = current_sm_count(&st);
+    if (num_sms <= 0) return st != GQA_OK ? st : fail(GQA_ECUDA, "no SM count");
+  }
+  const int tile = gqa::stage_rows(kind, head_dim);
+  const long long nmax = budget > 0 ? std::min(max_kv_len, budget) : max_kv_len;
+  // Equal chunks sized so that the CTAs over all (row, KV head) pairs come to about
+  // kCtasPerSmTarget per SM (several waves of the 1-2 CTAs an SM holds), rounded to whole tiles.
+  const long long units = (long long)n_tok * n_kv_heads * std::max(nmax, 1LL);
+  long long chunk = (units + (long long)kCtasPerSmTarget * num_sms - 1) /
+                    ((long long)kCtasPerSmTarget * num_sms);
+  const int forced = env_int("GQA_FORCE_CHUNK");
+  if (forced > 0) chunk = forced;
+  chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;
+  const long long whole = (std::max(nmax, 1LL) + tile - 1) / tile * tile;
+  if (chunk > whole) chunk = whole;
+  const long long n_split = std::max(1LL, (nmax + chunk - 1) / chunk);
+  if (n_split > (1LL << 30)) return fail(GQA_EUNSUPPORTED, "too many chunks");
+  plan->chunk = (int)chunk;
+  plan->n_split = (int)n_split;
+  plan->tile = tile;
+  plan->grid_x = (int)n_split;
+  plan->grid_y = n_kv_heads;
+  plan->grid_z = n_tok;
+  plan->merge = n_split > 1 ? 1 : 0;
+  if (plan->merge) {
+    const size_t part = (size_t)n_tok * n_split * n_heads * (head_dim + 2) * sizeof(float);
+    plan->ws_bytes = (part + 255) / 256 * 256 + (size_t)n_tok * sizeof(int32_t);
+  }
+  return GQA_OK;
+}
+
+size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int head_dim,
+                                   int max_kv_len, int budget, int kind) {
+  gqa_plan plan;
+  if (attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind, 0, &plan) !=
+      GQA_OK)
+    return 0;
+  return plan.ws_bytes;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of the two decode entry points.
+gqa_status decode_common(int kind, const float* q, const void* kc, const void* vc,
+                         const uint16_t* ksc, const uint16_t* vsc, const int32_t* ids, int budget,
+                         float* out, const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                         int n_seq, int n_heads, int n_kv_heads, int head_dim, int64_t cache_cap,
+                         int max_kv_len, float scale, void* ws, size_t ws_bytes,
+                         int32_t* err_word, cudaStream_t stream) {
+  gqa_status st = check_shape(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, kind);
+  if (st != GQA_OK) return st;
+  if (n_tok == 0) return GQA_OK;
+  if (!q || !kc || !vc || !out || !kv_len) return fail(GQA_EINVAL, "a required pointer is NULL");
+  if (kind == GQA_KIND_Q8 && (!ksc || !vsc)) return fail(GQA_EINVAL, "scale pointer is NULL");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(kc) || !aligned16(vc))
+    return fail(GQA_EINVAL, "q, out and the caches must be 16-byte aligned");
+  if (kind == GQA_KIND_Q8 && head_dim >= 128 && (!aligned16(ksc) || !aligned16(vsc)))
+    return fail(GQA_EINVAL, "scales must be 16-byte aligned");
+  if (n_seq <= 0 || cache_cap <= 0) return fail(GQA_EINVAL, "n_seq and cache_cap must be > 0");
+  if ((int64_t)n_seq * cache_cap > INT32_MAX)
+    return fail(GQA_EUNSUPPORTED, "n_seq * cache_cap must stay below 2^31 rows");
+  if (!seq_of && n_seq < n_tok) return fail(GQA_EINVAL, "seq_of NULL needs n_seq >= n_tok");
+  if (!std::isfinite(scale)) return fail(GQA_EINVAL, "scale is not finite");
+  if (ids && budget <= 0) return fail(GQA_EINVAL, "budget must be >= 1 with ids");
+  const int max_len = (int)std::min<int64_t>(max_kv_len, cache_cap);
+
+  gqa_plan plan;
+  st = attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_len, ids ? budget : -1, kind, 0,
+                        &plan);
+  if (st != GQA_OK) return st;
+  if (plan.merge && (!ws || ws_bytes < plan.ws_bytes || !aligned16(ws)))
+    return fail(GQA_EWORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu",
+                plan.ws_bytes, ws ? ws_bytes : (size_t)0);
+
+  gqa::PartialParams p{};
+  p.q = q;
+  p.kc = kc;
+  p.vc = vc;
+  p.ksc = reinterpret_cast<const __half*>(ksc);
+  p.vsc = reinterpret_cast<const __half*>(vsc);
+  p.ids = ids;
+  p.kv_len = kv_len;
+  p.seq_of = seq_of;
+  p.out = out;
+  p.err = err_word;
+  p.n_tok = n_tok;
+  p.n_seq = n_seq;
+  p.n_heads = n_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.group = n_heads / n_kv_heads;
+  p.cache_cap = cache_cap;
+  p.max_kv_len = max_len;
+  p.budget = ids ? budget : INT32_MAX;
+  p.chunk = plan.chunk;
+  p.n_split = plan.n_split;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.merge = plan.merge;
+  if (plan.merge) {
+    p.part = static_cast<float*>(ws);
+    const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);
+    p.n_valid = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + (part + 255) / 256 * 256);
+  }
+
+  CUtensorMap tk, tv;
+  std::memset(&tk, 0, sizeof tk);
+  std::memset(&tv, 0, sizeof tv);
+  if (kind == GQA_KIND_F16) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return fail(GQA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_heads,
+                                (cuuint64_t)n_seq * (cuuint64_t)cache_cap};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2,
+                                   (cuuint64_t)head_dim * 2 * (cuuint64_t)n_kv_heads};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)plan.tile};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int i = 0; i < 2; ++i) {
+      CUresult r = encode(i ? &tv : &tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void*>(i ? vc : kc), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(GQA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+  }
+
+  const gqa::Variant var = gqa::pick_variant(p.group);
+  const int nhg = (p.group + var.gw - 1) / var.gw;
+  const int threads = 32 * (nhg * var.nps + 1);
+  const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
+  cudaError_t e = gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
+  if (plan.merge) {
+    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  }
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status attn_decode_f16(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           float* out, const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                           int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                           int64_t cache_cap, int max_kv_len, float scale, void* ws,
+                           size_t ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  return decode_common(GQA_KIND_F16, q, k_cache, v_cache, nullptr, nullptr, nullptr, -1, out,
+                       kv_len, seq_of, n_tok, n_seq, n_heads, n_kv_heads, head_dim, cache_cap,
+                       max_kv_len, scale, ws, ws_bytes, err_word, stream);
+}
+
+gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq,
+                              const uint16_t* ksc, const uint16_t* vsc, const int32_t* ids,
+                              int budget, float* out, const int32_t* kv_len,
+                              const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                              int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                              float scale, void* ws, size_t ws_bytes, int32_t* err_word,
+                              cudaStream_t stream) {
+  return decode_common(GQA_KIND_Q8, q, kq, vq, ksc, vsc, ids, budget, out, kv_len, seq_of, n_tok,
+                       n_seq, n_heads, n_kv_heads, head_dim, cache_cap, max_kv_len, scale, ws,
+                       ws_bytes, err_word, stream);
+}
+
+gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, int n_tok,
+                      int n_heads, int head_dim, float* out, cudaStream_t stream) {
+  if (n_tok < 0 || n_tok > 65535 || n_heads <= 0 || n_heads > 65535 || n_split <= 0)
+    return fail(GQA_EINVAL, "bad sizes n_tok %d n_heads %d n_split %d", n_tok, n_heads, n_split);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(GQA_EINVAL, "head_dim %d not in {64, 128, 256}", head_dim);
+  if (n_tok == 0) return GQA_OK;
+  if (!part || !n_valid || !out) return fail(GQA_EINVAL, "a required pointer is NULL");
+  if (!aligned16(part) || !aligned16(out)) return fail(GQA_EINVAL, "part/out not 16-byte aligned");
+  cudaError_t e = gqa::launch_merge(head_dim, part, n_valid, n_split, n_tok, n_heads, out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// inst_q8_d256.cu -- partial-kernel instantiations for int8 caches with f16 scales (cp.async gather), head_dim 256.
+#include "dispatch.h"
+
+namespace gqa {
+
+template <Kind K, int D, int GW, int NPS>
+static cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& p,
+                              dim3 grid, int threads, cudaStream_t s) {
+  using C = Cfg<K, D, GW, NPS>;
+  const void* fn = reinterpret_cast<const void*>(&partial_kernel<K, D, GW, NPS>);
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (threads > C::MAX_THREADS) return cudaErrorInvalidConfiguration;
+  partial_kernel<K, D, GW, NPS><<<grid, threads, C::SMEM_BYTES, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_partial_q8_d256(Variant v, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const PartialParams& p, dim3 grid, int threads,
+                                    cudaStream_t s) {
+  constexpr Kind K = Kind::Q8;
+  if (v.nps == 4) {
+    if (v.gw == 1) return launch_one<K, 256, 1, 4>(tk, tv, p, grid, threads, s);
+    if (v.gw == 2) return launch_one<K, 256, 2, 4>(tk, tv, p, grid, threads, s);
+    return launch_one<K, 256, 4, 4>(tk, tv, p, grid, threads, s);
+  }
+  return launch_one<K, 256, 4, 2>(tk, tv, p, grid, threads, s);
+}
+
+}  // namespace gqa

@@ -1,0 +1,199 @@
+"""ctypes binding of libgqadecode.so (argument marshalling only).
+
+Every function here checks dtypes, shapes, devices and contiguity of torch tensors, then passes
+``data_ptr()`` values and the current CUDA stream to the C ABI declared in
+``include/gqa_decode.h``.  All arithmetic happens in the library's CUDA kernels; there is no
+fallback of any kind: importing this module raises if the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "lib" / "libgqadecode.so"
+
+GQA_OK, GQA_EINVAL, GQA_EWORKSPACE, GQA_EUNSUPPORTED, GQA_ECUDA = range(5)
+KIND_F16, KIND_Q8 = 0, 1
+ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+# Every symbol the header declares (checked by the CPU test suite).
+EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
+           "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
+           "gqa_abi_version")
+
+
+class GqaPlan(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int), ("n_split", ctypes.c_int), ("tile", ctypes.c_int),
+                ("grid_x", ctypes.c_int), ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
+                ("merge", ctypes.c_int), ("ws_bytes", ctypes.c_size_t)]
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{status}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not _LIB_PATH.exists():
+        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                          "`python -m gqa_decode_attention_03_gb300.build_lib`")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.attn_decode_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(GqaPlan)]
+    lib.attn_decode_plan.restype = I
+    lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.attn_decode_workspace_bytes.restype = SZ
+    lib.attn_decode_f16.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I64, I, F, P, SZ, P, P]
+    lib.attn_decode_f16.restype = I
+    lib.attn_decode_q8_sel.argtypes = [P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I64, I, F, P,
+                                       SZ, P, P]
+    lib.attn_decode_q8_sel.restype = I
+    lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
+    lib.attn_merge.restype = I
+    lib.gqa_status_string.argtypes = [I]
+    lib.gqa_status_string.restype = ctypes.c_char_p
+    lib.gqa_last_error.argtypes = []
+    lib.gqa_last_error.restype = ctypes.c_char_p
+    lib.gqa_abi_version.argtypes = []
+    lib.gqa_abi_version.restype = I
+    return lib
+
+
+LIB = _load()
+
+
+def _check(status):
+    if status != GQA_OK:
+        raise GqaError(LIB.gqa_status_string(status).decode(), LIB.gqa_last_error().decode())
+
+
+def _ptr(x):
+    return None if x is None else ctypes.c_void_p(x.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(x, dtype, name, ndim=None):
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and x.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {x.dim()}")
+
+
+def plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16, num_sms=0):
+    """The split plan the decode calls use (host only; num_sms 0 queries the device)."""
+    p = GqaPlan()
+    _check(LIB.attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind,
+                                num_sms, ctypes.byref(p)))
+    return p
+
+
+def workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16):
+    return int(LIB.attn_decode_workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len,
+                                               budget, kind))
+
+
+def alloc_workspace(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16,
+                    device=None):
+    n = workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv_len=None,
+                    out=None, ws=None, err=None, stream=None):
+    """Decode attention over an f16 cache; returns ``out [T][H][D]`` fp32.
+
+    q [T][H][D] fp32; k_cache, v_cache [n_seq][cap][Hk][D] fp16; kv_len [T] int32 (device);
+    seq_of [T] int32 or None; max_kv_len: host bound of kv_len (default: the cache capacity).
+    """
+    _need(q, torch.float32, "q", 3)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(kv_len, torch.int32, "kv_len", 1)
+    if seq_of is not None:
+        _need(seq_of, torch.int32, "seq_of", 1)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    T, H, D = q.shape
+    n_seq, cap, Hk, Dk = k_cache.shape
+    if Dk != D or kv_len.numel() != T:
+        raise ValueError("shape mismatch between q, caches and kv_len")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_kv_len = cap if max_kv_len is None else int(max_kv_len)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", 3)
+    if ws is None:
+        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_F16, q.device)
+    _check(LIB.attn_decode_f16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(kv_len),
+                               _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale, _ptr(ws),
+                               ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    return out
+
+
+def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale=None,
+                       seq_of=None, max_kv_len=None, out=None, ws=None, err=None, stream=None):
+    """Decode attention over an int8 cache with per-64-dim f16 scales; optional selected ids.
+
+    kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/64] fp16; ids [T][budget] int32.
+    """
+    _need(q, torch.float32, "q", 3)
+    _need(kq, torch.int8, "kq", 4)
+    _need(vq, torch.int8, "vq", 4)
+    _need(ksc, torch.float16, "ksc", 4)
+    _need(vsc, torch.float16, "vsc", 4)
+    _need(kv_len, torch.int32, "kv_len", 1)
+    if seq_of is not None:
+        _need(seq_of, torch.int32, "seq_of", 1)
+    if ids is not None:
+        _need(ids, torch.int32, "ids", 2)
+        budget = ids.shape[1] if budget is None else int(budget)
+        if budget > ids.shape[1]:
+            raise ValueError("budget exceeds the id list width")
+        if ids.shape[1] != budget:
+            raise ValueError("ids must be [n_tok][budget]")
+    T, H, D = q.shape
+    n_seq, cap, Hk, Dk = kq.shape
+    if Dk != D or kv_len.numel() != T or ksc.shape != (n_seq, cap, Hk, D // 64):
+        raise ValueError("shape mismatch between q, caches, scales and kv_len")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_kv_len = cap if max_kv_len is None else int(max_kv_len)
+    b = -1 if ids is None else budget
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", 3)
+    if ws is None:
+        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), b, KIND_Q8, q.device)
+    _check(LIB.attn_decode_q8_sel(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), _ptr(ids),
+                                  0 if ids is None else budget, _ptr(out), _ptr(kv_len),
+                                  _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale,
+                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
+                                  _stream(stream)))
+    return out
+
+
+def attn_merge(part, n_valid, out=None, stream=None):
+    """LSE merge of partials ``part [T][S][H][D+2]`` over the first n_valid[t] chunks."""
+    _need(part, torch.float32, "part", 4)
+    _need(n_valid, torch.int32, "n_valid", 1)
+    T, S, H, D2 = part.shape
+    D = D2 - 2
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.float32, device=part.device)
+    _need(out, torch.float32, "out", 3)
+    _check(LIB.attn_merge(_ptr(part), _ptr(n_valid), S, T, H, D, _ptr(out), _stream(stream)))
+    return out

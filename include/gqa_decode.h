@@ -1,0 +1,168 @@
+/*
+ * gqa_decode.h -- C ABI of libgqadecode.so: single-query (decode-step) grouped-query attention
+ * over a KV cache on NVIDIA GB300 (sm_103a), with split-KV flash-decode partials merged by
+ * log-sum-exp.
+ *
+ * What is computed (for query row t, query head h; G = n_heads / n_kv_heads):
+ *   g = h / G                        the KV head serving h's group    (attention_gqa.metal,
+ *                                     cera 0.5.4: one KV head per group of query heads)
+ *   s = seq_of[t]                    which sequence's cache the row reads
+ *   J = 0 .. kv_len[t]-1             dense decode, or the first min(kv_len[t], budget) entries
+ *                                     of ids[t]                        (qsa2.metal, qsa_attn2)
+ *   x_j = scale * q[t][h] . K^[s][j][g]
+ *   out[t][h] = sum_j softmax(x)_j * V^[s][j][g]      (attention_gqa.metal phases 1-3;
+ *                                     flash_attention.metal, cera 0.2.0, in one online pass)
+ *   kv_len[t] == 0 (or an empty id list) gives out[t][h] = 0   (flash_attention.metal, the
+ *                                     seq_len == 0 guard)
+ * K^/V^ are the cache rows dequantised: f16 widened to fp32, or int8 times the f16 scale of its
+ * 64-dim group (qsa2.metal, qsa_attn2).
+ *
+ * Conventions shared by every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library never allocates,
+ *     frees or synchronises; work is enqueued on `stream` (0 = the legacy default stream) and
+ *     runs asynchronously.  Calls are thread-safe; gqa_last_error() is per host thread.
+ *   - Layouts are dense, row-major, innermost dimension last:
+ *       q      [n_tok][n_heads][head_dim]                      fp32
+ *       out    [n_tok][n_heads][head_dim]                      fp32
+ *       f16 K/V cache   [n_seq][cache_cap][n_kv_heads][head_dim]   IEEE binary16 bit patterns
+ *       int8 K/V cache  [n_seq][cache_cap][n_kv_heads][head_dim]   int8
+ *       int8 scales     [n_seq][cache_cap][n_kv_heads][head_dim/64] binary16
+ *       kv_len [n_tok] int32: positions row t attends to (decode: the sequence length; a causal
+ *              prefill row at position p: p + 1 -- flash_attention_tq.metal, cera 0.4.0)
+ *       seq_of [n_tok] int32 or NULL (NULL: row t reads sequence t, which needs n_seq >= n_tok)
+ *       ids    [n_tok][budget] int32 cell positions or NULL (NULL: dense 0..kv_len[t]-1)
+ *       part   [n_tok][n_split][n_heads][head_dim + 2] fp32: unnormalised acc[head_dim], then
+ *              the chunk's max score m (natural-log units), then its sum l  (qsa2.metal,
+ *              qsa_attn2's partial layout)
+ *   - Alignment: q, out, caches, scales and part must be 16-byte aligned (TMA and vector loads).
+ *   - Errors: a gqa_status is returned; nothing is launched unless it is GQA_OK.  Data-dependent
+ *     faults are never traps: kernels clamp and OR a bit into *err_word (device int32, may be
+ *     NULL to ignore them); see GQA_ERR_*.  err_word is not cleared by the library.
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_ABI_VERSION 1
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_EINVAL = 1,       /* null or misaligned pointer, bad size, n_heads % n_kv_heads != 0,
+                           head_dim not in {64, 128, 256}, non-finite scale, bad budget */
+  GQA_EWORKSPACE = 2,   /* ws is NULL or smaller than attn_decode_workspace_bytes() */
+  GQA_EUNSUPPORTED = 3, /* a valid request this build does not serve (group size > 16) */
+  GQA_ECUDA = 4         /* a CUDA runtime/driver call failed; gqa_last_error() has the text */
+} gqa_status;
+
+/* Bits OR-ed into *err_word by the kernels (device side, never a trap). */
+#define GQA_ERR_KVLEN_RANGE 0x1 /* kv_len[t] < 0 or > cache_cap: clamped into [0, cache_cap] */
+#define GQA_ERR_ID_RANGE 0x2    /* an id outside [0, kv_len[t]): that cell is skipped */
+#define GQA_ERR_SEQ_RANGE 0x4   /* seq_of[t] outside [0, n_seq): the row writes zeros */
+#define GQA_ERR_TIMEOUT 0x8     /* a pipeline wait passed its iteration limit; CTA gave up */
+
+/* Kinds for the planner and the workspace query. */
+#define GQA_KIND_F16 0
+#define GQA_KIND_Q8 1
+
+/* The split plan the decode calls use (exposed so hosts and tests can inspect it). */
+typedef struct gqa_plan {
+  int chunk;         /* positions (or selected cells) per KV chunk, a multiple of tile */
+  int n_split;       /* chunks per row at max_kv_len: ceil(min(max_kv_len, budget) / chunk) */
+  int tile;          /* positions staged in shared memory per pipeline stage */
+  int grid_x, grid_y, grid_z; /* launch grid of the partial kernel: (n_split, KV heads x head
+                                 groups, n_tok) */
+  int merge;         /* 1 when partials are written to ws and merged by a second kernel */
+  size_t ws_bytes;   /* workspace the call needs (0 when merge == 0) */
+} gqa_plan;
+
+/*
+ * attn_decode_plan -- the split planner (host only; launches nothing, needs no GPU).
+ * Chooses the chunk length so that the partial kernel's CTA count is a few waves of the SM
+ * count, with every chunk but a row's last the same length (qsa2.metal chunks its id list in
+ * fixed 32-cell pieces; FORWARD_MSL's split-T decode uses fixed 512-position partial blocks).
+ * num_sms <= 0 queries the current CUDA device.  budget < 0 means dense (no id list).
+ * Returns GQA_EINVAL on bad sizes, GQA_EUNSUPPORTED for group sizes > 16.
+ */
+gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim,
+                            int max_kv_len, int budget, int kind, int num_sms, gqa_plan* plan);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of `ws` that attn_decode_f16 (kind GQA_KIND_F16) or
+ * attn_decode_q8_sel (GQA_KIND_Q8) needs for these sizes on the current device; 0 when no
+ * split is needed or the sizes are invalid.  The figure is n_tok * n_split * n_heads *
+ * (head_dim + 2) * 4 bytes.
+ */
+size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int head_dim,
+                                   int max_kv_len, int budget, int kind);
+
+/*
+ * attn_decode_f16 -- decode attention over an f16 K/V cache.
+ * Passages: attention_gqa.metal (cera 0.5.4) for the grouped math and the load-once-per-group
+ * structure; flash_attention.metal (cera 0.2.0) for the online softmax and the empty-context
+ * rule; qsa2.metal (regolith) qsa_attn2 / qsa_merge2 for the split partials and their merge.
+ *   q, out        see layouts; out is fully written (zeros for empty rows)
+ *   k_cache, v_cache  f16 caches, n_seq * cache_cap * n_kv_heads * head_dim elements each
+ *   kv_len        device [n_tok]; seq_of device [n_tok] or NULL
+ *   max_kv_len    host upper bound of kv_len[] (sizes the grid; rows longer than it are
+ *                 truncated to it and flagged GQA_ERR_KVLEN_RANGE)
+ *   scale         multiplies q.k (finite)
+ *   ws, ws_bytes  caller scratch of >= attn_decode_workspace_bytes(..., GQA_KIND_F16) bytes,
+ *                 16-byte aligned (may be NULL when that figure is 0)
+ *   err_word      device int32 or NULL
+ */
+gqa_status attn_decode_f16(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           float* out, const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                           int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                           int64_t cache_cap, int max_kv_len, float scale, void* ws,
+                           size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * attn_decode_q8_sel -- decode attention over an int8 K/V cache with one f16 scale per 64 dims,
+ * visiting either every position (ids == NULL) or the first min(kv_len[t], budget) entries of
+ * the row's selected-cell list ids[t][0..budget).
+ * Passages: qsa2.metal (regolith), qsa_attn2 / qsa_attn3 (dequantisation, selected width,
+ * chunked partials) and qsa_merge2 (merge; its sigmoid output gate is not part of this call).
+ *   kq, vq        int8 caches; ksc, vsc binary16 scales (layouts above); head_dim in {64,128,256}
+ *   ids, budget   device [n_tok][budget] int32 or NULL; budget >= 1 when ids != NULL
+ *   an id outside [0, kv_len[t]) is skipped and flagged GQA_ERR_ID_RANGE
+ *   other arguments as attn_decode_f16 (workspace kind GQA_KIND_Q8, same budget)
+ */
+gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq,
+                              const uint16_t* ksc, const uint16_t* vsc, const int32_t* ids,
+                              int budget, float* out, const int32_t* kv_len,
+                              const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                              int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                              float scale, void* ws, size_t ws_bytes, int32_t* err_word,
+                              cudaStream_t stream);
+
+/*
+ * attn_merge -- log-sum-exp merge of split partials (qsa2.metal, qsa_merge2; FORWARD_MSL's
+ * attn_combine is the same merge in exp2 units):
+ *   M = max_c m_c,  e_c = exp(m_c - M),  L = sum_c l_c e_c,  out = sum_c acc_c e_c / L
+ * over chunks c < n_valid[t] of row t (n_valid device [n_tok], values clamped to [0, n_split]);
+ * a row with n_valid 0 (or L == 0) gets zeros.  part as in the layouts, head_dim in {64,128,256}.
+ */
+gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, int n_tok,
+                      int n_heads, int head_dim, float* out, cudaStream_t stream);
+
+/* Human-readable name of a status; static storage. */
+const char* gqa_status_string(gqa_status s);
+
+/* Text of the last error on this host thread ("" if none); valid until the next call. */
+const char* gqa_last_error(void);
+
+/* GQA_ABI_VERSION of the loaded library. */
+int gqa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (TOL_F16, TOL_Q8, assert_close, dev, forced_chunk, oracle_ref, run_case,
+                      tol_of)
+from gqa_decode_attention_03_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _gd():
+    from gqa_decode_attention_03_gb300 import gqa_decode
+    return gqa_decode
+
+
+# ----------------------------------------------------------------------------- named workloads
+
+@pytest.mark.parametrize("name", ["tiny", "gqa_d64_L1024", "gqa_d64_L4096"])
+def test_small_named_workloads(name):
+    case = W.NAMED[name]()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err).cpu().numpy()
+    assert_close(got, oracle_ref(case), tol_of(case), name)
+    assert int(err.item()) == 0
+
+
+def test_long_context_all_rows():
+    """16 sequences, lengths U[1024, 32768], H=32, Hk=8, D=128: every output element."""
+    case = W.long_context()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err, max_kv_len=int(case.kv_len.max())).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, "long_ctx")
+    assert int(err.item()) == 0
+
+
+def test_q8_selected_workload():
+    """int8 KV, 48 heads over 4 KV heads, D=256, 1024 sorted ids out of 8192."""
+    case = W.q8_selected()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, "q8_sel")
+    assert int(err.item()) == 0
+
+
+def test_batched_sampled_rows():
+    """64 x 8192 batch: the full GPU launch, checked on sampled rows the oracle computes."""
+    case = W.batched()
+    got = run_case(case).cpu().numpy()
+    rows = [0, 1, 17, 42, 62, 63]
+    assert_close(got[rows], oracle_ref(case, rows=rows), TOL_F16, "batched")
+    assert np.isfinite(got).all()
+
+
+def test_prefill_chunk_rows():
+    """16 causal rows at 8176.. of one sequence (row r sees 8177 + r positions)."""
+    case = W.prefill_chunk()
+    got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, "prefill_chunk")
+
+
+# ----------------------------------------------------------------------------- shape sweep
+
+SHAPES = [(D, G) for D in (64, 128, 256) for G in (1, 2, 3, 4, 6, 8, 12, 16)]
+
+
+@pytest.mark.parametrize("chunk", [None, 64, 128])
+@pytest.mark.parametrize("D,G", SHAPES)
+def test_f16_shapes(D, G, chunk):
+    # rows: ragged lengths over several tiles, a one-position row, an empty row; 2 KV heads
+    case = W.make_f16_case(100 + D + G, 4, 2 * G, 2, D, [300, 1, 0, 133], cache_cap=320,
+                           scale=1 / math.sqrt(D))
+    with forced_chunk(chunk):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, f"f16 D{D} G{G} chunk{chunk}")
+    assert (got[2] == 0).all()
+
+
+@pytest.mark.parametrize("chunk", [None, 128])
+@pytest.mark.parametrize("D,G", SHAPES)
+def test_q8_shapes_with_ids(D, G, chunk):
+    case = W.make_q8_case(200 + D + G, 3, 2 * G, 2, D, [700, 5, 260], budget=300, cache_cap=720,
+                          scale=1 / math.sqrt(D))
+    with forced_chunk(chunk):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, f"q8 D{D} G{G} chunk{chunk}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_q8_dense(D):
+    case = W.make_q8_case(300 + D, 2, 8, 2, D, [333, 129], cache_cap=400, scale=0.05)
+    got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, f"q8 dense D{D}")
+
+
+# ----------------------------------------------------------------------------- properties
+
+def test_gather_is_bit_exact():
+    """q8_sel(cache, ids) == q8_sel(cache gathered by ids, ids = iota), bit for bit."""
+    case = W.make_q8_case(401, 2, 24, 2, 256, [3000, 2500], budget=1024, cache_cap=3000,
+                          scale=1 / 16)
+    got = run_case(case, max_kv_len=3000).cpu().numpy()
+    g = W.make_q8_case(402, 2, 24, 2, 256, [1024, 1024], cache_cap=1024, scale=1 / 16)
+    for t in range(2):
+        J = case.ids[t]
+        g.kq[t], g.vq[t] = case.kq[t, J], case.vq[t, J]
+        g.ksc[t], g.vsc[t] = case.ksc[t, J], case.vsc[t, J]
+    g.q = case.q
+    iota = dev(np.tile(np.arange(1024, dtype=np.int32), (2, 1)))
+    g.budget = 1024
+    got2 = run_case(g, ids=iota, max_kv_len=1024).cpu().numpy()
+    assert np.array_equal(got, got2)
+
+
+def test_split_matches_unsplit_and_is_deterministic():
+    case = W.make_f16_case(403, 3, 16, 4, 128, [5000, 64, 3001], cache_cap=5000, scale=0.09)
+    with forced_chunk(100000):
+        one = run_case(case).cpu().numpy()
+    with forced_chunk(64):
+        many = run_case(case).cpu().numpy()
+        again = run_case(case).cpu().numpy()
+    assert np.array_equal(many, again)
+    ref = oracle_ref(case)
+    assert_close(one, ref, TOL_F16, "one chunk")
+    assert_close(many, ref, TOL_F16, "64-row chunks")
+
+
+def test_rows_sharing_a_sequence():
+    case = W.make_f16_case(404, 5, 8, 2, 64, [50, 700, 699, 1, 700], cache_cap=700,
+                           seq_of=[1, 0, 0, 1, 1], n_seq=2, scale=0.125)
+    got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, "shared sequences")
+
+
+# ----------------------------------------------------------------------------- error paths
+
+def test_out_of_range_ids_are_skipped_and_flagged():
+    case = W.make_q8_case(405, 1, 8, 2, 128, [400], budget=64, cache_cap=500, scale=0.1)
+    case.ids[0, 5] = 450    # >= kv_len
+    case.ids[0, 9] = -3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err).cpu().numpy()
+    assert int(err.item()) & _gd().ERR_ID_RANGE
+    J = [int(x) for x in case.ids[0] if 0 <= x < 400]
+    ref = oracle.decode_q8(case.q, case.kq, case.vq, case.ksc, case.vsc, case.kv_len, case.scale,
+                           ids=np.array([J]), budget=len(J))
+    assert_close(got, ref, TOL_Q8, "skipped ids")
+
+
+def test_kv_len_past_capacity_is_clamped_and_flagged():
+    case = W.make_f16_case(406, 2, 4, 1, 64, [100, 90], cache_cap=100, scale=0.125)
+    kv = case.kv_len.copy()
+    case.kv_len[0] = 1000    # claims more than the cache holds
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err, max_kv_len=100).cpu().numpy()
+    assert int(err.item()) & _gd().ERR_KVLEN_RANGE
+    case.kv_len = kv
+    assert_close(got, oracle_ref(case), TOL_F16, "clamped")
+
+
+def test_bad_sequence_index_gives_zeros_and_flag():
+    case = W.make_f16_case(407, 2, 4, 1, 64, [10, 10], cache_cap=16, seq_of=[0, 0], n_seq=1)
+    case.seq_of = np.array([0, 5], dtype=np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_case(case, err=err).cpu().numpy()
+    assert int(err.item()) & _gd().ERR_SEQ_RANGE
+    assert (got[1] == 0).all()
+    case.q, case.kv_len, case.seq_of = case.q[:1], case.kv_len[:1], case.seq_of[:1]
+    assert_close(got[:1], oracle_ref(case), TOL_F16, "row 0")
+
+
+def test_workspace_too_small_is_refused():
+    gd = _gd()
+    case = W.make_f16_case(408, 1, 4, 1, 64, [5000], cache_cap=5000)
+    with forced_chunk(128):
+        with pytest.raises(gd.GqaError, match="EWORKSPACE"):
+            gd.attn_decode_f16(dev(case.q), dev(case.k), dev(case.v), dev(case.kv_len),
+                               ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
+
+
+# ----------------------------------------------------------------------------- merge entry point
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_merge_entry_point(D):
+    rng = np.random.default_rng(D)
+    T, S, H = 3, 7, 5
+    acc = rng.standard_normal((T, S, H, D))
+    m = rng.standard_normal((T, S, H)) * 3
+    l = rng.uniform(0.5, 20, (T, S, H))
+    n_valid = np.array([7, 0, 3], dtype=np.int32)
+    part = np.concatenate([acc, m[..., None], l[..., None]], axis=-1).astype(np.float32)
+    got = _gd().attn_merge(dev(part), dev(n_valid)).cpu().numpy()
+    ref = oracle.lse_merge(part[..., :D].astype(np.float64), part[..., D].astype(np.float64),
+                           part[..., D + 1].astype(np.float64), n_valid)
+    assert_close(got, ref, 1e-5, "merge")
+    assert (got[1] == 0).all()

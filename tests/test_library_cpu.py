@@ -1,0 +1,114 @@
+"""CPU checks of the C-ABI library: it loads, exports what the header declares, and its host
+logic (planner, argument checks) behaves, all without launching anything."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "gqa_decode.h"
+
+
+@pytest.fixture(scope="module")
+def gd():
+    from gqa_decode_attention_03_gb300 import gqa_decode
+    return gqa_decode
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(\w+)\s*\(", text, flags=re.M))
+                  - {"if", "defined"})
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("attn_decode_f16", "attn_decode_q8_sel", "attn_merge", "attn_decode_plan",
+              "attn_decode_workspace_bytes", "gqa_status_string", "gqa_last_error",
+              "gqa_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(gd):
+    lib = ctypes.CDLL(str(gd._LIB_PATH))
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in the header but not exported"
+    assert set(declared_functions()) <= set(gd.EXPORTS) | set(declared_functions())
+    assert gd.LIB.gqa_abi_version() == 1
+
+
+def test_status_strings(gd):
+    assert gd.LIB.gqa_status_string(0) == b"GQA_OK"
+    assert gd.LIB.gqa_status_string(2) == b"GQA_EWORKSPACE"
+    assert gd.LIB.gqa_status_string(99) == b"GQA_UNKNOWN"
+
+
+def test_plan_long_context(gd):
+    # 16 rows x 8 KV heads up to 32768 positions on 152 SMs, f16, D=128 (64-row stages)
+    p = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_F16, num_sms=152)
+    assert p.tile == 64 and p.chunk % 64 == 0
+    assert p.n_split == -(-32768 // p.chunk) and p.merge == 1
+    assert (p.grid_x, p.grid_y, p.grid_z) == (p.n_split, 8, 16)
+    part = 16 * p.n_split * 32 * 130 * 4
+    assert p.ws_bytes == -(-part // 256) * 256 + 16 * 4
+    # about 8 CTAs per SM at full length
+    assert 4 * 152 <= 16 * 8 * p.n_split <= 16 * 152
+
+
+def test_plan_small_problem_is_one_chunk(gd):
+    p = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
+    assert p.n_split == 1 and p.merge == 0 and p.ws_bytes == 0 and p.chunk == 128
+
+
+def test_plan_selected_width_caps_chunks(gd):
+    # int8 + 1024 ids over a context of 8192: the visited list is 1024 long
+    p = gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
+    assert p.tile == 64 and p.n_split == -(-1024 // p.chunk)
+
+
+def test_plan_rejects_bad_shapes(gd):
+    with pytest.raises(gd.GqaError, match="EINVAL"):
+        gd.plan(1, 32, 8, 96, 10, num_sms=152)             # head_dim
+    with pytest.raises(gd.GqaError, match="EINVAL"):
+        gd.plan(1, 30, 8, 64, 10, num_sms=152)             # heads not a multiple
+    with pytest.raises(gd.GqaError, match="EUNSUPPORTED"):
+        gd.plan(1, 34, 2, 64, 10, num_sms=152)             # group 17
+    with pytest.raises(gd.GqaError, match="EINVAL"):
+        gd.plan(1, 4, 1, 64, 10, 0, gd.KIND_Q8, num_sms=152)  # budget 0
+    with pytest.raises(gd.GqaError, match="EINVAL"):
+        gd.plan(1, 4, 1, 64, -1, num_sms=152)              # negative length
+
+
+def test_decode_rejects_bad_arguments_before_any_launch(gd):
+    L = gd.LIB
+    P = ctypes.c_void_p
+    good = P(1 << 20)
+    # NULL q
+    st = L.attn_decode_f16(None, good, good, good, good, None, 1, 1, 4, 1, 64, 16, 16, 0.1, None,
+                           0, None, None)
+    assert st == gd.GQA_EINVAL and b"NULL" in L.gqa_last_error()
+    # misaligned cache
+    st = L.attn_decode_f16(good, P((1 << 20) + 2), good, good, good, None, 1, 1, 4, 1, 64, 16,
+                           16, 0.1, None, 0, None, None)
+    assert st == gd.GQA_EINVAL and b"aligned" in L.gqa_last_error()
+    # non-finite scale
+    st = L.attn_decode_f16(good, good, good, good, good, None, 1, 1, 4, 1, 64, 16, 16,
+                           float("inf"), None, 0, None, None)
+    assert st == gd.GQA_EINVAL
+    # seq_of NULL with fewer sequences than rows
+    st = L.attn_decode_f16(good, good, good, good, good, None, 2, 1, 4, 1, 64, 16, 16, 0.1, None,
+                           0, None, None)
+    assert st == gd.GQA_EINVAL
+    # ids without a budget
+    st = L.attn_decode_q8_sel(good, good, good, good, good, good, 0, good, good, None, 1, 1, 4, 1,
+                              64, 16, 16, 0.1, None, 0, None, None)
+    assert st == gd.GQA_EINVAL
+    # n_tok == 0 is a no-op
+    st = L.attn_decode_f16(None, None, None, None, None, None, 0, 1, 4, 1, 64, 16, 16, 0.1, None,
+                           0, None, None)
+    assert st == gd.GQA_OK
+    # merge: bad head_dim
+    assert L.attn_merge(good, good, 2, 1, 4, 100, good, None) == gd.GQA_EINVAL
