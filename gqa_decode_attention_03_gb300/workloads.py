@@ -228,6 +228,13 @@ def long_context() -> Case:
                          name="long_ctx_b16_U1024-32768_h32_hk8_d128")
 
 
+def long_context_4() -> Case:
+    """The long-context shape with 4 sequences (a smaller case for profiler captures)."""
+    L = long_context_lengths(seed=1007, n=4)
+    return make_f16_case(1007, 4, 32, 8, 128, L, cache_cap=32768, scale=1 / math.sqrt(128),
+                         name="long_ctx_b4_U1024-32768_h32_hk8_d128")
+
+
 def q8_selected() -> Case:
     """int8 KV, 4 KV heads x 12 = 48 heads, D=256, context 8192, 1024 sorted ids, scale 1/16."""
     return make_q8_case(1004, 1, 48, 4, 256, [8192], budget=1024, scale=1 / 16,
@@ -254,6 +261,7 @@ NAMED = {
     "gqa_d64_L1024": lambda: gqa_d64(1024),
     "gqa_d64_L4096": lambda: gqa_d64(4096),
     "long_ctx": long_context,
+    "long_ctx_4": long_context_4,
     "q8_sel": q8_selected,
     "batched": batched,
     "prefill_chunk": prefill_chunk,
