@@ -100,6 +100,8 @@ gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int
 
 namespace gqa {
 
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 Variant pick_variant(int group) {
   if (group <= 4) return Variant{group <= 1 ? 1 : (group <= 2 ? 2 : 4), 4};
   return Variant{4, 2};

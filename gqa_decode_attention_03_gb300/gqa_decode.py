@@ -23,7 +23,8 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
-           "gqa_abi_version")
+           "gqa_abi_version", "attn_decode_f16_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
 class GqaPlan(ctypes.Structure):
@@ -53,6 +54,8 @@ def _load():
     lib.attn_decode_q8_sel.argtypes = [P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I64, I, F, P,
                                        SZ, P, P]
     lib.attn_decode_q8_sel.restype = I
+    lib.attn_decode_f16_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I64, I, F, P, P]
+    lib.attn_decode_f16_noalloc.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -142,6 +145,30 @@ def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv
     _check(LIB.attn_decode_f16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(kv_len),
                                _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale, _ptr(ws),
                                ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    return out
+
+
+def attn_decode_f16_noalloc(q, k_cache, v_cache, kv_len, scale=None, seq_of=None,
+                            max_kv_len=None, out=None, err=None, stream=None):
+    """attn_decode_f16 for callers that cannot allocate device memory: the split partials go to
+    a static 16 MiB device array inside the library instead of a caller workspace.  Calls that
+    overlap on the GPU share that array and race; sizes needing more scratch are refused."""
+    _need(q, torch.float32, "q", 3)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(kv_len, torch.int32, "kv_len", 1)
+    if seq_of is not None:
+        _need(seq_of, torch.int32, "seq_of", 1)
+    T, H, D = q.shape
+    n_seq, cap, Hk, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_kv_len = cap if max_kv_len is None else int(max_kv_len)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", 3)
+    _check(LIB.attn_decode_f16_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                       _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
+                                       max_kv_len, scale, _ptr(err), _stream(stream)))
     return out
 
 

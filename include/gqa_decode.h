@@ -152,6 +152,39 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
 gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, int n_tok,
                       int n_heads, int head_dim, float* out, cudaStream_t stream);
 
+/*
+ * attn_decode_f16_noalloc -- attn_decode_f16 without a caller-provided workspace.  The pages
+ * have no counterpart of this call; it exists for callers that cannot allocate device memory.
+ *
+ * Who needs it: hosts that own all device memory and hand a plug-in nothing but its input and
+ * output buffers -- e.g. a serving runtime that reserves a fixed arena at start-up and forbids
+ * any later cudaMalloc, or a foreign-language caller that reaches this library only through the
+ * C ABI and has no allocator of its own.  When a row is split into several KV chunks,
+ * attn_decode_f16 needs `ws` for the chunk partials; this call takes them from a static
+ * __device__ array of GQA_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library instead.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *   - Arguments, layouts, results and error bits are those of attn_decode_f16.
+ *   - Sizes whose workspace (attn_decode_workspace_bytes(..., budget -1, GQA_KIND_F16) with
+ *     max_kv_len capped at cache_cap) exceeds GQA_NOALLOC_SCRATCH_BYTES are refused with
+ *     GQA_EWORKSPACE before anything launches; gqa_last_error() gives both sizes.
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents.  No
+ *     part of it has to start at zero: each call writes every partial and chunk count it
+ *     reads.  Calls whose kernels overlap on the GPU (different streams, or threads) race on
+ *     it; serialise them, e.g. on one stream.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (16 << 20)
+gqa_status attn_decode_f16_noalloc(const float* q, const uint16_t* k_cache,
+                                   const uint16_t* v_cache, float* out, const int32_t* kv_len,
+                                   const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                                   int n_kv_heads, int head_dim, int64_t cache_cap,
+                                   int max_kv_len, float scale, int32_t* err_word,
+                                   cudaStream_t stream);
+
 /* Human-readable name of a status; static storage. */
 const char* gqa_status_string(gqa_status s);
 
