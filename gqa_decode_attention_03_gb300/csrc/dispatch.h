@@ -10,8 +10,9 @@
 namespace gqa {
 
 struct Variant {
-  int gw;   // query heads per consumer warp (1, 2 or 4)
-  int nps;  // row slices of a stage (consumer warps per head group)
+  int gw;   // CUDA-core kernel: query heads per consumer warp (1, 2 or 4)
+  int nps;  // CUDA-core kernel: row slices of a stage (consumer warps per head group)
+  int mma;  // 1: the tensor-core kernel (f16 caches only)
 };
 
 Variant pick_variant(int group);

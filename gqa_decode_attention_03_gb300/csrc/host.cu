@@ -103,8 +103,8 @@ namespace gqa {
 void set_last_error(const char* msg) { g_last_error = msg; }
 
 Variant pick_variant(int group) {
-  if (group <= 4) return Variant{group <= 1 ? 1 : (group <= 2 ? 2 : 4), 4};
-  return Variant{4, 2};
+  if (group <= 4) return Variant{group <= 1 ? 1 : (group <= 2 ? 2 : 4), 4, 0};
+  return Variant{4, 2, 0};
 }
 
 int stage_rows(int kind, int head_dim) {
@@ -267,9 +267,14 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     }
   }
 
-  const gqa::Variant var = gqa::pick_variant(p.group);
+  gqa::Variant var = gqa::pick_variant(p.group);
   const int nhg = (p.group + var.gw - 1) / var.gw;
   const int threads = 32 * (nhg * var.nps + 1);
+  // f16 caches run on the tensor cores unless GQA_F16_KERNEL=fma asks for the CUDA-core kernel
+  if (kind == GQA_KIND_F16) {
+    const char* k = std::getenv("GQA_F16_KERNEL");
+    var.mma = !(k && std::strcmp(k, "fma") == 0);
+  }
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
   cudaError_t e = gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");

@@ -1,5 +1,7 @@
-// inst_f16_d128.cu -- partial-kernel instantiations for f16 caches (TMA), head_dim 128.
+// inst_f16_d128.cu -- partial-kernel instantiations for f16 caches, head_dim 128: the tensor-core
+// kernel (default) and the CUDA-core kernel (kept for comparison and as a parity cross-check).
 #include "dispatch.h"
+#include "partial_mma.cuh"
 
 namespace gqa {
 
@@ -15,10 +17,23 @@ static cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, cons
   return cudaGetLastError();
 }
 
+template <int D, int NHG>
+static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& p,
+                              dim3 grid, cudaStream_t s) {
+  using C = MmaCfg<D, NHG>;
+  const void* fn = reinterpret_cast<const void*>(&partial_mma_kernel<D, NHG>);
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  partial_mma_kernel<D, NHG><<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_partial_f16_d128(Variant v, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PartialParams& p, dim3 grid, int threads,
                                     cudaStream_t s) {
   constexpr Kind K = Kind::F16;
+  if (v.mma) return p.group <= 8 ? launch_mma<128, 1>(tk, tv, p, grid, s)
+                                 : launch_mma<128, 2>(tk, tv, p, grid, s);
   if (v.nps == 4) {
     if (v.gw == 1) return launch_one<K, 128, 1, 4>(tk, tv, p, grid, threads, s);
     if (v.gw == 2) return launch_one<K, 128, 2, 4>(tk, tv, p, grid, threads, s);

@@ -35,6 +35,21 @@ def forced_chunk(n):
             os.environ["GQA_FORCE_CHUNK"] = old
 
 
+@contextmanager
+def f16_kernel(name):
+    """Runs the block with the f16 path on the given kernel: "mma" (tensor cores, the default)
+    or "fma" (the CUDA-core kernel)."""
+    old = os.environ.get("GQA_F16_KERNEL")
+    os.environ["GQA_F16_KERNEL"] = name
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("GQA_F16_KERNEL", None)
+        else:
+            os.environ["GQA_F16_KERNEL"] = old
+
+
 def run_case(case, err=None, max_kv_len=None, ids=None, seq_of="case"):
     from gqa_decode_attention_03_gb300 import gqa_decode as gd
     q = dev(case.q)

@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (TOL_F16, TOL_Q8, assert_close, dev, forced_chunk, oracle_ref, run_case,
-                      tol_of)
+from gpu_util import (TOL_F16, TOL_Q8, assert_close, dev, f16_kernel, forced_chunk, oracle_ref,
+                      run_case, tol_of)
 from gqa_decode_attention_03_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -69,16 +69,35 @@ def test_prefill_chunk_rows():
 SHAPES = [(D, G) for D in (64, 128, 256) for G in (1, 2, 3, 4, 6, 8, 12, 16)]
 
 
+@pytest.mark.parametrize("kernel", ["mma", "fma"])
 @pytest.mark.parametrize("chunk", [None, 64, 128])
 @pytest.mark.parametrize("D,G", SHAPES)
-def test_f16_shapes(D, G, chunk):
+def test_f16_shapes(D, G, chunk, kernel):
     # rows: ragged lengths over several tiles, a one-position row, an empty row; 2 KV heads
     case = W.make_f16_case(100 + D + G, 4, 2 * G, 2, D, [300, 1, 0, 133], cache_cap=320,
                            scale=1 / math.sqrt(D))
-    with forced_chunk(chunk):
+    with forced_chunk(chunk), f16_kernel(kernel):
         got = run_case(case).cpu().numpy()
-    assert_close(got, oracle_ref(case), TOL_F16, f"f16 D{D} G{G} chunk{chunk}")
+    assert_close(got, oracle_ref(case), TOL_F16, f"f16 {kernel} D{D} G{G} chunk{chunk}")
     assert (got[2] == 0).all()
+
+
+@pytest.mark.parametrize("kernel", ["mma", "fma"])
+def test_long_context_subset_both_kernels(kernel):
+    """Both f16 kernels on the long-context shape (4 sequences), every output element."""
+    case = W.long_context_4()
+    with f16_kernel(kernel):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, f"long_ctx_4 {kernel}")
+
+
+def test_peaked_attention_stays_exact():
+    """Scores spread over ~60 in log2 units (large scale): the lazy rescale and the hi/lo split
+    of p must keep the result at the oracle's value."""
+    case = W.make_f16_case(409, 2, 8, 2, 128, [3000, 2000], cache_cap=3000, scale=2.0)
+    with forced_chunk(512):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, "peaked")
 
 
 @pytest.mark.parametrize("chunk", [None, 128])
