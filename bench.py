@@ -2,8 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_ctx] [--impl gb300|reference]
 
-One step = one call of the whole path (split-KV partial kernel + log-sum-exp merge) over the
-workload's batch.  Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+One step = one call of the whole path over the workload's batch: a single kernel launch that
+computes the split-KV partials and, in the last CTA of each (row, KV head), their log-sum-exp
+merge.  Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
 independent replica of the workload on its own GPU (weak scaling; the path needs no exchange).
 
 Timing: W untimed warm-up steps, then K steps on the launching stream between CUDA events.
@@ -155,6 +156,16 @@ def _device_inputs(case, torch):
     return t
 
 
+def _kernel_name(case, plan):
+    if plan.streamk:
+        return "streamk_mma_kernel (stream-K split, merge fused)"
+    if case.kind == "f16" and os.environ.get("GQA_F16_KERNEL") != "fma":
+        name = "partial_mma_kernel"
+    else:
+        name = "partial_kernel"
+    return name + (" (split-KV, merge fused)" if plan.merge else "")
+
+
 def run_gpu(args):
     import torch
     world, rank, local = _dist()
@@ -221,24 +232,6 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
 
-    # the merge kernel alone (same partials, L2 as the step leaves it), to isolate the partial
-    # kernel's duration for the roofline
-    merge_ms = 0.0
-    if plan.merge:
-        part = ws[: T * plan.n_split * H * (D + 2) * 4].view(torch.float32).view(
-            T, plan.n_split, H, D + 2)
-        off = -(-part.numel() * 4 // 256) * 256
-        n_valid = ws[off: off + 4 * T].view(torch.int32)
-        evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(min(K, 500))]
-        for a, b in evm:
-            step()
-            a.record(stream)
-            gd.attn_merge(part, n_valid, out=out, stream=stream)
-            b.record(stream)
-        torch.cuda.synchronize()
-        merge_ms = float(np.mean([a.elapsed_time(b) for a, b in evm]))
-
     # end to end through host buffers: pinned q / kv_len in, out back, every step
     q_h = torch.from_numpy(case.q).pin_memory()
     kv_h = torch.from_numpy(case.kv_len).pin_memory()
@@ -268,8 +261,7 @@ def run_gpu(args):
         return
     alg = case.algorithmic_bytes()
     peak, peak_src = _peaks()
-    part_ms = ms - merge_ms
-    achieved = alg / (part_ms * 1e-3) / 1e9
+    achieved = alg / (ms * 1e-3) / 1e9  # one kernel per step: the partial kernel, merge fused
     traffic = _ncu_traffic(case.name)
     gbs = world * alg / (ms * 1e-3) / 1e9
     line = {
@@ -280,16 +272,16 @@ def run_gpu(args):
         "data": "synthetic: seeded N(0,1) q and f16 K/V, NaN past each sequence's length",
         "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
                                  "n_split": plan.n_split, "parallelism": f"replicas x{world}"}),
-        "roofline": {"bound": "hbm", "kernel": "partial_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": _kernel_name(case, plan),
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "partial_us": round(part_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3)},
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic},
         "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "h2d_bytes_per_step": int(case.q.nbytes + case.kv_len.nbytes),
                 "d2h_bytes_per_step": int(T * H * D * 4)},
-        "gpu_launches": int(K * (2 if plan.merge else 1)),
+        "gpu_launches": int(K),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -77,7 +77,17 @@ int env_int(const char* name) {
   return v ? std::atoi(v) : 0;
 }
 
-constexpr int kCtasPerSmTarget = 8;  // partial-kernel CTAs per SM the planner aims for
+// Chunked split: enough chunks for about one wave of CTAs (two per SM) at the longest row, but
+// no chunk longer than kMaxChunk positions.  Measured on GB300 (f16, D = 128): a CTA streams at
+// most ~51 GB/s (three 32 KB stages in flight), so chunks far above 8192 positions leave a
+// long tail, while short chunks multiply the fixed cost of a CTA (pipeline fill, partial
+// write, merge ticket); 4096..8192-position chunks gave 98-108 % of the measured copy
+// bandwidth on both the mixed-length and the uniform batch.
+constexpr int kCtasPerSm = 2;
+constexpr long long kMaxChunk = 8192;
+// Rows whose whole visited list is at most this many bytes of K/V (and scales) are not split:
+// one CTA streams them in a few microseconds, less than a split's merge step costs.
+constexpr long long kMinSplitBytes = 256 << 10;
 
 // Shapes that do not depend on the device.
 gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
@@ -102,9 +112,35 @@ namespace gqa {
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
-Variant pick_variant(int group) {
-  if (group <= 4) return Variant{group <= 1 ? 1 : (group <= 2 ? 2 : 4), 4, 0};
+// CUDA-core kernel: heads per warp for the query heads one CTA serves (at most 4 after the
+// head split), four row slices per stage.
+Variant pick_variant(int heads_per_cta) {
+  if (heads_per_cta <= 4) return Variant{heads_per_cta <= 1 ? 1 : (heads_per_cta <= 2 ? 2 : 4), 4, 0};
   return Variant{4, 2, 0};
+}
+
+// The CUDA-core kernel (int8 caches, or f16 with GQA_F16_KERNEL=fma) splits a KV head's query
+// heads over head_split CTAs of at most four heads each -- the smallest divisor of the group
+// size that gets there -- so a wide group (12 heads) spreads over three times as many CTAs.
+// The tensor-core kernels serve the whole group in one CTA.
+int head_split_for(int kind, int group) {
+  const char* k = std::getenv("GQA_F16_KERNEL");
+  const bool fma = kind == GQA_KIND_Q8 || (k && std::strcmp(k, "fma") == 0);
+  if (!fma) return 1;
+  for (int hs = 1; hs <= group; ++hs)
+    if (group % hs == 0 && group / hs <= 4) return hs;
+  return group;
+}
+
+// The stream-K split is opt-in (GQA_F16_SPLIT=streamk): on GB300 the chunked grid measured
+// faster on both the mixed-length and the uniform batch (a fixed cost per piece end outweighs
+// the perfect balance), so it stays the default.
+bool use_streamk(int kind, int n_tok) {
+  if (kind != GQA_KIND_F16 || n_tok > kStreamKMaxRows) return false;
+  const char* k = std::getenv("GQA_F16_KERNEL");  // "fma": CUDA-core kernel, chunked grid
+  if (k && std::strcmp(k, "fma") == 0) return false;
+  const char* m = std::getenv("GQA_F16_SPLIT");
+  return m && std::strcmp(m, "streamk") == 0;
 }
 
 int stage_rows(int kind, int head_dim) {
@@ -146,11 +182,32 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
   }
   const int tile = gqa::stage_rows(kind, head_dim);
   const long long nmax = budget > 0 ? std::min(max_kv_len, budget) : max_kv_len;
-  // Equal chunks sized so that the CTAs over all (row, KV head) pairs come to about
-  // kCtasPerSmTarget per SM (several waves of the 1-2 CTAs an SM holds), rounded to whole tiles.
-  const long long units = (long long)n_tok * n_kv_heads * std::max(nmax, 1LL);
-  long long chunk = (units + (long long)kCtasPerSmTarget * num_sms - 1) /
-                    ((long long)kCtasPerSmTarget * num_sms);
+  if (gqa::use_streamk(kind, n_tok)) {
+    // equal shares of the whole stream, at least 256 positions each, two CTAs per SM at most
+    const long long wmax = (long long)n_tok * n_kv_heads * std::max(nmax, 1LL);
+    int ctas = (int)std::min<long long>(2LL * num_sms, std::max(1LL, (wmax + 255) / 256));
+    const int forced_ctas = env_int("GQA_FORCE_CTAS");  // tests: many small shares
+    if (forced_ctas > 0) ctas = std::min(forced_ctas, 65535);
+    const int group = n_heads / n_kv_heads;
+    plan->chunk = 0;
+    plan->n_split = ctas;
+    plan->tile = tile;
+    plan->grid_x = ctas;
+    plan->grid_y = 1;
+    plan->grid_z = 1;
+    plan->merge = 1;
+    plan->streamk = 1;
+    const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
+    plan->ws_bytes = cnt + ((size_t)ctas + (size_t)n_tok * n_kv_heads) * group *
+                               (head_dim + 2) * sizeof(float);
+    return GQA_OK;
+  }
+  const int hsplit = gqa::head_split_for(kind, n_heads / n_kv_heads);
+  const long long units = (long long)n_tok * n_kv_heads * hsplit * std::max(nmax, 1LL);
+  long long chunk = (units + (long long)kCtasPerSm * num_sms - 1) / ((long long)kCtasPerSm * num_sms);
+  chunk = std::min(chunk, kMaxChunk);
+  const long long row_bytes = kind == GQA_KIND_F16 ? 4LL * head_dim : 2LL * (head_dim + head_dim / 32);
+  if (nmax * row_bytes <= kMinSplitBytes) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");
   if (forced > 0) chunk = forced;
   chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;
@@ -162,12 +219,13 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
   plan->n_split = (int)n_split;
   plan->tile = tile;
   plan->grid_x = (int)n_split;
-  plan->grid_y = n_kv_heads;
+  plan->grid_y = n_kv_heads * hsplit;
   plan->grid_z = n_tok;
   plan->merge = n_split > 1 ? 1 : 0;
   if (plan->merge) {
+    const size_t cnt = ((size_t)n_tok * plan->grid_y * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t part = (size_t)n_tok * n_split * n_heads * (head_dim + 2) * sizeof(float);
-    plan->ws_bytes = (part + 255) / 256 * 256 + (size_t)n_tok * sizeof(int32_t);
+    plan->ws_bytes = cnt + (part + 255) / 256 * 256 + (size_t)n_tok * sizeof(int32_t);
   }
   return GQA_OK;
 }
@@ -233,6 +291,7 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.n_heads = n_heads;
   p.n_kv_heads = n_kv_heads;
   p.group = n_heads / n_kv_heads;
+  p.head_split = 1;
   p.cache_cap = cache_cap;
   p.max_kv_len = max_len;
   p.budget = ids ? budget : INT32_MAX;
@@ -240,10 +299,16 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.n_split = plan.n_split;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.merge = plan.merge;
-  if (plan.merge) {
-    p.part = static_cast<float*>(ws);
+  if (plan.streamk) {  // ws = [arrival counters][piece records]
+    const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
+    p.counters = static_cast<unsigned int*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
+  } else if (plan.merge) {  // ws = [arrival counters][partials][n_valid], 256-byte aligned
+    const size_t cnt = ((size_t)n_tok * plan.grid_y * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);
-    p.n_valid = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + (part + 255) / 256 * 256);
+    p.counters = static_cast<unsigned int*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
+    p.n_valid = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + cnt + (part + 255) / 256 * 256);
   }
 
   CUtensorMap tk, tv;
@@ -267,8 +332,9 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     }
   }
 
-  gqa::Variant var = gqa::pick_variant(p.group);
-  const int nhg = (p.group + var.gw - 1) / var.gw;
+  p.head_split = plan.streamk ? 1 : plan.grid_y / n_kv_heads;
+  gqa::Variant var = gqa::pick_variant(p.group / p.head_split);
+  const int nhg = (p.group / p.head_split + var.gw - 1) / var.gw;
   const int threads = 32 * (nhg * var.nps + 1);
   // f16 caches run on the tensor cores unless GQA_F16_KERNEL=fma asks for the CUDA-core kernel
   if (kind == GQA_KIND_F16) {
@@ -276,13 +342,11 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     var.mma = !(k && std::strcmp(k, "fma") == 0);
   }
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-  cudaError_t e = gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
+  cudaError_t e = plan.streamk
+                      ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
+                      : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
-  if (plan.merge) {
-    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-  }
-  return GQA_OK;
+  return GQA_OK;  // split rows are merged inside the kernel by each (row, KV head)'s last CTA
 }
 
 }  // namespace

@@ -1,7 +1,9 @@
-// inst_f16_d128.cu -- partial-kernel instantiations for f16 caches, head_dim 128: the tensor-core
-// kernel (default) and the CUDA-core kernel (kept for comparison and as a parity cross-check).
+// inst_f16_d128.cu -- kernel instantiations for f16 caches, head_dim 128: the stream-K
+// tensor-core kernel (default), the chunked-grid tensor-core kernel (more than 8192 rows, or
+// GQA_F16_SPLIT=chunked) and the CUDA-core kernel (GQA_F16_KERNEL=fma; comparison and parity
+// cross-check).
 #include "dispatch.h"
-#include "partial_mma.cuh"
+#include "streamk_mma.cuh"
 
 namespace gqa {
 
@@ -26,6 +28,24 @@ static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, cons
   if (e != cudaSuccess) return e;
   partial_mma_kernel<D, NHG><<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
   return cudaGetLastError();
+}
+
+template <int NHG>
+static cudaError_t launch_sk(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& p,
+                             dim3 grid, cudaStream_t s) {
+  using C = MmaCfg<128, NHG>;
+  const void* fn = reinterpret_cast<const void*>(&streamk_mma_kernel<128, NHG>);
+  // the stage ring, barriers and the [slices][group][D + 2] slice-merge area
+  const int smem = C::SMEM_BYTES + C::NPS * p.group * (128 + 2) * 4;
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES + C::NPS * 16 * (128 + 2) * 4);
+  if (e != cudaSuccess) return e;
+  streamk_mma_kernel<128, NHG><<<grid, C::MAX_THREADS, smem, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_streamk_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const PartialParams& p, dim3 grid, cudaStream_t s) {
+  return p.group <= 8 ? launch_sk<1>(tk, tv, p, grid, s) : launch_sk<2>(tk, tv, p, grid, s);
 }
 
 cudaError_t launch_partial_f16_d128(Variant v, const CUtensorMap& tk, const CUtensorMap& tv,

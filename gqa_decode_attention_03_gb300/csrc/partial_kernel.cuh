@@ -42,8 +42,11 @@ struct PartialParams {
   float* out;              // [T][H][D]          (merge == 0)
   float* part;             // [T][S][H][D+2]     (merge == 1)
   int32_t* n_valid;        // [T] chunks holding data, written when merge == 1
+  unsigned int* counters;  // [T][Hk] chunk arrivals (zero before and after every call)
   int32_t* err;            // device error word or null
   int n_tok, n_seq, n_heads, n_kv_heads, group;
+  int head_split;          // CUDA-core kernel: CTAs per KV head, each serving group/head_split
+                           // query heads (grid.y = n_kv_heads * head_split); 1 elsewhere
   long long cache_cap;
   int max_kv_len;
   int budget;              // ids != null: width cap; otherwise unused
@@ -179,6 +182,82 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[GW], int lane) {
   }
 }
 
+// ------------------------------------------------------------------------------ fused merge
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Called by every consumer thread after this CTA wrote its chunk's partial records.  The CTA
+// takes a ticket on its counter (one per row, KV head and CTA head group); the CTA holding the
+// last of the nv tickets merges the nv chunks of heads head0 .. head0 + nheads - 1 by
+// log-sum-exp (qsa2.metal, qsa_merge2) and writes out.  atomicInc wraps the counter back to 0
+// on the last ticket, so every call leaves it at zero.  Nobody waits for anybody: the CTAs that
+// are not last simply finish.  One warp per head; lane c holds chunk c's (m, l) and weight and
+// broadcasts the weight by shuffle, so a head's loads go out in one round.
+template <int D>
+__device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int head0,
+                                              int nheads, size_t counter, int nv, int ncw) {
+  __shared__ int s_last;
+  __threadfence();  // this thread's partial stores, visible device-wide before the ticket
+  named_bar_sync(1, ncw * 32);
+  if (threadIdx.x == 0)
+    s_last = atomicInc(p.counters + counter, (unsigned)(nv - 1)) == (unsigned)(nv - 1);
+  named_bar_sync(1, ncw * 32);
+  if (!s_last) return;
+  __threadfence();
+  constexpr int DPL = D / 32;  // output dims per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t rec = (size_t)p.n_heads * (D + 2);  // floats between consecutive chunks
+  for (int h = warp; h < nheads; h += ncw) {
+    const int head = head0 + h;
+    const float* base = p.part + ((size_t)t * p.n_split * p.n_heads + head) * (D + 2);
+    float* o = p.out + ((size_t)t * p.n_heads + head) * D + lane * DPL;
+    float M = -INFINITY;
+    for (int cc = lane; cc < nv; cc += 32) M = fmaxf(M, __ldcg(base + cc * rec + D));
+    M = warp_max(M);
+    float a[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a[k] = 0.f;
+    float Ls = 0.f;
+    if (M != -INFINITY) {
+      for (int c0 = 0; c0 < nv; c0 += 32) {
+        float e = 0.f;
+        if (c0 + lane < nv) {
+          const float m = __ldcg(base + (c0 + lane) * rec + D);
+          e = m == -INFINITY ? 0.f : __expf(m - M);
+          Ls = fmaf(__ldcg(base + (c0 + lane) * rec + D + 1), e, Ls);
+        }
+        const int nb = min(32, nv - c0);
+#pragma unroll 8
+        for (int j = 0; j < nb; ++j) {
+          const float ej = __shfl_sync(0xffffffffu, e, j);
+          const float* ac = base + (c0 + j) * rec + lane * DPL;
+#pragma unroll
+          for (int k = 0; k < DPL; k += 2) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(ac + k));
+            a[k] = fmaf(ej, v.x, a[k]);
+            a[k + 1] = fmaf(ej, v.y, a[k + 1]);
+          }
+        }
+      }
+      Ls = warp_sum(Ls);
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; k += 2)
+      *reinterpret_cast<float2*>(o + k) = make_float2(a[k] * inv, a[k + 1] * inv);
+  }
+}
+
 // ------------------------------------------------------------------------------ producers
 
 // f16: lane 0 streams the chunk's K/V tiles by TMA into the stage ring.
@@ -293,8 +372,10 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
                    const PartialParams p) {
   using C = Cfg<K, D, GW, NPS>;
   extern __shared__ uint8_t smem_raw[];
-  const int c = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
-  const int G = p.group;
+  const int c = blockIdx.x, t = blockIdx.z;
+  const int g = blockIdx.y / p.head_split;        // KV head
+  const int G = p.group / p.head_split;           // query heads served by this CTA
+  const int head0 = g * p.group + (blockIdx.y % p.head_split) * G;  // its first query head
   const int nhg = (G + GW - 1) / GW;
   const int ncw = nhg * NPS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -315,16 +396,16 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
   const int nsel = p.ids ? min(L, p.budget) : L;  // qsa2.metal: width = min(n_kv, budget)
   const int c0 = c * p.chunk;
   const int c1 = min(c0 + p.chunk, nsel);
-  if (c == 0 && g == 0 && threadIdx.x == 0) {
+  if (c == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     if (errbits) flag_error(p.err, errbits);
     if (p.merge) p.n_valid[t] = (nsel + p.chunk - 1) / p.chunk;
   }
   if (c0 >= nsel) {
-    // empty context: zeros (flash_attention.metal's seq_len == 0 guard); with partials the
-    // merge writes them, since this chunk is not counted in n_valid
-    if (!p.merge && c == 0)
+    // empty context: zeros (flash_attention.metal's seq_len == 0 guard), written by chunk 0
+    // whether or not the row is split, since no CTA of the row merges anything
+    if (c == 0)
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
+        p.out[((size_t)t * p.n_heads + head0 + i / D) * D + i % D] = 0.f;
     return;
   }
   const int ntiles = (c1 - c0 + C::TP - 1) / C::TP;
@@ -365,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
 #pragma unroll
   for (int h = 0; h < GW; ++h) {
     const int hh = hg * GW + h;
-    const float* qh = p.q + ((size_t)t * p.n_heads + g * G + (hh < G ? hh : 0)) * D;
+    const float* qh = p.q + ((size_t)t * p.n_heads + head0 + (hh < G ? hh : 0)) * D;
 #pragma unroll
     for (int k = 0; k < C::CPL; ++k) {
       const int d0 = (li + k * C::LPP) * C::DPC;
@@ -534,7 +615,7 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
       A = fmaf(rr[d], e, A);
       Ls = fmaf(rr[D + 1], e, Ls);
     }
-    const int head = g * G + hh;
+    const int head = head0 + hh;
     if (p.merge) {
       float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
       pr[d] = A;
@@ -546,6 +627,9 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
       p.out[((size_t)t * p.n_heads + head) * D + d] = Ls > 0.f ? A / Ls : 0.f;
     }
   }
+  if (p.merge)
+    merge_if_last<D>(p, t, head0, G, (size_t)t * gridDim.y + blockIdx.y,
+                     (nsel + p.chunk - 1) / p.chunk, ncw);
 }
 
 }  // namespace gqa

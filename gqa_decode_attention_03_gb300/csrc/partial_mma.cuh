@@ -1,7 +1,8 @@
 // partial_mma.cuh -- split-KV decode-attention partial kernel for f16 caches on the tensor cores.
 //
-// Same CTA structure, TMA producer, stage ring, partial format and end-of-chunk merge as
-// partial_kernel (see partial_kernel.cuh), but q.k^T and p.v run as mma.sync m16n8k16 with f32
+// Same CTA structure, TMA producer, stage ring, partial format, end-of-chunk merge and fused
+// last-CTA merge as partial_kernel (see partial_kernel.cuh), but q.k^T and p.v run as
+// mma.sync m16n8k16 with f32
 // accumulation instead of fp32 FMA: the CUDA-core kernel is issue-bound (about 64 warp
 // instructions per position and KV head), this one needs about 6.
 //
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
     if (p.merge) p.n_valid[t] = (L + p.chunk - 1) / p.chunk;
   }
   if (c0 >= L) {
-    if (!p.merge && c == 0)  // empty context: zeros (flash_attention.metal, seq_len == 0)
+    if (c == 0)  // empty context: zeros (flash_attention.metal, seq_len == 0), split or not
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)
         p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
     return;
@@ -304,6 +305,9 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
       p.out[((size_t)t * p.n_heads + head) * D + d] = Ls > 0.f ? A / Ls : 0.f;
     }
   }
+  if (p.merge)
+    merge_if_last<D>(p, t, g * G, G, (size_t)t * p.n_kv_heads + g, (L + p.chunk - 1) / p.chunk,
+                     C::NCW);
 }
 
 }  // namespace gqa

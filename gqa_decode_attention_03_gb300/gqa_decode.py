@@ -30,7 +30,7 @@ NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_dec
 class GqaPlan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int), ("n_split", ctypes.c_int), ("tile", ctypes.c_int),
                 ("grid_x", ctypes.c_int), ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
-                ("merge", ctypes.c_int), ("ws_bytes", ctypes.c_size_t)]
+                ("merge", ctypes.c_int), ("streamk", ctypes.c_int), ("ws_bytes", ctypes.c_size_t)]
 
 
 class GqaError(RuntimeError):
@@ -112,8 +112,10 @@ def workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1,
 
 def alloc_workspace(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16,
                     device=None):
+    """A zeroed workspace: its leading arrival counters must be zero before the first call (every
+    call leaves them zero again), so one workspace can be reused across calls and shapes."""
     n = workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv_len=None,

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 1
+#define GQA_ABI_VERSION 2
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -73,20 +73,27 @@ typedef enum gqa_status {
 
 /* The split plan the decode calls use (exposed so hosts and tests can inspect it). */
 typedef struct gqa_plan {
-  int chunk;         /* positions (or selected cells) per KV chunk, a multiple of tile */
-  int n_split;       /* chunks per row at max_kv_len: ceil(min(max_kv_len, budget) / chunk) */
+  int chunk;         /* chunked mode: positions (or selected cells) per KV chunk, a multiple of
+                        tile; stream-K mode: 0 */
+  int n_split;       /* chunked mode: chunks per row at max_kv_len; stream-K mode: CTAs */
   int tile;          /* positions staged in shared memory per pipeline stage */
-  int grid_x, grid_y, grid_z; /* launch grid of the partial kernel: (n_split, KV heads x head
-                                 groups, n_tok) */
-  int merge;         /* 1 when partials are written to ws and merged by a second kernel */
+  int grid_x, grid_y, grid_z; /* launch grid: chunked (n_split, n_kv_heads, n_tok);
+                                 stream-K (CTAs, 1, 1) */
+  int merge;         /* 1 when rows may be split: partials go to ws and are merged inside the
+                        same kernel by whichever CTA (or warp) finishes a row's KV head last */
+  int streamk;       /* 1: stream-K split (f16 caches): the (row, KV head, position) stream is
+                        cut into equal shares, one per CTA of a persistent grid */
   size_t ws_bytes;   /* workspace the call needs (0 when merge == 0) */
 } gqa_plan;
 
 /*
  * attn_decode_plan -- the split planner (host only; launches nothing, needs no GPU).
- * Chooses the chunk length so that the partial kernel's CTA count is a few waves of the SM
- * count, with every chunk but a row's last the same length (qsa2.metal chunks its id list in
- * fixed 32-cell pieces; FORWARD_MSL's split-T decode uses fixed 512-position partial blocks).
+ * Rows are cut into equal chunks (qsa2.metal chunks its id list in fixed 32-cell pieces;
+ * FORWARD_MSL's split-T decode uses fixed 512-position partial blocks): enough chunks for about
+ * one wave of two CTAs per SM at max_kv_len, none longer than 8192 positions.  With
+ * GQA_F16_SPLIT=streamk in the environment, f16 calls with n_tok <= 8192 use the stream-K
+ * split instead: a persistent grid of up to two CTAs per SM, each taking an equal share of
+ * all rows' KV positions.
  * num_sms <= 0 queries the current CUDA device.  budget < 0 means dense (no id list).
  * Returns GQA_EINVAL on bad sizes, GQA_EUNSUPPORTED for group sizes > 16.
  */
@@ -96,8 +103,10 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
 /*
  * attn_decode_workspace_bytes -- bytes of `ws` that attn_decode_f16 (kind GQA_KIND_F16) or
  * attn_decode_q8_sel (GQA_KIND_Q8) needs for these sizes on the current device; 0 when no
- * split is needed or the sizes are invalid.  The figure is n_tok * n_split * n_heads *
- * (head_dim + 2) * 4 bytes.
+ * split is needed or the sizes are invalid.  It is the arrival counters (n_tok * n_kv_heads *
+ * 4 bytes, rounded up to 256) followed by the partials: chunked mode n_tok * n_split *
+ * n_heads * (head_dim + 2) * 4 bytes (rounded up to 256) and n_valid (n_tok * 4 bytes);
+ * stream-K mode (CTAs + n_tok * n_kv_heads) * group * (head_dim + 2) * 4 bytes.
  */
 size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int head_dim,
                                    int max_kv_len, int budget, int kind);
@@ -114,7 +123,13 @@ size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int h
  *                 truncated to it and flagged GQA_ERR_KVLEN_RANGE)
  *   scale         multiplies q.k (finite)
  *   ws, ws_bytes  caller scratch of >= attn_decode_workspace_bytes(..., GQA_KIND_F16) bytes,
- *                 16-byte aligned (may be NULL when that figure is 0)
+ *                 16-byte aligned (may be NULL when that figure is 0).  Its first
+ *                 ceil(n_tok * n_kv_heads * 4 / 256) * 256 bytes are per-(row, KV head) arrival
+ *                 counters: they must be zero before the first call that uses this ws (zero
+ *                 the buffer once after allocating it); every call leaves them zero again, so
+ *                 the same ws serves any later call.  The rest holds the split partials
+ *                 (see attn_decode_workspace_bytes); it needs no clearing.  Calls sharing a ws
+ *                 must not overlap on the GPU.
  *   err_word      device int32 or NULL
  */
 gqa_status attn_decode_f16(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -172,10 +187,11 @@ gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, in
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that first call
  *     before any stream capture.
- *   - All calls on a device share the one array and it keeps the last call's contents.  No
- *     part of it has to start at zero: each call writes every partial and chunk count it
- *     reads.  Calls whose kernels overlap on the GPU (different streams, or threads) race on
- *     it; serialise them, e.g. on one stream.
+ *   - All calls on a device share the one array and it keeps the last call's contents.  Its
+ *     leading arrival counters (see attn_decode_f16's ws) are zero when the library loads and
+ *     every call leaves them zero again; the partials need no clearing, since each call writes
+ *     every partial it reads.  Calls whose kernels overlap on the GPU (different streams, or
+ *     threads) race on it; serialise them, e.g. on one stream.
  */
 #define GQA_NOALLOC_SCRATCH_BYTES (16 << 20)
 gqa_status attn_decode_f16_noalloc(const float* q, const uint16_t* k_cache,

@@ -36,18 +36,39 @@ def forced_chunk(n):
 
 
 @contextmanager
-def f16_kernel(name):
-    """Runs the block with the f16 path on the given kernel: "mma" (tensor cores, the default)
-    or "fma" (the CUDA-core kernel)."""
-    old = os.environ.get("GQA_F16_KERNEL")
-    os.environ["GQA_F16_KERNEL"] = name
+def _env(**kw):
+    old = {k: os.environ.get(k) for k in kw}
+    for k, v in kw.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = str(v)
     try:
         yield
     finally:
-        if old is None:
-            os.environ.pop("GQA_F16_KERNEL", None)
-        else:
-            os.environ["GQA_F16_KERNEL"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+@contextmanager
+def f16_kernel(name):
+    """Runs the block with the f16 path on one kernel: "chunked" (tensor cores, chunked grid:
+    the default), "streamk" (tensor cores, stream-K split) or "fma" (CUDA cores, chunked)."""
+    env = {"streamk": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT="streamk"),
+           "chunked": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT=None),
+           "fma": dict(GQA_F16_KERNEL="fma", GQA_F16_SPLIT=None)}[name]
+    with _env(**env):
+        yield
+
+
+@contextmanager
+def forced_ctas(n):
+    """Runs the block with the stream-K grid forced to n CTAs (None: the planner's choice)."""
+    with _env(GQA_FORCE_CTAS=n):
+        yield
 
 
 def run_case(case, err=None, max_kv_len=None, ids=None, seq_of="case"):

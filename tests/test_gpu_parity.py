@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (TOL_F16, TOL_Q8, assert_close, dev, f16_kernel, forced_chunk, oracle_ref,
-                      run_case, tol_of)
+from gpu_util import (TOL_F16, TOL_Q8, assert_close, dev, f16_kernel, forced_chunk, forced_ctas,
+                      oracle_ref, run_case, tol_of)
 from gqa_decode_attention_03_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -69,10 +69,10 @@ def test_prefill_chunk_rows():
 SHAPES = [(D, G) for D in (64, 128, 256) for G in (1, 2, 3, 4, 6, 8, 12, 16)]
 
 
-@pytest.mark.parametrize("kernel", ["mma", "fma"])
+@pytest.mark.parametrize("kernel", ["chunked", "fma"])
 @pytest.mark.parametrize("chunk", [None, 64, 128])
 @pytest.mark.parametrize("D,G", SHAPES)
-def test_f16_shapes(D, G, chunk, kernel):
+def test_f16_shapes_chunked(D, G, chunk, kernel):
     # rows: ragged lengths over several tiles, a one-position row, an empty row; 2 KV heads
     case = W.make_f16_case(100 + D + G, 4, 2 * G, 2, D, [300, 1, 0, 133], cache_cap=320,
                            scale=1 / math.sqrt(D))
@@ -82,7 +82,20 @@ def test_f16_shapes(D, G, chunk, kernel):
     assert (got[2] == 0).all()
 
 
-@pytest.mark.parametrize("kernel", ["mma", "fma"])
+@pytest.mark.parametrize("ctas", [None, 1, 3, 16, 77])
+@pytest.mark.parametrize("D,G", SHAPES)
+def test_f16_shapes_stream_k(D, G, ctas):
+    # the same rows under several stream-K grids: shares that cut segments anywhere, shares
+    # smaller than a tile, shares spanning many segments, and an empty row in between
+    case = W.make_f16_case(100 + D + G, 4, 2 * G, 2, D, [300, 1, 0, 133], cache_cap=320,
+                           scale=1 / math.sqrt(D))
+    with forced_ctas(ctas), f16_kernel("streamk"):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, f"f16 stream-K D{D} G{G} ctas{ctas}")
+    assert (got[2] == 0).all()
+
+
+@pytest.mark.parametrize("kernel", ["streamk", "chunked", "fma"])
 def test_long_context_subset_both_kernels(kernel):
     """Both f16 kernels on the long-context shape (4 sequences), every output element."""
     case = W.long_context_4()
@@ -136,17 +149,19 @@ def test_gather_is_bit_exact():
     assert np.array_equal(got, got2)
 
 
-def test_split_matches_unsplit_and_is_deterministic():
+@pytest.mark.parametrize("kernel", ["streamk", "chunked"])
+def test_split_matches_unsplit_and_is_deterministic(kernel):
     case = W.make_f16_case(403, 3, 16, 4, 128, [5000, 64, 3001], cache_cap=5000, scale=0.09)
-    with forced_chunk(100000):
-        one = run_case(case).cpu().numpy()
-    with forced_chunk(64):
-        many = run_case(case).cpu().numpy()
-        again = run_case(case).cpu().numpy()
+    with f16_kernel(kernel):
+        with forced_chunk(100000), forced_ctas(1):
+            one = run_case(case).cpu().numpy()
+        with forced_chunk(64), forced_ctas(200):
+            many = run_case(case).cpu().numpy()
+            again = run_case(case).cpu().numpy()
     assert np.array_equal(many, again)
     ref = oracle_ref(case)
-    assert_close(one, ref, TOL_F16, "one chunk")
-    assert_close(many, ref, TOL_F16, "64-row chunks")
+    assert_close(one, ref, TOL_F16, "one share / chunk")
+    assert_close(many, ref, TOL_F16, "many shares / chunks")
 
 
 def test_rows_sharing_a_sequence():
@@ -218,3 +233,20 @@ def test_merge_entry_point(D):
                            part[..., D + 1].astype(np.float64), n_valid)
     assert_close(got, ref, 1e-5, "merge")
     assert (got[1] == 0).all()
+
+
+def test_workspace_reuse_leaves_counters_zero():
+    """One zeroed workspace serves several split calls of different shapes; the arrival counters
+    at its head are zero again after every call."""
+    gd = _gd()
+    cases = [W.make_f16_case(410 + i, T, 8, 2, 128, L, cache_cap=4000, scale=0.1)
+             for i, (T, L) in enumerate([(3, [4000, 10, 2500]), (2, [300, 3999]),
+                                         (4, [1, 2, 3, 4000])])]
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    with forced_chunk(128):
+        for case in cases:
+            got = gd.attn_decode_f16(dev(case.q), dev(case.k), dev(case.v), dev(case.kv_len),
+                                     scale=case.scale, max_kv_len=4000, ws=ws)
+            torch.cuda.synchronize()
+            assert_close(got.cpu().numpy(), oracle_ref(case), TOL_F16, "reused ws")
+            assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(gd):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in the header but not exported"
     assert set(declared_functions()) <= set(gd.EXPORTS) | set(declared_functions())
-    assert gd.LIB.gqa_abi_version() == 1
+    assert gd.LIB.gqa_abi_version() == 2
 
 
 def test_status_strings(gd):
@@ -46,27 +46,50 @@ def test_status_strings(gd):
     assert gd.LIB.gqa_status_string(99) == b"GQA_UNKNOWN"
 
 
-def test_plan_long_context(gd):
-    # 16 rows x 8 KV heads up to 32768 positions on 152 SMs, f16, D=128 (64-row stages)
+def test_plan_long_context_stream_k(gd, monkeypatch):
+    # opt-in stream-K: 16 rows x 8 KV heads up to 32768 positions, f16, D=128, on 152 SMs:
+    # two CTAs per SM, each an equal share of the (row, KV head, position) stream
+    monkeypatch.setenv("GQA_F16_SPLIT", "streamk")
     p = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_F16, num_sms=152)
-    assert p.tile == 64 and p.chunk % 64 == 0
-    assert p.n_split == -(-32768 // p.chunk) and p.merge == 1
-    assert (p.grid_x, p.grid_y, p.grid_z) == (p.n_split, 8, 16)
-    part = 16 * p.n_split * 32 * 130 * 4
-    assert p.ws_bytes == -(-part // 256) * 256 + 16 * 4
-    # about 8 CTAs per SM at full length
-    assert 4 * 152 <= 16 * 8 * p.n_split <= 16 * 152
+    assert p.streamk == 1 and p.merge == 1 and p.tile == 64
+    assert (p.grid_x, p.grid_y, p.grid_z) == (304, 1, 1) and p.n_split == 304
+    counters = -(-16 * 8 * 4 // 256) * 256
+    records = (304 + 16 * 8) * 4 * 130 * 4   # (CTAs + segments) x G=4 x (D+2) floats
+    assert p.ws_bytes == counters + records
+    q = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
+    assert q.streamk == 1 and q.grid_x == 1
 
 
-def test_plan_small_problem_is_one_chunk(gd):
-    p = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
-    assert p.n_split == 1 and p.merge == 0 and p.ws_bytes == 0 and p.chunk == 128
+def test_plan_long_context_chunked(gd):
+    # the default: chunks of min(8192, one wave of 2 CTAs per SM at max length) positions
+    p = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_F16, num_sms=152)
+    assert p.streamk == 0 and p.tile == 64 and p.chunk == 8192
+    assert p.n_split == 4 and p.merge == 1
+    assert (p.grid_x, p.grid_y, p.grid_z) == (4, 8, 16)
+    part = 16 * 4 * 32 * 130 * 4
+    counters = -(-16 * 8 * 4 // 256) * 256          # per-(row, KV head) arrival counters
+    assert p.ws_bytes == counters + -(-part // 256) * 256 + 16 * 4
+    # short rows: enough chunks for a wave (1 row x 8 KV heads x 4096 positions, D=64)
+    q = gd.plan(1, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
+    assert q.chunk == 128 and q.n_split == 32
+    r = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
+    assert r.n_split == 1 and r.merge == 0 and r.ws_bytes == 0 and r.chunk == 128
 
 
 def test_plan_selected_width_caps_chunks(gd):
-    # int8 + 1024 ids over a context of 8192: the visited list is 1024 long
+    # int8 + 1024 ids over a context of 8192: the visited list is 1024 long (chunked mode);
+    # the 12 query heads of a KV head spread over 3 CTAs of 4 heads each
     p = gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
-    assert p.tile == 64 and p.n_split == -(-1024 // p.chunk)
+    assert p.streamk == 0 and p.tile == 64 and p.n_split == -(-1024 // p.chunk)
+    assert p.grid_y == 4 * 3 and p.chunk == 64
+
+
+def test_plan_small_rows_are_not_split(gd):
+    # 256 positions of f16 D=64 are 64 KB of K/V: below the split threshold
+    p = gd.plan(1, 4, 1, 64, 256, -1, gd.KIND_F16, num_sms=152)
+    assert p.n_split == 1 and p.merge == 0
+    q = gd.plan(1, 4, 1, 64, 1025, -1, gd.KIND_F16, num_sms=152)   # 262 400 bytes: split
+    assert q.n_split > 1
 
 
 def test_plan_rejects_bad_shapes(gd):

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL_F16, assert_close, dev, forced_chunk
+from gpu_util import TOL_F16, assert_close, dev, f16_kernel, forced_chunk
 from gqa_decode_attention_03_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -44,7 +44,8 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     T, H, Hk, D, cap = 4, 32, 8, 128, 1 << 20
     q = torch.zeros((T, H, D), dtype=torch.float32, device="cuda")
     kc = torch.zeros((1, 16, Hk, D), dtype=torch.float16, device="cuda")
-    with forced_chunk(64):  # 64-position chunks over 2^20 positions: ~1 GB of partials
+    # the chunked split with 64-position chunks over 2^20 positions: ~1 GB of partials
+    with f16_kernel("chunked"), forced_chunk(64):
         assert gd.workspace_bytes(T, H, Hk, D, cap) > gd.NOALLOC_SCRATCH_BYTES
         # refused on the size alone.  kv_len is passed as NULL, so that even if the size check
         # let the call through, attn_decode_f16 would stop at its own argument check and
