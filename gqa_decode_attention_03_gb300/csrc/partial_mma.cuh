@@ -2,9 +2,8 @@
 //
 // Same CTA structure, TMA producer, stage ring, partial format, end-of-chunk merge and fused
 // last-CTA merge as partial_kernel (see partial_kernel.cuh), but q.k^T and p.v run as
-// mma.sync m16n8k16 with f32
-// accumulation instead of fp32 FMA: the CUDA-core kernel is issue-bound (about 64 warp
-// instructions per position and KV head), this one needs about 6.
+// mma.sync m16n8k16 with f32 accumulation instead of fp32 FMA: the CUDA-core kernel is
+// issue-bound (about 64 warp instructions per position and KV head), this one needs about 14.
 //
 // Exactness.  K and V are f16 already, so they enter the MMA unchanged.  q (fp32, pre-scaled by
 // scale * log2 e) and p (fp32 probabilities) are each split into an f16 "hi" part and an f16 "lo"
