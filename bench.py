@@ -181,8 +181,8 @@ def run_gpu(args):
     max_len = int(min(case.cache_cap, case.kv_len.max()))
     kind = gd.KIND_F16 if case.kind == "f16" else gd.KIND_Q8
     budget = -1 if case.ids is None else int(case.budget)
-    plan = gd.plan(T, H, Hk, D, max_len, budget, kind)
-    ws = gd.alloc_workspace(T, H, Hk, D, max_len, budget, kind)
+    plan = gd.plan(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
+    ws = gd.alloc_workspace(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
     out = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 

@@ -6,6 +6,7 @@
 
 #include "gqa_decode.h"
 #include "partial_kernel.cuh"
+#include "rows_mma.cuh"
 #include "streamk_mma.cuh"
 
 namespace gqa {
@@ -20,6 +21,7 @@ Variant pick_variant(int heads_per_cta);
 int head_split_for(int kind, int group);
 int stage_rows(int kind, int head_dim);
 bool use_streamk(int kind, int n_tok);  // f16 on the tensor cores with few enough rows
+int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim);
 
 // Defined in the inst_*.cu files, one per (cache kind, head_dim).
 cudaError_t launch_partial_f16_d64(Variant v, const CUtensorMap&, const CUtensorMap&,
@@ -60,6 +62,17 @@ inline cudaError_t launch_streamk_f16(int head_dim, const CUtensorMap& tk, const
   if (head_dim == 64) return launch_streamk_f16_d64(tk, tv, p, grid, s);
   if (head_dim == 128) return launch_streamk_f16_d128(tk, tv, p, grid, s);
   return launch_streamk_f16_d256(tk, tv, p, grid, s);
+}
+
+cudaError_t launch_rows_f16_d64(const CUtensorMap&, const CUtensorMap&, const PartialParams&,
+                               dim3, cudaStream_t);
+cudaError_t launch_rows_f16_d128(const CUtensorMap&, const CUtensorMap&, const PartialParams&,
+                                dim3, cudaStream_t);
+
+inline cudaError_t launch_rows_f16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const PartialParams& p, dim3 grid, cudaStream_t s) {
+  return head_dim == 64 ? launch_rows_f16_d64(tk, tv, p, grid, s)
+                        : launch_rows_f16_d128(tk, tv, p, grid, s);
 }
 
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,

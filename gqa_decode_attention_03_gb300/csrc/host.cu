@@ -143,6 +143,18 @@ bool use_streamk(int kind, int n_tok) {
   return m && std::strcmp(m, "streamk") == 0;
 }
 
+// Rows sharing a sequence are grouped (64 / group size rows per CTA) on the f16 tensor-core
+// path when the caller's cache holds fewer sequences than there are rows.
+int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
+  if (kind != GQA_KIND_F16 || n_seq >= n_tok || use_streamk(kind, n_tok)) return 1;
+  const char* k = std::getenv("GQA_F16_KERNEL");
+  if (k && std::strcmp(k, "fma") == 0) return 1;
+  const char* r = std::getenv("GQA_F16_ROWS");  // "off": one CTA per row (tests, comparison)
+  if (r && std::strcmp(r, "off") == 0) return 1;
+  if (head_dim == 256 || (group != 1 && group != 2 && group != 4 && group != 8)) return 1;
+  return 64 / group;
+}
+
 int stage_rows(int kind, int head_dim) {
   if (kind == GQA_KIND_F16) return head_dim == 64 ? 128 : (head_dim == 128 ? 64 : 32);
   return head_dim == 256 ? 64 : 128;
@@ -167,12 +179,14 @@ const char* gqa_status_string(gqa_status s) {
   return "GQA_UNKNOWN";
 }
 
-gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
-                            int budget, int kind, int num_sms, gqa_plan* plan) {
+gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                            int max_kv_len, int budget, int kind, int num_sms, gqa_plan* plan) {
   if (!plan) return fail(GQA_EINVAL, "plan is NULL");
   std::memset(plan, 0, sizeof *plan);
   gqa_status st = check_shape(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, kind);
   if (st != GQA_OK) return st;
+  if (n_seq <= 0) return fail(GQA_EINVAL, "n_seq %d must be > 0", n_seq);
+  plan->row_group = 1;
   if (kind == GQA_KIND_F16) budget = -1;
   if (budget == 0 || budget < -1) return fail(GQA_EINVAL, "budget %d (use -1 for dense)", budget);
   if (num_sms <= 0) {
@@ -203,8 +217,16 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
     return GQA_OK;
   }
   const int hsplit = gqa::head_split_for(kind, n_heads / n_kv_heads);
-  const long long units = (long long)n_tok * n_kv_heads * hsplit * std::max(nmax, 1LL);
-  long long chunk = (units + (long long)kCtasPerSm * num_sms - 1) / ((long long)kCtasPerSm * num_sms);
+  const int rgroup = gqa::row_group_for(kind, n_tok, n_seq, n_heads / n_kv_heads, head_dim);
+  // CTAs that do work: one per row, or per group of rows sharing a sequence (at least one group
+  // per sequence, and at least n_tok / rgroup groups)
+  const long long groups =
+      rgroup > 1 ? std::max<long long>((n_tok + rgroup - 1) / rgroup, std::min(n_seq, n_tok)) : n_tok;
+  plan->row_group = rgroup;
+  const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
+  // the grouped kernel is one 288-thread CTA per SM; the others fit two
+  const long long slots = (long long)(rgroup > 1 ? 1 : kCtasPerSm) * num_sms;
+  long long chunk = (units + slots - 1) / slots;
   chunk = std::min(chunk, kMaxChunk);
   const long long row_bytes = kind == GQA_KIND_F16 ? 4LL * head_dim : 2LL * (head_dim + head_dim / 32);
   if (nmax * row_bytes <= kMinSplitBytes) chunk = std::max(nmax, 1LL);
@@ -230,11 +252,11 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
   return GQA_OK;
 }
 
-size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int head_dim,
-                                   int max_kv_len, int budget, int kind) {
+size_t attn_decode_workspace_bytes(int n_tok, int n_seq, int n_heads, int n_kv_heads,
+                                   int head_dim, int max_kv_len, int budget, int kind) {
   gqa_plan plan;
-  if (attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind, 0, &plan) !=
-      GQA_OK)
+  if (attn_decode_plan(n_tok, n_seq, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind, 0,
+                       &plan) != GQA_OK)
     return 0;
   return plan.ws_bytes;
 }
@@ -268,8 +290,8 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   const int max_len = (int)std::min<int64_t>(max_kv_len, cache_cap);
 
   gqa_plan plan;
-  st = attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_len, ids ? budget : -1, kind, 0,
-                        &plan);
+  st = attn_decode_plan(n_tok, n_seq, n_heads, n_kv_heads, head_dim, max_len, ids ? budget : -1,
+                        kind, 0, &plan);
   if (st != GQA_OK) return st;
   if (plan.merge && (!ws || ws_bytes < plan.ws_bytes || !aligned16(ws)))
     return fail(GQA_EWORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu",
@@ -342,11 +364,17 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     var.mma = !(k && std::strcmp(k, "fma") == 0);
   }
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-  cudaError_t e = plan.streamk
-                      ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
-                      : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
+  cudaError_t e =
+      plan.streamk        ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
+      : plan.row_group > 1 ? gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream)
+                           : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
-  return GQA_OK;  // split rows are merged inside the kernel by each (row, KV head)'s last CTA
+  if (plan.merge && !plan.streamk && plan.row_group > 1) {
+    // grouped rows: their partials are merged by merge_kernel, one CTA per (head, row)
+    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  }
+  return GQA_OK;  // otherwise split rows were merged inside the kernel by their last CTA
 }
 
 }  // namespace

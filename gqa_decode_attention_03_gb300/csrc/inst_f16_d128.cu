@@ -3,6 +3,7 @@
 // GQA_F16_SPLIT=chunked) and the CUDA-core kernel (GQA_F16_KERNEL=fma; comparison and parity
 // cross-check).
 #include "dispatch.h"
+#include "rows_mma.cuh"
 #include "streamk_mma.cuh"
 
 namespace gqa {
@@ -46,6 +47,16 @@ static cudaError_t launch_sk(const CUtensorMap& tk, const CUtensorMap& tv, const
 cudaError_t launch_streamk_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const PartialParams& p, dim3 grid, cudaStream_t s) {
   return p.group <= 8 ? launch_sk<1>(tk, tv, p, grid, s) : launch_sk<2>(tk, tv, p, grid, s);
+}
+
+cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                const PartialParams& p, dim3 grid, cudaStream_t s) {
+  using C = RowsCfg<128>;
+  const void* fn = reinterpret_cast<const void*>(&partial_mma_rows_kernel<128>);
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  partial_mma_rows_kernel<128><<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_partial_f16_d128(Variant v, const CUtensorMap& tk, const CUtensorMap& tv,

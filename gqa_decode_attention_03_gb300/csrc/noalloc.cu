@@ -63,7 +63,7 @@ gqa_status attn_decode_f16_noalloc(const float* q, const uint16_t* k_cache,
   }
   // The same plan attn_decode_f16 will use; reject what does not fit before anything launches.
   const int64_t len = max_kv_len < cache_cap ? max_kv_len : cache_cap;
-  const size_t need = attn_decode_workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim,
+  const size_t need = attn_decode_workspace_bytes(n_tok, n_seq, n_heads, n_kv_heads, head_dim,
                                                   len < 0 ? -1 : (int)len, -1, GQA_KIND_F16);
   if (need > (size_t)GQA_NOALLOC_SCRATCH_BYTES) {
     char buf[256];

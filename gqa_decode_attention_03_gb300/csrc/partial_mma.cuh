@@ -186,14 +186,23 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
       const int nv = min(max(c1 - (c0 + i * C::TP + r0), 0), 16);  // valid rows, a prefix
       if (nv == 0) continue;
       // -- S = Q . K^T for 16 positions (two n-tiles of 8)
+      // four independent accumulator chains (n-tile x k-step parity), summed after
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        uint32_t kb[4];
+      for (int ks = 0; ks < C::KS; ks += 2) {
+        uint32_t kb[4], kc[4];
         ldsm_x4(kb, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + (mi & 1), C::TP));
+        ldsm_x4(kc, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + 2 + (mi & 1), C::TP));
         mma_f16(sc[0], qa[ks], kb[0], kb[1]);
         mma_f16(sc[1], qa[ks], kb[2], kb[3]);
+        mma_f16(sd[0], qa[ks + 1], kc[0], kc[1]);
+        mma_f16(sd[1], qa[ks + 1], kc[2], kc[3]);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
       // -- scores of head hh at positions nt*8 + 2*tig + j (hi row + lo row)
       float x[2][2];
       float mt = -INFINITY;

@@ -30,7 +30,8 @@ NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_dec
 class GqaPlan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int), ("n_split", ctypes.c_int), ("tile", ctypes.c_int),
                 ("grid_x", ctypes.c_int), ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
-                ("merge", ctypes.c_int), ("streamk", ctypes.c_int), ("ws_bytes", ctypes.c_size_t)]
+                ("merge", ctypes.c_int), ("streamk", ctypes.c_int), ("row_group", ctypes.c_int),
+                ("ws_bytes", ctypes.c_size_t)]
 
 
 class GqaError(RuntimeError):
@@ -45,9 +46,9 @@ def _load():
                           "`python -m gqa_decode_attention_03_gb300.build_lib`")
     lib = ctypes.CDLL(str(_LIB_PATH))
     P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-    lib.attn_decode_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(GqaPlan)]
+    lib.attn_decode_plan.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.POINTER(GqaPlan)]
     lib.attn_decode_plan.restype = I
-    lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
     lib.attn_decode_workspace_bytes.restype = SZ
     lib.attn_decode_f16.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I64, I, F, P, SZ, P, P]
     lib.attn_decode_f16.restype = I
@@ -97,24 +98,27 @@ def _need(x, dtype, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {x.dim()}")
 
 
-def plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16, num_sms=0):
-    """The split plan the decode calls use (host only; num_sms 0 queries the device)."""
+def plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16, num_sms=0,
+         n_seq=None):
+    """The split plan the decode calls use (host only; num_sms 0 queries the device).
+    n_seq: sequences in the cache (default n_tok: every row its own sequence)."""
     p = GqaPlan()
-    _check(LIB.attn_decode_plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind,
-                                num_sms, ctypes.byref(p)))
+    _check(LIB.attn_decode_plan(n_tok, n_tok if n_seq is None else n_seq, n_heads, n_kv_heads,
+                                head_dim, max_kv_len, budget, kind, num_sms, ctypes.byref(p)))
     return p
 
 
-def workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16):
-    return int(LIB.attn_decode_workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len,
-                                               budget, kind))
+def workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16,
+                    n_seq=None):
+    return int(LIB.attn_decode_workspace_bytes(n_tok, n_tok if n_seq is None else n_seq, n_heads,
+                                               n_kv_heads, head_dim, max_kv_len, budget, kind))
 
 
 def alloc_workspace(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16,
-                    device=None):
+                    device=None, n_seq=None):
     """A zeroed workspace: its leading arrival counters must be zero before the first call (every
     call leaves them zero again), so one workspace can be reused across calls and shapes."""
-    n = workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind)
+    n = workspace_bytes(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget, kind, n_seq)
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
@@ -143,7 +147,7 @@ def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv
         out = torch.empty_like(q)
     _need(out, torch.float32, "out", 3)
     if ws is None:
-        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_F16, q.device)
+        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_F16, q.device, n_seq)
     _check(LIB.attn_decode_f16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(kv_len),
                                _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale, _ptr(ws),
                                ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
@@ -206,7 +210,7 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
         out = torch.empty_like(q)
     _need(out, torch.float32, "out", 3)
     if ws is None:
-        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), b, KIND_Q8, q.device)
+        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), b, KIND_Q8, q.device, n_seq)
     _check(LIB.attn_decode_q8_sel(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), _ptr(ids),
                                   0 if ids is None else budget, _ptr(out), _ptr(kv_len),
                                   _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale,

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 2
+#define GQA_ABI_VERSION 3
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -80,9 +80,13 @@ typedef struct gqa_plan {
   int grid_x, grid_y, grid_z; /* launch grid: chunked (n_split, n_kv_heads, n_tok);
                                  stream-K (CTAs, 1, 1) */
   int merge;         /* 1 when rows may be split: partials go to ws and are merged inside the
-                        same kernel by whichever CTA (or warp) finishes a row's KV head last */
+                        same kernel by whichever CTA finishes a row's KV head last, or (rows
+                        grouped by sequence) by a second kernel, one CTA per (head, row) */
   int streamk;       /* 1: stream-K split (f16 caches): the (row, KV head, position) stream is
                         cut into equal shares, one per CTA of a persistent grid */
+  int row_group;     /* rows one CTA serves from a shared K/V tile: > 1 when rows may share a
+                        sequence (n_seq < n_tok; f16 caches, head_dim 64 or 128, group size
+                        1, 2, 4 or 8), else 1 */
   size_t ws_bytes;   /* workspace the call needs (0 when merge == 0) */
 } gqa_plan;
 
@@ -94,10 +98,14 @@ typedef struct gqa_plan {
  * GQA_F16_SPLIT=streamk in the environment, f16 calls with n_tok <= 8192 use the stream-K
  * split instead: a persistent grid of up to two CTAs per SM, each taking an equal share of
  * all rows' KV positions.
- * num_sms <= 0 queries the current CUDA device.  budget < 0 means dense (no id list).
+ * When rows may share a sequence (n_seq < n_tok) an f16 call groups the rows of each run of
+ * equal seq_of[] values (up to 64 / group size rows) into one CTA that reads each K/V tile once
+ * for all of them; the chunks are then sized for the groups rather than the rows.
+ * num_sms <= 0 queries the current CUDA device.  budget < 0 means dense (no id list).  n_seq
+ * is the number of sequences in the cache, as passed to the decode call.
  * Returns GQA_EINVAL on bad sizes, GQA_EUNSUPPORTED for group sizes > 16.
  */
-gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim,
+gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, int head_dim,
                             int max_kv_len, int budget, int kind, int num_sms, gqa_plan* plan);
 
 /*
@@ -108,8 +116,8 @@ gqa_status attn_decode_plan(int n_tok, int n_heads, int n_kv_heads, int head_dim
  * n_heads * (head_dim + 2) * 4 bytes (rounded up to 256) and n_valid (n_tok * 4 bytes);
  * stream-K mode (CTAs + n_tok * n_kv_heads) * group * (head_dim + 2) * 4 bytes.
  */
-size_t attn_decode_workspace_bytes(int n_tok, int n_heads, int n_kv_heads, int head_dim,
-                                   int max_kv_len, int budget, int kind);
+size_t attn_decode_workspace_bytes(int n_tok, int n_seq, int n_heads, int n_kv_heads,
+                                   int head_dim, int max_kv_len, int budget, int kind);
 
 /*
  * attn_decode_f16 -- decode attention over an f16 K/V cache.

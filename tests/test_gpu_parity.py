@@ -250,3 +250,41 @@ def test_workspace_reuse_leaves_counters_zero():
             torch.cuda.synchronize()
             assert_close(got.cpu().numpy(), oracle_ref(case), TOL_F16, "reused ws")
             assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
+
+
+# ----------------------------------------------------------------------------- row grouping
+
+@pytest.mark.parametrize("chunk", [None, 64, 256])
+@pytest.mark.parametrize("D,G", [(D, G) for D in (64, 128) for G in (1, 2, 4, 8)])
+def test_rows_grouped_by_sequence(D, G, chunk):
+    """Rows sharing a sequence are served from one staged K/V tile per group: runs longer than a
+    group (G=8: 8 rows), causal and ragged lengths inside a group, an empty row, a row of one
+    position, and sequences interleaved."""
+    seq_of = [0] * 11 + [1, 1, 2] + [0] * 3 + [2]
+    L = [400 + 7 * r for r in range(11)] + [1, 399, 0, 300, 5, 401, 250]
+    case = W.make_f16_case(500 + D + G, len(seq_of), 2 * G, 2, D, L, cache_cap=480,
+                           seq_of=seq_of, n_seq=3, scale=1 / math.sqrt(D))
+    gd = _gd()
+    assert gd.plan(len(seq_of), 2 * G, 2, D, 480, n_seq=3).row_group == 64 // G
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with forced_chunk(chunk):
+        got = run_case(case, err=err).cpu().numpy()
+    assert int(err.item()) == 0
+    assert_close(got, oracle_ref(case), TOL_F16, f"rows D{D} G{G} chunk{chunk}")
+    assert (got[13] == 0).all()
+
+
+def test_rows_grouped_matches_per_row_kernel():
+    """The prefill chunk (16 causal rows over one cache) with and without row grouping."""
+    case = W.prefill_chunk()
+    got = run_case(case).cpu().numpy()
+    with _rows_off():
+        per_row = run_case(case).cpu().numpy()
+    ref = oracle_ref(case)
+    assert_close(got, ref, TOL_F16, "grouped")
+    assert_close(per_row, ref, TOL_F16, "per row")
+
+
+def _rows_off():
+    from gpu_util import _env
+    return _env(GQA_F16_ROWS="off")

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(gd):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in the header but not exported"
     assert set(declared_functions()) <= set(gd.EXPORTS) | set(declared_functions())
-    assert gd.LIB.gqa_abi_version() == 2
+    assert gd.LIB.gqa_abi_version() == 3
 
 
 def test_status_strings(gd):
@@ -82,6 +82,19 @@ def test_plan_selected_width_caps_chunks(gd):
     p = gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
     assert p.streamk == 0 and p.tile == 64 and p.n_split == -(-1024 // p.chunk)
     assert p.grid_y == 4 * 3 and p.chunk == 64
+
+
+def test_plan_groups_rows_sharing_a_sequence(gd):
+    # 16 causal rows over one sequence (n_seq 1): one group of 16 rows (G=4); chunks sized for
+    # 1 group x 8 KV heads on one CTA per SM: 8 * 8192 / 152 -> 432 -> 448 positions, 19 chunks
+    p = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1)
+    assert p.row_group == 16 and p.chunk == 448 and p.n_split == 19
+    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 16)
+    # every row its own sequence, D=256, int8, or group size 3: no grouping
+    assert gd.plan(16, 32, 8, 128, 8192, num_sms=152).row_group == 1
+    assert gd.plan(16, 32, 8, 256, 8192, num_sms=152, n_seq=1).row_group == 1
+    assert gd.plan(16, 48, 4, 128, 8192, 64, gd.KIND_Q8, num_sms=152, n_seq=1).row_group == 1
+    assert gd.plan(16, 24, 8, 128, 8192, num_sms=152, n_seq=1).row_group == 1
 
 
 def test_plan_small_rows_are_not_split(gd):
