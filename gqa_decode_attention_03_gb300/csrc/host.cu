@@ -143,7 +143,7 @@ bool use_streamk(int kind, int n_tok) {
   return m && std::strcmp(m, "streamk") == 0;
 }
 
-// Rows sharing a sequence are grouped (64 / group size rows per CTA) on the f16 tensor-core
+// Rows sharing a sequence are grouped (32 / group size rows per CTA) on the f16 tensor-core
 // path when the caller's cache holds fewer sequences than there are rows.
 int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
   if (kind != GQA_KIND_F16 || n_seq >= n_tok || use_streamk(kind, n_tok)) return 1;
@@ -152,7 +152,7 @@ int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
   const char* r = std::getenv("GQA_F16_ROWS");  // "off": one CTA per row (tests, comparison)
   if (r && std::strcmp(r, "off") == 0) return 1;
   if (head_dim == 256 || (group != 1 && group != 2 && group != 4 && group != 8)) return 1;
-  return 64 / group;
+  return 32 / group;  // 4 consumer warps x 8 (row, head) pairs
 }
 
 int stage_rows(int kind, int head_dim) {
@@ -224,8 +224,7 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
       rgroup > 1 ? std::max<long long>((n_tok + rgroup - 1) / rgroup, std::min(n_seq, n_tok)) : n_tok;
   plan->row_group = rgroup;
   const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
-  // the grouped kernel is one 288-thread CTA per SM; the others fit two
-  const long long slots = (long long)(rgroup > 1 ? 1 : kCtasPerSm) * num_sms;
+  const long long slots = (long long)kCtasPerSm * num_sms;
   long long chunk = (units + slots - 1) / slots;
   chunk = std::min(chunk, kMaxChunk);
   const long long row_bytes = kind == GQA_KIND_F16 ? 4LL * head_dim : 2LL * (head_dim + head_dim / 32);
@@ -242,7 +241,7 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   plan->tile = tile;
   plan->grid_x = (int)n_split;
   plan->grid_y = n_kv_heads * hsplit;
-  plan->grid_z = n_tok;
+  plan->grid_z = rgroup > 1 ? (int)std::min<long long>(groups, n_tok) : n_tok;  // group slots
   plan->merge = n_split > 1 ? 1 : 0;
   if (plan->merge) {
     const size_t cnt = ((size_t)n_tok * plan->grid_y * sizeof(uint32_t) + 255) / 256 * 256;

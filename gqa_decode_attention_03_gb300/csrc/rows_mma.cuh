@@ -17,11 +17,13 @@
 // there.  Split rows are merged afterwards by merge_kernel (one CTA per row and head): a
 // group's rows bring many partials at once, too many for one last CTA to merge quickly.
 //
-// Rows.  The grid stays (chunks, KV heads, rows); the CTA of row t works only if t leads a
-// group: groups of consecutive rows with equal seq_of[] start at every multiple of R and
-// wherever seq_of[] changes.  Every other CTA exits at once.  A row keeps its own chunk count
-// ceil(L / chunk) (n_valid), so a row shorter than the group's longest simply has no partials
-// for the chunks past its end.
+// Rows.  Groups of consecutive rows with equal seq_of[] start at every multiple of R and
+// wherever seq_of[] changes.  The grid is (chunks, KV heads, slots): slot z serves groups
+// z, z + slots, ..., found on the device by a warp-wide ballot over seq_of[], with the TMA ring
+// running on from one group to the next.  The host sizes the slots from the sequence count, so
+// a prefill chunk (one sequence) is one slot and no CTA is launched only to exit.  A row keeps
+// its own chunk count ceil(L / chunk) (n_valid), so a row shorter than the group's longest
+// simply has no partials for the chunks past its end.
 #pragma once
 
 #include "partial_mma.cuh"
@@ -39,7 +41,9 @@ struct RowsCfg {
   static constexpr int BOX_BYTES = TP * 128;
   static constexpr int KV_BYTES = 2 * NBOX * BOX_BYTES;
   static constexpr int STAGE_BYTES = KV_BYTES;
-  static constexpr int NCW = 8;                   // consumer warps: 64 (row, head) pairs
+  static constexpr int NCW = 4;                   // consumer warps: 32 (row, head) pairs, so
+                                                  // two CTAs fit an SM (16 warps to hide the
+                                                  // MMA / softmax latency of each block)
   static constexpr int MAX_THREADS = 32 * (NCW + 1);
   static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + 2 * NST * 8;
   static constexpr float RESCALE_LOG2 = 8.f;
@@ -50,58 +54,87 @@ __device__ __forceinline__ int rows_seq(const PartialParams& p, int t) {
   return p.seq_of ? __ldg(p.seq_of + t) : t;
 }
 
+// Group leaders: a group starts at every multiple of R and wherever seq_of[] changes.
+__device__ __forceinline__ bool rows_is_leader(const PartialParams& p, int t, int R) {
+  return t % R == 0 || rows_seq(p, t - 1) != rows_seq(p, t);
+}
+
+// Warp-cooperative search for the k-th group leader, scanning rows forward 32 at a time from a
+// cursor (scan_t, scan_cnt = leaders before scan_t) that only moves forward; -1 past the last.
+// Every lane of the warp calls it with the same arguments and gets the same answer.
+__device__ __forceinline__ int rows_find_leader(const PartialParams& p, int R, int k, int& scan_t,
+                                                int& scan_cnt, int lane) {
+  while (scan_t < p.n_tok) {
+    const int t = scan_t + lane;
+    const unsigned m = __ballot_sync(0xffffffffu, t < p.n_tok && rows_is_leader(p, t, R));
+    const int n = __popc(m);
+    if (scan_cnt + n > k) {
+      unsigned mm = m;
+      for (int i = 0; i < k - scan_cnt; ++i) mm &= mm - 1;  // drop the earlier leaders
+      return scan_t + __ffs(mm) - 1;
+    }
+    scan_cnt += n;
+    scan_t += 32;
+  }
+  return -1;
+}
+
+// One group: its leader row, row count, sequence and longest (clamped) length.  Warp-wide.
+struct RowGroup {
+  int t0, nr, s, lmax;
+};
+
+__device__ __forceinline__ int rows_len(const PartialParams& p, int t, bool seq_ok, int* err) {
+  const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
+  int L = __ldg(p.kv_len + t);
+  if (L < 0 || L > lmax) {
+    *err |= GQA_ERR_KVLEN_RANGE;
+    L = L < 0 ? 0 : lmax;
+  }
+  if (!seq_ok) {
+    *err |= GQA_ERR_SEQ_RANGE;
+    L = 0;
+  }
+  return L;
+}
+
+__device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, int R, int lane) {
+  RowGroup gr;
+  gr.t0 = t0;
+  gr.s = rows_seq(p, t0);
+  // rows t0 + 1 + i belong to the group while seq_of stays and no multiple of R is crossed;
+  // checked 32 rows at a time (R can reach 64)
+  gr.nr = 1;
+  for (int base = 0; base < R - 1; base += 32) {
+    const int i = base + lane, t = t0 + 1 + i;
+    const bool same = i < R - 1 && t < p.n_tok && t % R != 0 && rows_seq(p, t) == gr.s;
+    const unsigned run = __ballot_sync(0xffffffffu, same);
+    const int lead = __ffs(~run) - 1;  // leading rows of this window inside the group (-1: 32)
+    gr.nr += lead < 0 ? 32 : lead;
+    if (lead >= 0) break;
+  }
+  const bool seq_ok = gr.s >= 0 && gr.s < p.n_seq;
+  int err = 0;
+  int L = 0;
+  for (int jj = lane; jj < gr.nr; jj += 32) L = max(L, rows_len(p, t0 + jj, seq_ok, &err));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L = max(L, __shfl_xor_sync(0xffffffffu, L, o));
+  gr.lmax = L;
+  return gr;
+}
+
 template <int D>
-__global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 1)
+__global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
     partial_mma_rows_kernel(const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const PartialParams p) {
   using C = RowsCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_len[64];  // clamped length of each row of the group
-  const int c = blockIdx.x, g = blockIdx.y, t0 = blockIdx.z;
+  const int c = blockIdx.x, g = blockIdx.y, slot = blockIdx.z, nslots = gridDim.z;
   const int G = p.group;             // 1, 2, 4 or 8
   const int rpw = 8 / G;             // rows per warp
   const int R = rpw * C::NCW;        // rows per group at most
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- is row t0 a group leader?  Groups start at every multiple of R and wherever seq_of
-  //      changes, and run on while seq_of stays the same (uniform over the CTA).
-  const int s = rows_seq(p, t0);
-  if (t0 % R != 0 && rows_seq(p, t0 - 1) == s) return;
-  int nr = 1;  // rows of this group
-  while ((t0 + nr) % R != 0 && t0 + nr < p.n_tok && rows_seq(p, t0 + nr) == s) ++nr;
-
-  // ---- the rows' lengths (clamped and flagged like the per-row kernels)
-  const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
-  const bool seq_ok = s >= 0 && s < p.n_seq;
-  if (threadIdx.x < nr) {
-    int L = __ldg(p.kv_len + t0 + threadIdx.x);
-    int err = 0;
-    if (L < 0 || L > lmax) {
-      err |= GQA_ERR_KVLEN_RANGE;
-      L = L < 0 ? 0 : lmax;
-    }
-    if (!seq_ok) {
-      err |= GQA_ERR_SEQ_RANGE;
-      L = 0;
-    }
-    if (err && c == 0 && g == 0) flag_error(p.err, err);
-    if (c == 0 && g == 0 && p.merge) p.n_valid[t0 + threadIdx.x] = (L + p.chunk - 1) / p.chunk;
-    s_len[threadIdx.x] = L;
-  }
-  __syncthreads();
-  int Lmax = 0;
-  for (int j = 0; j < nr; ++j) Lmax = max(Lmax, s_len[j]);
   const int c0 = c * p.chunk;
-  // empty rows: zeros, written by chunk 0 (flash_attention.metal, seq_len == 0)
-  if (c == 0)
-    for (int j = 0; j < nr; ++j)
-      if (s_len[j] == 0)
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-          p.out[((size_t)(t0 + j) * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
-  if (c0 >= Lmax) return;
-  const int c1 = min(c0 + p.chunk, Lmax);
-  const int ntiles = (c1 - c0 + C::TP - 1) / C::TP;
-  const int nw = (nr * G + 7) / 8;  // consumer warps with rows
 
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
@@ -110,147 +143,227 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], nw);
+      mbar_init(&empty[i], C::NCW);
     }
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == C::NCW) {  // ---- producer warp
-    if (lane == 0)
-      produce_tma<C>(&tmK, &tmV, stages, full, empty, ntiles, g,
-                     s * static_cast<int>(p.cache_cap) + c0, p.err);
+  // Every warp walks the same groups (k = slot, slot + nslots, ...) in the same order, so the
+  // producer's tiles and the consumers' waits line up across groups.
+  int scan_t = 0, scan_cnt = 0;
+
+  if (warp == C::NCW) {  // ---- producer warp: lane 0 issues, the warp walks the groups
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    int it = 0;
+    bool ok = true;
+    for (int k = slot; ok; k += nslots) {
+      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      if (t0 < 0) break;
+      const RowGroup gr = rows_group(p, t0, R, lane);
+      if (c0 >= gr.lmax) continue;
+      const int c1 = min(c0 + p.chunk, gr.lmax);
+      const int zb = gr.s * static_cast<int>(p.cache_cap) + c0;
+      for (int pos = c0; pos < c1; pos += C::TP, ++it) {
+        const int st = it % C::NST;
+        if (it >= C::NST &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((it / C::NST) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[st], C::KV_BYTES);
+          uint8_t* sk = stages + st * C::STAGE_BYTES;
+          uint8_t* sv = sk + C::NBOX * C::BOX_BYTES;
+#pragma unroll
+          for (int bx = 0; bx < C::NBOX; ++bx) {
+            tma_load_3d(sk + bx * C::BOX_BYTES, &tmK, bx * 64, g, zb + pos - c0, &full[st]);
+            tma_load_3d(sv + bx * C::BOX_BYTES, &tmV, bx * 64, g, zb + pos - c0, &full[st]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      if (!ok) flag_error(p.err, GQA_ERR_TIMEOUT);
+      for (int st = 0; st < C::NST && st < it; ++st) {  // the last load of each stage lands
+        const int last = st + ((it - 1 - st) / C::NST) * C::NST;
+        if (!mbar_wait(&full[st], (last / C::NST) & 1)) flag_error(p.err, GQA_ERR_TIMEOUT);
+      }
+    }
     return;
   }
-  if (warp >= nw) return;  // no rows for this warp
 
-  // ---- consumer warp: pairs (row j, head h) with j = warp * rpw + gid / G, h = gid % G
+  // ---- consumer warps: pairs (row j, head h) with j = warp * rpw + gid / G, h = gid % G
   const int gid = lane >> 2, tig = lane & 3;
-  const int j = warp * rpw + gid / G, h = gid % G;
-  const bool rv = j < nr;                  // this thread's pair is a real row
-  const int t = t0 + (rv ? j : 0);
-  const int Lr = rv ? s_len[j] : 0;        // this row's length
+  const int h = gid % G;
   const int head = g * G + h;
-
-  uint32_t qa[C::KS][4];
-  {
-    const float* qrow = p.q + ((size_t)t * p.n_heads + head) * D;
-    const float f = rv ? p.scale_log2 : 0.f;
-#pragma unroll
-    for (int ks = 0; ks < C::KS; ++ks) {
-      const int d0 = ks * 16 + 2 * tig;
-      const float2 x0 = __ldg(reinterpret_cast<const float2*>(qrow + d0));
-      const float2 x1 = __ldg(reinterpret_cast<const float2*>(qrow + d0 + 8));
-      split_hi_lo(x0.x * f, x0.y * f, qa[ks][0], qa[ks][1]);
-      split_hi_lo(x1.x * f, x1.y * f, qa[ks][2], qa[ks][3]);
-    }
-  }
-  float o[C::NT][4];
-#pragma unroll
-  for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
   const int mi = lane >> 3, rr = lane & 7;
+  int it = 0;
   bool ok = true;
 
-  for (int i = 0; i < ntiles; ++i) {
-    const int st = i % C::NST;
-    ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / C::NST) & 1));
-    if (!ok) break;
-    const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
-    const uint32_t sv = sk + C::NBOX * C::BOX_BYTES;
-#pragma unroll
-    for (int b = 0; b < C::NB16; ++b) {
-      const int r0 = b * 16;
-      const int base = c0 + i * C::TP + r0;             // cache position of the block's row 0
-      const int nv = min(max(c1 - base, 0), 16);         // rows holding data for some row
-      if (nv == 0) continue;
-      const int nrow = min(max(Lr - base, 0), 16);       // rows inside this thread's window
-      // four independent accumulator chains (n-tile x k-step parity), summed after
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < C::KS; ks += 2) {
-        uint32_t kb[4], kc[4];
-        ldsm_x4(kb, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + (mi & 1), C::TP));
-        ldsm_x4(kc, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + 2 + (mi & 1), C::TP));
-        mma_f16(sc[0], qa[ks], kb[0], kb[1]);
-        mma_f16(sc[1], qa[ks], kb[2], kb[3]);
-        mma_f16(sd[0], qa[ks + 1], kc[0], kc[1]);
-        mma_f16(sd[1], qa[ks + 1], kc[2], kc[3]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
-      float x[2][2];
-      float mt = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const float v = sc[nt][jj] + sc[nt][2 + jj];
-          x[nt][jj] = (nt * 8 + 2 * tig + jj) < nrow ? v : -INFINITY;
-          mt = fmaxf(mt, x[nt][jj]);
+  for (int k = slot; ok; k += nslots) {
+    const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+    if (t0 < 0) break;
+    const RowGroup gr = rows_group(p, t0, R, lane);
+    const bool seq_ok = gr.s >= 0 && gr.s < p.n_seq;
+    if (c == 0 && warp == 0) {  // per-row bookkeeping: flags, chunk counts, empty rows
+      for (int jb = 0; jb < gr.nr; jb += 32) {
+        int err = 0;
+        const int L = jb + lane < gr.nr ? rows_len(p, t0 + jb + lane, seq_ok, &err) : 0;
+        if (jb + lane < gr.nr) {
+          if (err && g == 0) flag_error(p.err, err);
+          if (g == 0 && p.merge) p.n_valid[t0 + jb + lane] = (L + p.chunk - 1) / p.chunk;
         }
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      // a pair whose row ends before this block keeps mt = -inf: nothing to add
-      const bool grow = mt != -INFINITY && mt > m_run + C::RESCALE_LOG2;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mt : m_run;
-        const float corr = grow ? fast_exp2(m_run - m_new) : 1.f;
-        m_run = m_new;
-        l_run *= corr;
-#pragma unroll
-        for (int n = 0; n < C::NT; ++n) {
-          o[n][0] *= corr;
-          o[n][1] *= corr;
-          o[n][2] *= corr;
-          o[n][3] *= corr;
+        for (int jj = 0; jj < 32 && jb + jj < gr.nr; ++jj) {
+          if (__shfl_sync(0xffffffffu, L, jj) != 0) continue;  // empty row: zeros
+          for (int i = lane; i < G * D; i += 32)
+            p.out[((size_t)(t0 + jb + jj) * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
         }
-      }
-      float pr[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          pr[nt][jj] = m_run == -INFINITY ? 0.f : fast_exp2(x[nt][jj] - m_run);
-          l_run += pr[nt][jj];
-        }
-      uint32_t pa[4];
-      split_hi_lo(pr[0][0], pr[0][1], pa[0], pa[1]);
-      split_hi_lo(pr[1][0], pr[1][1], pa[2], pa[3]);
-      const bool tail = nv < 16;
-      const uint32_t mk0 =
-          ((2 * tig < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 1 < nv) ? 0xffff0000u : 0u);
-      const uint32_t mk1 =
-          ((2 * tig + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 9 < nv) ? 0xffff0000u : 0u);
-#pragma unroll
-      for (int np = 0; np < C::NT / 2; ++np) {
-        uint32_t vb[4];
-        ldsm_x4_t(vb, sv + swz_off(r0 + (mi & 1) * 8 + rr, np * 2 + (mi >> 1), C::TP));
-        if (tail) {
-          vb[0] &= mk0;
-          vb[1] &= mk1;
-          vb[2] &= mk0;
-          vb[3] &= mk1;
-        }
-        mma_f16(o[2 * np], pa, vb[0], vb[1]);
-        mma_f16(o[2 * np + 1], pa, vb[2], vb[3]);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-  if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
+    if (c0 >= gr.lmax) continue;
+    const int c1 = min(c0 + p.chunk, gr.lmax);
+    const int j = warp * rpw + gid / G;
+    const bool rv = j < gr.nr;               // this thread's pair is a real row
+    const int t = t0 + (rv ? j : 0);
+    int dummy = 0;
+    const int Lr = rv ? rows_len(p, t, seq_ok, &dummy) : 0;  // this row's length
+    const bool active = warp * rpw < gr.nr;  // the warp has rows in this group
 
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    uint32_t qa[C::KS][4];
+    {
+      const float* qrow = p.q + ((size_t)t * p.n_heads + head) * D;
+      const float f = rv ? p.scale_log2 : 0.f;
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        const int d0 = ks * 16 + 2 * tig;
+        const float2 x0 = __ldg(reinterpret_cast<const float2*>(qrow + d0));
+        const float2 x1 = __ldg(reinterpret_cast<const float2*>(qrow + d0 + 8));
+        split_hi_lo(x0.x * f, x0.y * f, qa[ks][0], qa[ks][1]);
+        split_hi_lo(x1.x * f, x1.y * f, qa[ks][2], qa[ks][3]);
+      }
+    }
+    float o[C::NT][4];
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
 
-  // ---- this thread's (row, head): output, or the chunk's partial plus the row's ticket
-  const bool has = rv && c0 < Lr;  // the chunk holds positions of this row
-  if (!p.merge) {
-    if (has) {
+    for (int pos0 = c0; pos0 < c1; pos0 += C::TP, ++it) {
+      const int st = it % C::NST;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (it / C::NST) & 1));
+      if (!ok) break;
+      if (active) {
+        const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
+        const uint32_t sv = sk + C::NBOX * C::BOX_BYTES;
+        // q.k^T for every 16-position block of the stage first (independent MMA chains), then the
+        // softmax and p.v of each block: the scheduler can overlap one block's softmax with
+        // another's MMAs
+        float sc[C::NB16][2][4];
+#pragma unroll
+        for (int b = 0; b < C::NB16; ++b) {
+          const int r0 = b * 16;
+          float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[b][nt][e] = 0.f;
+          if (pos0 + r0 >= c1) continue;  // block past the chunk end
+#pragma unroll
+          for (int ks = 0; ks < C::KS; ks += 2) {
+            uint32_t kb[4], kc[4];
+            ldsm_x4(kb, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + (mi & 1), C::TP));
+            ldsm_x4(kc, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + 2 + (mi & 1), C::TP));
+            mma_f16(sc[b][0], qa[ks], kb[0], kb[1]);
+            mma_f16(sc[b][1], qa[ks], kb[2], kb[3]);
+            mma_f16(sd[0], qa[ks + 1], kc[0], kc[1]);
+            mma_f16(sd[1], qa[ks + 1], kc[2], kc[3]);
+          }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[b][nt][e] += sd[nt][e];
+        }
+#pragma unroll
+        for (int b = 0; b < C::NB16; ++b) {
+          const int r0 = b * 16;
+          const int base = pos0 + r0;  // cache position of the block's row 0
+          const int nv = min(max(c1 - base, 0), 16);         // rows holding data for some row
+          if (nv == 0) continue;
+          const int nrow = min(max(Lr - base, 0), 16);       // rows inside this thread's window
+          float x[2][2];
+          float mt = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const float v = sc[b][nt][jj] + sc[b][nt][2 + jj];
+              x[nt][jj] = (nt * 8 + 2 * tig + jj) < nrow ? v : -INFINITY;
+              mt = fmaxf(mt, x[nt][jj]);
+            }
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+          // a pair whose row ends before this block keeps mt = -inf: nothing to add
+          const bool grow = mt != -INFINITY && mt > m_run + C::RESCALE_LOG2;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? mt : m_run;
+            const float corr = grow ? fast_exp2(m_run - m_new) : 1.f;
+            m_run = m_new;
+            l_run *= corr;
+#pragma unroll
+            for (int n = 0; n < C::NT; ++n) {
+              o[n][0] *= corr;
+              o[n][1] *= corr;
+              o[n][2] *= corr;
+              o[n][3] *= corr;
+            }
+          }
+          float pr[2][2];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              pr[nt][jj] = m_run == -INFINITY ? 0.f : fast_exp2(x[nt][jj] - m_run);
+              l_run += pr[nt][jj];
+            }
+          uint32_t pa[4];
+          split_hi_lo(pr[0][0], pr[0][1], pa[0], pa[1]);
+          split_hi_lo(pr[1][0], pr[1][1], pa[2], pa[3]);
+          const bool tail = nv < 16;
+          const uint32_t mk0 =
+              ((2 * tig < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 1 < nv) ? 0xffff0000u : 0u);
+          const uint32_t mk1 =
+              ((2 * tig + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 9 < nv) ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int np = 0; np < C::NT / 2; ++np) {
+            uint32_t vb[4];
+            ldsm_x4_t(vb, sv + swz_off(r0 + (mi & 1) * 8 + rr, np * 2 + (mi >> 1), C::TP));
+            if (tail) {
+              vb[0] &= mk0;
+              vb[1] &= mk1;
+              vb[2] &= mk0;
+              vb[3] &= mk1;
+            }
+            mma_f16(o[2 * np], pa, vb[0], vb[1]);
+            mma_f16(o[2 * np + 1], pa, vb[2], vb[3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (!ok) break;
+    if (!active) continue;
+
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    // ---- this thread's (row, head): the output, or the chunk's partial (merged afterwards by
+    //      merge_kernel)
+    if (!rv || c0 >= Lr) continue;
+    if (!p.merge) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       float* orow = p.out + ((size_t)t * p.n_heads + head) * D;
 #pragma unroll
@@ -259,21 +372,20 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 1)
         *reinterpret_cast<float2*>(orow + d) =
             make_float2((o[n][0] + o[n][2]) * inv, (o[n][1] + o[n][3]) * inv);
       }
-    }
-    return;
-  }
-  if (has) {
-    float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
+    } else {
+      float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
 #pragma unroll
-    for (int n = 0; n < C::NT; ++n) {
-      const int d = n * 8 + 2 * tig;
-      *reinterpret_cast<float2*>(pr + d) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
-    }
-    if (tig == 0) {
-      pr[D] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;  // natural-log units
-      pr[D + 1] = l_run;
+      for (int n = 0; n < C::NT; ++n) {
+        const int d = n * 8 + 2 * tig;
+        *reinterpret_cast<float2*>(pr + d) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+      }
+      if (tig == 0) {
+        pr[D] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;  // natural-log units
+        pr[D + 1] = l_run;
+      }
     }
   }
+  if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
 }
 
 }  // namespace gqa

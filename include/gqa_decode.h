@@ -77,7 +77,8 @@ typedef struct gqa_plan {
                         tile; stream-K mode: 0 */
   int n_split;       /* chunked mode: chunks per row at max_kv_len; stream-K mode: CTAs */
   int tile;          /* positions staged in shared memory per pipeline stage */
-  int grid_x, grid_y, grid_z; /* launch grid: chunked (n_split, n_kv_heads, n_tok);
+  int grid_x, grid_y, grid_z; /* launch grid: chunked (n_split, n_kv_heads x head split,
+                                 n_tok, or row-group slots when row_group > 1);
                                  stream-K (CTAs, 1, 1) */
   int merge;         /* 1 when rows may be split: partials go to ws and are merged inside the
                         same kernel by whichever CTA finishes a row's KV head last, or (rows

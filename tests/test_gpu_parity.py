@@ -265,7 +265,7 @@ def test_rows_grouped_by_sequence(D, G, chunk):
     case = W.make_f16_case(500 + D + G, len(seq_of), 2 * G, 2, D, L, cache_cap=480,
                            seq_of=seq_of, n_seq=3, scale=1 / math.sqrt(D))
     gd = _gd()
-    assert gd.plan(len(seq_of), 2 * G, 2, D, 480, n_seq=3).row_group == 64 // G
+    assert gd.plan(len(seq_of), 2 * G, 2, D, 480, n_seq=3).row_group == 32 // G
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     with forced_chunk(chunk):
         got = run_case(case, err=err).cpu().numpy()
@@ -288,3 +288,15 @@ def test_rows_grouped_matches_per_row_kernel():
 def _rows_off():
     from gpu_util import _env
     return _env(GQA_F16_ROWS="off")
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_rows_grouped_long_runs(G):
+    """Runs longer than a group (32 / G rows: 32 for G = 1), split at multiples of the group
+    size, with a second sequence starting mid-group."""
+    seq_of = [0] * 70 + [1] * 5
+    L = [100 + r for r in range(70)] + [60, 0, 61, 62, 1]
+    case = W.make_f16_case(600 + G, len(seq_of), 2 * G, 2, 64, L, cache_cap=200, seq_of=seq_of,
+                           n_seq=2, scale=0.125)
+    got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, f"long runs G{G}")

@@ -85,11 +85,14 @@ def test_plan_selected_width_caps_chunks(gd):
 
 
 def test_plan_groups_rows_sharing_a_sequence(gd):
-    # 16 causal rows over one sequence (n_seq 1): one group of 16 rows (G=4); chunks sized for
-    # 1 group x 8 KV heads on one CTA per SM: 8 * 8192 / 152 -> 432 -> 448 positions, 19 chunks
+    # 16 causal rows over one sequence (n_seq 1): two groups of 8 rows (G=4); chunks sized for
+    # 2 groups x 8 KV heads on two CTAs per SM: 16 * 8192 / 304 -> 432 -> 448 positions
     p = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1)
-    assert p.row_group == 16 and p.chunk == 448 and p.n_split == 19
-    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 16)
+    assert p.row_group == 8 and p.chunk == 448 and p.n_split == 19
+    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 2)   # two group slots
+    # 64 rows of 32 sequences (pairs): 32 slots
+    q = gd.plan(64, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=32)
+    assert q.row_group == 8 and q.grid_z == 32
     # every row its own sequence, D=256, int8, or group size 3: no grouping
     assert gd.plan(16, 32, 8, 128, 8192, num_sms=152).row_group == 1
     assert gd.plan(16, 32, 8, 256, 8192, num_sms=152, n_seq=1).row_group == 1
