@@ -23,7 +23,7 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
-           "gqa_abi_version", "attn_decode_f16_noalloc")
+           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -57,6 +57,8 @@ def _load():
     lib.attn_decode_q8_sel.restype = I
     lib.attn_decode_f16_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I64, I, F, P, P]
     lib.attn_decode_f16_noalloc.restype = I
+    lib.attn_select_topk.argtypes = [P, I64, P, I, I, I, P, P, P]
+    lib.attn_select_topk.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -217,6 +219,23 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
                                   _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
                                   _stream(stream)))
     return out
+
+
+def attn_select_topk(block_scores, kv_len, budget, max_kv_len=None, ids=None, err=None,
+                     stream=None):
+    """Selected-cell ids [T][budget] from per-row block scores [T][stride] (4 cells a block)."""
+    _need(block_scores, torch.float32, "block_scores", 2)
+    _need(kv_len, torch.int32, "kv_len", 1)
+    T, stride = block_scores.shape
+    if kv_len.numel() != T:
+        raise ValueError("kv_len must have one entry per row")
+    max_kv_len = 4 * (stride - 1) + 3 if max_kv_len is None else int(max_kv_len)
+    if ids is None:
+        ids = torch.empty((T, budget), dtype=torch.int32, device=block_scores.device)
+    _need(ids, torch.int32, "ids", 2)
+    _check(LIB.attn_select_topk(_ptr(block_scores), stride, _ptr(kv_len), T, max_kv_len,
+                                int(budget), _ptr(ids), _ptr(err), _stream(stream)))
+    return ids
 
 
 def attn_merge(part, n_valid, out=None, stream=None):

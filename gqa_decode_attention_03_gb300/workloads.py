@@ -204,6 +204,16 @@ def make_q8_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, budget=None
                 vsc=vsc, ids=ids, budget=budget, seed=seed)
 
 
+def make_block_scores(seed, n_tok, stride, levels=None) -> np.ndarray:
+    """Block scores [n_tok][stride] fp32 for the top-k selection: N(0, 1), or (``levels``) drawn
+    from that many distinct values so that equal scores cross the selection threshold."""
+    g = _gen(np.random.SeedSequence(seed).spawn(1)[0])
+    if levels is None:
+        return g.standard_normal((n_tok, stride), dtype=np.float32)
+    vals = np.linspace(-2.0, 2.0, levels, dtype=np.float32)
+    return vals[g.integers(0, levels, size=(n_tok, stride))]
+
+
 # ----------------------------------------------------------------------------- named workloads
 
 def tiny() -> Case:

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 3
+#define GQA_ABI_VERSION 4
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -165,6 +165,25 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
                               int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
                               float scale, void* ws, size_t ws_bytes, int32_t* err_word,
                               cudaStream_t stream);
+
+/*
+ * attn_select_topk -- the selected-cell id list of attn_decode_q8_sel (qsa2.metal, qsa_topk2).
+ * Row t's cells 0..kv_len[t]-1 come in blocks of 4 (the last block holds kv_len[t] % 4 cells);
+ * cell c carries the score of its block, block_scores[t * score_stride + c / 4].  The row keeps
+ * the `budget` cells with the largest scores, equal scores going to the lower cell, and writes
+ * them in ascending order to ids[t][0..budget).  A row with kv_len[t] <= budget keeps every
+ * cell: ids[t] = 0, 1, .., kv_len[t]-1, then -1.  Scores are compared through the
+ * order-preserving map of fp32 bit patterns to uint32 (negative values: all bits flipped;
+ * others: sign bit set), so -0 ranks below +0; page 1 names this map `okey` without defining
+ * it.
+ *   block_scores  device fp32 [n_tok][score_stride], score_stride >= max_kv_len / 4 + 1
+ *   kv_len        device int32 [n_tok]; values outside [0, max_kv_len] are clamped and flagged
+ *                 GQA_ERR_KVLEN_RANGE
+ *   ids           device int32 [n_tok][budget], fully written; budget >= 1
+ */
+gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
+                            const int32_t* kv_len, int n_tok, int max_kv_len, int budget,
+                            int32_t* ids, int32_t* err_word, cudaStream_t stream);
 
 /*
  * attn_merge -- log-sum-exp merge of split partials (qsa2.metal, qsa_merge2; FORWARD_MSL's

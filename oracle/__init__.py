@@ -18,6 +18,8 @@ from .gqa_oracle import (  # noqa: F401
     dequant_f16,
     dequant_q8,
     lse_merge,
+    order_key,
+    select_topk_cells,
     selected_positions,
     split_partials_f16,
     split_partials_q8,

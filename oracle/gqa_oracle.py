@@ -26,6 +26,7 @@ Passages followed (page title, then the part of it):
     split partials are the unnormalised accumulator with the chunk's max and sum.
   * qsa2.metal (regolith), qsa_merge2: the log-sum-exp merge of those partials.
   * flash_attention_tq.metal (cera 0.4.0 sources): a causal row at position p attends to [0, p].
+  * qsa2.metal (regolith), qsa_topk2: the selected-cell id list, top `budget` cells by block score.
 
 Readings taken where the pages leave a step open are listed in DESIGN.md ("Readings").
 """
@@ -231,3 +232,33 @@ def lse_merge(acc, m, l, n_valid) -> np.ndarray:
         L = (l[t, :n] * e).sum(axis=0)              # [H]
         out[t] = (acc[t, :n] * e[:, :, None]).sum(axis=0) / L[:, None]
     return out
+
+
+# ----------------------------------------------------------------------------- block top-k
+
+def order_key(x) -> np.ndarray:
+    """Order-preserving map of fp32 values to uint32 (the `okey` that qsa2.metal's qsa_topk2
+    applies but does not define; the plain reading): flip every bit of a negative value, set the
+    sign bit of a non-negative one, so unsigned order follows float order (-0 < +0)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    neg = (u >> 31) == 1
+    return np.where(neg, (~u) & 0xFFFFFFFF, u | 0x80000000).astype(np.uint64)
+
+
+def select_topk_cells(block_scores_row, n_kv: int, budget: int) -> np.ndarray:
+    """Selected-cell ids of one row (qsa2.metal, qsa_topk2).
+
+    Cells 0..n_kv-1 come in blocks of 4; cell c carries its block's score, block_scores_row[c//4]
+    (the last block may be partial).  Rows with n_kv <= budget select every cell.  Otherwise the
+    `budget` cells with the largest keys are selected, equal keys going to the lower cell index
+    (qsa_topk2 takes whole blocks above the threshold key and, at the threshold, blocks in
+    ascending order and the first cells of a block).  Returned ascending, as qsa_topk2 emits.
+    """
+    n_kv = max(int(n_kv), 0)
+    if n_kv <= budget:
+        return np.arange(n_kv, dtype=np.int64)
+    cells = np.arange(n_kv)
+    keys = order_key(np.asarray(block_scores_row, np.float32)[cells // 4])
+    # stable sort on descending key keeps ascending cell order among equal keys
+    order = np.argsort(-keys.astype(np.int64), kind="stable")
+    return np.sort(order[:budget]).astype(np.int64)

@@ -1,0 +1,60 @@
+"""GPU parity of the block top-k selection (attn_select_topk) against the oracle: bit-exact ids,
+and the selected int8 path fed by it."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_Q8, assert_close, dev, oracle_ref, run_case
+from gqa_decode_attention_03_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _gd():
+    from gqa_decode_attention_03_gb300 import gqa_decode
+    return gqa_decode
+
+
+def _oracle_ids(scores, kv_len, budget):
+    ids = np.full((len(kv_len), budget), -1, dtype=np.int64)
+    for t, n in enumerate(kv_len):
+        sel = oracle.select_topk_cells(scores[t], int(n), budget)
+        ids[t, :len(sel)] = sel
+    return ids
+
+
+@pytest.mark.parametrize("levels", [None, 3, 17])
+@pytest.mark.parametrize("budget", [1, 5, 64, 1024])
+def test_topk_bit_exact(levels, budget):
+    # lengths: multiples of 4 and not, shorter and longer than the budget, a row of blocks well
+    # past the 1024 threads of a CTA, an empty row
+    kv_len = np.array([8192, 8190, 4097, 3, budget, budget + 1, 0, 17000, 64, 65], np.int32)
+    stride = 17000 // 4 + 1
+    scores = W.make_block_scores(700 + budget, len(kv_len), stride, levels)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _gd().attn_select_topk(dev(scores), dev(kv_len), budget, max_kv_len=17000,
+                                 err=err).cpu().numpy()
+    assert int(err.item()) == 0
+    assert np.array_equal(got, _oracle_ids(scores, kv_len, budget))
+
+
+def test_topk_signed_zero_and_infinities():
+    s = np.array([[0.0, -0.0, np.inf, -np.inf, 1.0, -1.0, 0.0, -0.0]], np.float32)
+    kv_len = np.array([30], np.int32)
+    got = _gd().attn_select_topk(dev(s), dev(kv_len), 9, max_kv_len=30).cpu().numpy()
+    assert np.array_equal(got, _oracle_ids(s, kv_len, 9))
+
+
+def test_topk_feeds_the_selected_int8_path():
+    """Block scores -> ids (GPU) -> int8 selected decode (GPU), against the oracle on the same
+    chain: 48 heads over 4 KV heads, D=256, context 8192, budget 1024."""
+    case = W.q8_selected()
+    stride = 8192 // 4 + 1
+    scores = W.make_block_scores(710, 1, stride)
+    ids = _gd().attn_select_topk(dev(scores), dev(case.kv_len), 1024, max_kv_len=8192)
+    case.ids = _oracle_ids(scores, case.kv_len, 1024).astype(np.int32)
+    assert np.array_equal(ids.cpu().numpy(), case.ids)
+    got = run_case(case, ids=ids).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, "topk -> q8_sel")

@@ -175,3 +175,78 @@ def test_planted_merge_mistakes_are_caught(monkeypatch):
         return out
     monkeypatch.setattr(oracle, "lse_merge", merge_without_weights)
     assert pins.check_closed_forms() != [] or pins.check_invariants() != []
+
+
+# ----------------------------------------------------------------------------- block top-k
+
+def _topk_brute(scores, n_kv, budget):
+    """Plain Python: cells ranked by (score descending, cell ascending), first `budget` taken."""
+    cells = sorted(range(n_kv), key=lambda c: (-float(scores[c // 4]), c))
+    return sorted(cells[:budget]) if n_kv > budget else list(range(n_kv))
+
+
+def topk_pin_failures():
+    fails = []
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        n_kv = int(rng.integers(1, 90))
+        budget = int(rng.integers(1, 40))
+        nb = n_kv // 4 + 1
+        # few distinct non-zero values so that ties cross the threshold often
+        scores = rng.choice(np.array([-3.5, -1.0, -0.25, 0.5, 2.0, 7.0], np.float32), size=nb)
+        try:
+            got = list(oracle.select_topk_cells(scores, n_kv, budget))
+        except Exception as e:
+            fails.append(f"raised {e!r}")
+            break
+        if got != _topk_brute(scores, n_kv, budget):
+            fails.append(f"trial {trial}: n_kv {n_kv} budget {budget}")
+            break
+    return fails
+
+
+def test_topk_matches_plain_ranking():
+    assert topk_pin_failures() == []
+
+
+def test_order_key_is_monotone():
+    x = np.array([-np.inf, -3e38, -1.5, -1e-30, -0.0, 0.0, 1e-30, 2.0, 3e38, np.inf], np.float32)
+    k = oracle.order_key(x)
+    assert (np.diff(k.astype(np.int64)) > 0).all()
+
+
+def test_topk_closed_cases():
+    # page's short-row rule: n_kv <= budget selects every cell
+    assert list(oracle.select_topk_cells(np.zeros(3, np.float32), 9, 9)) == list(range(9))
+    # ties at the threshold go to the lower blocks, and to the first cells of a block:
+    # blocks (cells) 0:(0-3)=1, 1:(4-7)=5, 2:(8-11)=5, 3:(12,13)=2; budget 6 -> cells 4..9
+    s = np.array([1, 5, 5, 2], np.float32)
+    assert list(oracle.select_topk_cells(s, 14, 6)) == [4, 5, 6, 7, 8, 9]
+    # the partial last block holds n_kv % 4 cells: here 2 cells of the best block
+    s = np.array([1, 1, 9], np.float32)
+    assert list(oracle.select_topk_cells(s, 10, 3)) == [0, 8, 9]
+
+
+@pytest.mark.parametrize("name", ["ties to higher cells", "full last block", "sign ignored"])
+def test_planted_topk_mistakes_are_caught(name, monkeypatch):
+    assert topk_pin_failures() == []
+    if name == "ties to higher cells":
+        def wrong(block_scores_row, n_kv, budget):
+            n_kv = int(n_kv)
+            if n_kv <= budget:
+                return np.arange(n_kv)
+            keys = OG.order_key(np.asarray(block_scores_row, np.float32)[np.arange(n_kv) // 4])
+            order = np.argsort(-keys.astype(np.int64), kind="stable")[::-1]
+            order = order[np.argsort(-keys[order].astype(np.int64), kind="stable")]
+            return np.sort(order[:budget])
+        monkeypatch.setattr(oracle, "select_topk_cells", wrong)
+    elif name == "full last block":
+        def wrong(block_scores_row, n_kv, budget):
+            n = int(n_kv)
+            return OG.select_topk_cells.__wrapped__(block_scores_row, (n // 4 + 1) * 4, budget)
+        OG.select_topk_cells.__wrapped__ = OG.select_topk_cells
+        monkeypatch.setattr(oracle, "select_topk_cells", wrong)
+    else:
+        monkeypatch.setattr(OG, "order_key",
+                            lambda x: np.asarray(x, np.float32).view(np.uint32).astype(np.uint64))
+    assert topk_pin_failures() != [], f"planted mistake '{name}' went unnoticed"
