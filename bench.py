@@ -156,7 +156,18 @@ def _device_inputs(case, torch):
     return t
 
 
+def _merge_launch(plan):
+    """1 when the step ends with a separate merge kernel (rows grouped by sequence)."""
+    return 1 if plan.merge and not plan.streamk and plan.row_group > 1 else 0
+
+
 def _kernel_name(case, plan):
+    if plan.streamk:
+        return "streamk_mma_kernel (stream-K split, merge fused)"
+    if plan.row_group > 1:
+        return "partial_mma_rows_kernel (rows grouped by sequence) + merge_kernel"
+    if "block_scores" in case.meta:
+        return "topk_kernel + partial_kernel (split-KV, merge fused)"
     if plan.streamk:
         return "streamk_mma_kernel (stream-K split, merge fused)"
     if case.kind == "f16" and os.environ.get("GQA_F16_KERNEL") != "fma":
@@ -186,9 +197,17 @@ def run_gpu(args):
     out = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    scores = case.meta.get("block_scores")
+    if scores is not None:  # the step chooses its ids first (block top-k selection)
+        x["scores"] = torch.from_numpy(scores).cuda()
+        x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
+
     def step(q=None, kv=None):
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
+        if scores is not None:
+            gd.attn_select_topk(x["scores"], kv, case.budget, max_kv_len=case.cache_cap,
+                                ids=x["ids"], stream=stream)
         if case.kind == "f16":
             gd.attn_decode_f16(q, x["k"], x["v"], kv, scale=case.scale, seq_of=x["seq_of"],
                                max_kv_len=max_len, out=out, ws=ws, stream=stream)
@@ -261,7 +280,9 @@ def run_gpu(args):
         return
     alg = case.algorithmic_bytes()
     peak, peak_src = _peaks()
-    achieved = alg / (ms * 1e-3) / 1e9  # one kernel per step: the partial kernel, merge fused
+    # algorithmic bytes over the step time: on the default workload a step is one kernel (the
+    # split-KV partial kernel with its merge fused); multi-kernel steps name every kernel
+    achieved = alg / (ms * 1e-3) / 1e9
     traffic = _ncu_traffic(case.name)
     gbs = world * alg / (ms * 1e-3) / 1e9
     line = {
@@ -281,7 +302,7 @@ def run_gpu(args):
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "h2d_bytes_per_step": int(case.q.nbytes + case.kv_len.nbytes),
                 "d2h_bytes_per_step": int(T * H * D * 4)},
-        "gpu_launches": int(K),
+        "gpu_launches": int(K * (1 + (scores is not None) + _merge_launch(plan))),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

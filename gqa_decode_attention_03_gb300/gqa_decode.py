@@ -23,7 +23,7 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
-           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk")
+           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -59,6 +59,8 @@ def _load():
     lib.attn_decode_f16_noalloc.restype = I
     lib.attn_select_topk.argtypes = [P, I64, P, I, I, I, P, P, P]
     lib.attn_select_topk.restype = I
+    lib.kv_append_q8.argtypes = [P, P, I, I, I, P, P, P, P, I, I64, I, I, P]
+    lib.kv_append_q8.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -236,6 +238,22 @@ def attn_select_topk(block_scores, kv_len, budget, max_kv_len=None, ids=None, er
     _check(LIB.attn_select_topk(_ptr(block_scores), stride, _ptr(kv_len), T, max_kv_len,
                                 int(budget), _ptr(ids), _ptr(err), _stream(stream)))
     return ids
+
+
+def kv_append_q8(k_new, v_new, kq, vq, ksc, vsc, seq, t0, stream=None):
+    """Quantise fp32 rows k_new / v_new [n_new][Hk][D] into positions t0.. of sequence `seq` of
+    the int8 cache (kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/64] fp16)."""
+    _need(k_new, torch.float32, "k_new", 3)
+    _need(v_new, torch.float32, "v_new", 3)
+    for name, x, dt in (("kq", kq, torch.int8), ("vq", vq, torch.int8),
+                        ("ksc", ksc, torch.float16), ("vsc", vsc, torch.float16)):
+        _need(x, dt, name, 4)
+    n_new, Hk, D = k_new.shape
+    n_seq, cap, Hk2, D2 = kq.shape
+    if v_new.shape != k_new.shape or (Hk2, D2) != (Hk, D) or ksc.shape != (n_seq, cap, Hk, D // 64):
+        raise ValueError("shape mismatch between new rows and the cache")
+    _check(LIB.kv_append_q8(_ptr(k_new), _ptr(v_new), n_new, Hk, D, _ptr(kq), _ptr(vq), _ptr(ksc),
+                            _ptr(vsc), n_seq, cap, int(seq), int(t0), _stream(stream)))
 
 
 def attn_merge(part, n_valid, out=None, stream=None):

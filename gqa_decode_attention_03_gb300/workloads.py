@@ -135,10 +135,13 @@ class Case:
         return sum(self.visited(t) for t in range(self.n_tok)) * Hk * per_pos
 
     def algorithmic_bytes(self) -> int:
-        """KV bytes + ids + q (fp32) + out (fp32): the bytes a perfect kernel moves per step."""
+        """KV bytes + ids + q (fp32) + out (fp32) (+ block scores read by the selection when the
+        ids are chosen in the step): the bytes a perfect pipeline moves per step."""
         extra = 2 * self.q.size * 4
         if self.ids is not None:
             extra += sum(self.visited(t) for t in range(self.n_tok)) * 4
+        if "block_scores" in self.meta:
+            extra += self.meta["block_scores"].nbytes
         return self.kv_bytes() + extra
 
     def flops(self) -> int:
@@ -251,6 +254,15 @@ def q8_selected() -> Case:
                         name="q8_sel_h48_hk4_d256_ctx8192_b1024")
 
 
+def q8_topk_selected() -> Case:
+    """q8_selected with its ids chosen on the GPU from block scores: the 2049 block scores of the
+    8192-cell context (N(0, 1), seed 1008) go through the top-1024 selection first."""
+    c = q8_selected()
+    c.name = "q8_topk_sel_h48_hk4_d256_ctx8192_b1024"
+    c.meta["block_scores"] = make_block_scores(1008, c.n_tok, 8192 // 4 + 1)
+    return c
+
+
 def batched() -> Case:
     """64 sequences of 8192 positions, 32 heads / 8 KV heads, D=128."""
     return make_f16_case(1005, 64, 32, 8, 128, [8192] * 64, scale=1 / math.sqrt(128),
@@ -273,6 +285,7 @@ NAMED = {
     "long_ctx": long_context,
     "long_ctx_4": long_context_4,
     "q8_sel": q8_selected,
+    "q8_topk_sel": q8_topk_selected,
     "batched": batched,
     "prefill_chunk": prefill_chunk,
 }

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 4
+#define GQA_ABI_VERSION 5
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -184,6 +184,20 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
 gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
                             const int32_t* kv_len, int n_tok, int max_kv_len, int budget,
                             int32_t* ids, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * kv_append_q8 -- quantise new K/V rows into the int8 cache (FORWARD_MSL, kv_append_q8, with
+ * the 64-dim scale groups of the cache attn_decode_q8_sel reads).  For every 64-dim group of a
+ * (position, KV head) row: d = amax|x| / 127, codes q = rint(x / d) clamped to [-127, 127]
+ * (all 0 when d = 0), scale = f16(d); the arithmetic is IEEE fp32 (division to nearest, rint to
+ * even).  Writes positions t0 .. t0 + n_new - 1 of sequence `seq`.
+ *   k_new, v_new  device fp32 [n_new][n_kv_heads][head_dim], 8-byte aligned
+ *   kq, vq, ksc, vsc  the int8 cache and its scales (layouts above), n_seq x cache_cap rows
+ *   requires 0 <= seq < n_seq and t0 + n_new <= cache_cap; head_dim in {64, 128, 256}
+ */
+gqa_status kv_append_q8(const float* k_new, const float* v_new, int n_new, int n_kv_heads,
+                        int head_dim, int8_t* kq, int8_t* vq, uint16_t* ksc, uint16_t* vsc,
+                        int n_seq, int64_t cache_cap, int seq, int t0, cudaStream_t stream);
 
 /*
  * attn_merge -- log-sum-exp merge of split partials (qsa2.metal, qsa_merge2; FORWARD_MSL's

@@ -19,6 +19,7 @@ from .gqa_oracle import (  # noqa: F401
     dequant_q8,
     lse_merge,
     order_key,
+    quantize_q8,
     select_topk_cells,
     selected_positions,
     split_partials_f16,

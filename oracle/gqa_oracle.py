@@ -27,6 +27,7 @@ Passages followed (page title, then the part of it):
   * qsa2.metal (regolith), qsa_merge2: the log-sum-exp merge of those partials.
   * flash_attention_tq.metal (cera 0.4.0 sources): a causal row at position p attends to [0, p].
   * qsa2.metal (regolith), qsa_topk2: the selected-cell id list, top `budget` cells by block score.
+  * FORWARD_MSL (cherenkov docs), kv_append_q8: quantise-on-append, amax / 127 and rint.
 
 Readings taken where the pages leave a step open are listed in DESIGN.md ("Readings").
 """
@@ -262,3 +263,28 @@ def select_topk_cells(block_scores_row, n_kv: int, budget: int) -> np.ndarray:
     # stable sort on descending key keeps ascending cell order among equal keys
     order = np.argsort(-keys.astype(np.int64), kind="stable")
     return np.sort(order[:budget]).astype(np.int64)
+
+
+# ----------------------------------------------------------------------------- quantise on append
+
+def quantize_q8(x) -> tuple[np.ndarray, np.ndarray]:
+    """int8 codes and f16 scales of fp32 rows ``x[..., D]``, one scale per 64 dims
+    (FORWARD_MSL, kv_append_q8, with the 64-dim groups of the int8 cache read by qsa2.metal):
+
+        d = amax|x_group| / 127,  q = rint(x / d) clamped to [-127, 127] (0 when d = 0),
+        scale = f16(d)
+
+    Every step is taken in fp32, as the kernel takes it, so that the integer codes follow from
+    the same roundings (IEEE division, round half to even).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    if D % SCALE_GROUP:
+        raise ValueError("head_dim must be a multiple of 64")
+    g = x.reshape(x.shape[:-1] + (D // SCALE_GROUP, SCALE_GROUP))
+    amax = np.abs(g).max(axis=-1)                                   # fp32
+    d = (amax / np.float32(127)).astype(np.float32)                 # fp32 division
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d[..., None] > 0, np.rint(g / d[..., None]), np.float32(0))
+    q = np.clip(q, -127, 127).astype(np.int8).reshape(x.shape)
+    return q, d.astype(np.float16)

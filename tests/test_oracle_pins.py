@@ -250,3 +250,34 @@ def test_planted_topk_mistakes_are_caught(name, monkeypatch):
         monkeypatch.setattr(OG, "order_key",
                             lambda x: np.asarray(x, np.float32).view(np.uint32).astype(np.uint64))
     assert topk_pin_failures() != [], f"planted mistake '{name}' went unnoticed"
+
+
+# ----------------------------------------------------------------------------- quantise on append
+
+def test_quantize_roundtrip_within_half_a_step():
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((5, 3, 128)) * rng.uniform(0.01, 100, (5, 3, 1))).astype(np.float32)
+    q, s = oracle.quantize_q8(x)
+    d = x.reshape(5, 3, 2, 64)
+    amax = np.abs(d).max(-1)
+    deq = q.reshape(5, 3, 2, 64).astype(np.float64) * (amax / 127.0)[..., None]
+    # |x - q d| <= d / 2 (up to fp32 rounding of d), the largest element maps to +-127
+    assert (np.abs(d - deq) <= (amax / 127.0)[..., None] * (0.5 + 1e-5)).all()
+    big = np.abs(d).argmax(-1)
+    assert (np.abs(np.take_along_axis(q.reshape(5, 3, 2, 64), big[..., None], -1)) == 127).all()
+    assert np.array_equal(s, (amax / np.float32(127)).astype(np.float16))
+
+
+def test_quantize_closed_cases():
+    x = np.zeros((1, 64), np.float32)
+    q, s = oracle.quantize_q8(x)
+    assert (q == 0).all() and (s == 0).all()           # an all-zero group: scale 0, codes 0
+    x = np.linspace(-1, 1, 64, dtype=np.float32)[None]  # amax 1: d = 1/127, q = rint(127 x)
+    q, s = oracle.quantize_q8(x)
+    assert np.array_equal(q[0], np.rint(x[0] / np.float32(1 / 127)).astype(np.int8))
+    assert q[0, 0] == -127 and q[0, -1] == 127 and s[0, 0] == np.float16(1 / 127)
+    # halves round to even: x = 2.5 d -> 2, 3.5 d -> 4 (d = 127 / 127 = 1 when amax = 127)
+    x = np.zeros((1, 64), np.float32)
+    x[0, :4] = [127.0, 2.5, 3.5, -2.5]
+    q, _ = oracle.quantize_q8(x)
+    assert list(q[0, :4]) == [127, 2, 4, -2]
