@@ -402,6 +402,25 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
                        ws_bytes, err_word, stream);
 }
 
+gqa_status attn_merge_gated(const float* part, const int32_t* n_valid, int n_split, int n_tok,
+                            int n_heads, int head_dim, const float* gate, int64_t gate_stride,
+                            float* out, cudaStream_t stream) {
+  if (!gate) return fail(GQA_EINVAL, "attn_merge_gated: gate is NULL");
+  if (gate_stride < head_dim || (gate_stride & 1) || (reinterpret_cast<uintptr_t>(gate) & 7))
+    return fail(GQA_EINVAL, "attn_merge_gated: gate 8-byte aligned, gate_stride even and >= head_dim");
+  if (n_tok < 0 || n_tok > 65535 || n_heads <= 0 || n_heads > 65535 || n_split <= 0)
+    return fail(GQA_EINVAL, "bad sizes n_tok %d n_heads %d n_split %d", n_tok, n_heads, n_split);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(GQA_EINVAL, "head_dim %d not in {64, 128, 256}", head_dim);
+  if (n_tok == 0) return GQA_OK;
+  if (!part || !n_valid || !out) return fail(GQA_EINVAL, "a required pointer is NULL");
+  if (!aligned16(part) || !aligned16(out)) return fail(GQA_EINVAL, "part/out not 16-byte aligned");
+  cudaError_t e = gqa::launch_merge(head_dim, part, n_valid, n_split, n_tok, n_heads, out, stream,
+                                    gate, gate_stride);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return GQA_OK;
+}
+
 gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, int n_tok,
                       int n_heads, int head_dim, float* out, cudaStream_t stream) {
   if (n_tok < 0 || n_tok > 65535 || n_heads <= 0 || n_heads > 65535 || n_split <= 0)

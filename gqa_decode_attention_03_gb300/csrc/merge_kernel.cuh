@@ -5,6 +5,8 @@
 // part[t][c][h][acc(D) | m | l], natural-log m):
 //   M = max_c m_c,  e_c = exp(m_c - M),  L = sum_c l_c e_c,  out[d] = sum_c acc_c[d] e_c / L
 // as in qsa2.metal's qsa_merge2 (regolith) and FORWARD_MSL's attn_combine (there in exp2 units).
+// With a gate, the merged row is multiplied by 1 / (1 + exp(-gate)) on the way out -- the
+// sigmoid output gate both pages apply after their merge.
 // Every thread reads the chunks' (m, l) itself (the same few lines for all threads of the CTA,
 // served by L1), so all its loads are independent and go out together.  A row without valid
 // chunks, or with L == 0, gets zeros.
@@ -18,6 +20,8 @@ template <int D>
 __global__ void __launch_bounds__(D / 2) merge_kernel(const float* __restrict__ part,
                                                       const int32_t* __restrict__ n_valid,
                                                       int n_split, int n_heads,
+                                                      const float* __restrict__ gate,
+                                                      long long gate_stride,
                                                       float* __restrict__ out) {
   const int h = blockIdx.x, t = blockIdx.y, d = 2 * threadIdx.x;
   int nv = __ldg(n_valid + t);
@@ -41,8 +45,14 @@ __global__ void __launch_bounds__(D / 2) merge_kernel(const float* __restrict__ 
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  *reinterpret_cast<float2*>(out + ((size_t)t * n_heads + h) * D + d) =
-      make_float2(a.x * inv, a.y * inv);
+  float2 y = make_float2(a.x * inv, a.y * inv);
+  if (gate) {  // sigmoid output gate (qsa_merge2, attn_combine)
+    const float2 gv =
+        __ldg(reinterpret_cast<const float2*>(gate + ((size_t)t * n_heads + h) * gate_stride + d));
+    y.x *= 1.f / (1.f + __expf(-gv.x));
+    y.y *= 1.f / (1.f + __expf(-gv.y));
+  }
+  *reinterpret_cast<float2*>(out + ((size_t)t * n_heads + h) * D + d) = y;
 }
 
 }  // namespace gqa

@@ -23,7 +23,7 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
-           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8")
+           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8", "attn_merge_gated")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -61,6 +61,8 @@ def _load():
     lib.attn_select_topk.restype = I
     lib.kv_append_q8.argtypes = [P, P, I, I, I, P, P, P, P, I, I64, I, I, P]
     lib.kv_append_q8.restype = I
+    lib.attn_merge_gated.argtypes = [P, P, I, I, I, I, P, I64, P, P]
+    lib.attn_merge_gated.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -256,8 +258,10 @@ def kv_append_q8(k_new, v_new, kq, vq, ksc, vsc, seq, t0, stream=None):
                             _ptr(vsc), n_seq, cap, int(seq), int(t0), _stream(stream)))
 
 
-def attn_merge(part, n_valid, out=None, stream=None):
-    """LSE merge of partials ``part [T][S][H][D+2]`` over the first n_valid[t] chunks."""
+def attn_merge(part, n_valid, out=None, gate=None, gate_stride=None, stream=None):
+    """LSE merge of partials ``part [T][S][H][D+2]`` over the first n_valid[t] chunks; with
+    ``gate`` (fp32, element (t, h, d) at flat index (t*H + h)*gate_stride + d), the merged row
+    is multiplied by sigmoid(gate) (attn_merge_gated)."""
     _need(part, torch.float32, "part", 4)
     _need(n_valid, torch.int32, "n_valid", 1)
     T, S, H, D2 = part.shape
@@ -265,5 +269,16 @@ def attn_merge(part, n_valid, out=None, stream=None):
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.float32, device=part.device)
     _need(out, torch.float32, "out", 3)
-    _check(LIB.attn_merge(_ptr(part), _ptr(n_valid), S, T, H, D, _ptr(out), _stream(stream)))
+    if gate is None:
+        _check(LIB.attn_merge(_ptr(part), _ptr(n_valid), S, T, H, D, _ptr(out), _stream(stream)))
+    else:
+        if gate.dtype != torch.float32 or not gate.is_cuda:
+            raise TypeError("gate must be a CUDA fp32 tensor")
+        gs = D if gate_stride is None else int(gate_stride)
+        if gate.dim() != 1 and not gate.is_contiguous():
+            raise ValueError("gate must be contiguous")
+        if gate.numel() < (T * H - 1) * gs + D:
+            raise ValueError("gate too small for its stride")
+        _check(LIB.attn_merge_gated(_ptr(part), _ptr(n_valid), S, T, H, D, _ptr(gate), gs,
+                                    _ptr(out), _stream(stream)))
     return out

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 5
+#define GQA_ABI_VERSION 6
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -205,6 +205,8 @@ gqa_status kv_append_q8(const float* k_new, const float* v_new, int n_new, int n
  *   M = max_c m_c,  e_c = exp(m_c - M),  L = sum_c l_c e_c,  out = sum_c acc_c e_c / L
  * over chunks c < n_valid[t] of row t (n_valid device [n_tok], values clamped to [0, n_split]);
  * a row with n_valid 0 (or L == 0) gets zeros.  part as in the layouts, head_dim in {64,128,256}.
+ * The pages multiply the merged row by a sigmoid output gate; attn_merge leaves it out (the
+ * plain merge) and attn_merge_gated below applies it.
  */
 gqa_status attn_merge(const float* part, const int32_t* n_valid, int n_split, int n_tok,
                       int n_heads, int head_dim, float* out, cudaStream_t stream);
@@ -242,6 +244,18 @@ gqa_status attn_decode_f16_noalloc(const float* q, const uint16_t* k_cache,
                                    int n_kv_heads, int head_dim, int64_t cache_cap,
                                    int max_kv_len, float scale, int32_t* err_word,
                                    cudaStream_t stream);
+
+/*
+ * attn_merge_gated -- attn_merge followed by the sigmoid output gate both pages apply after
+ * their merge (qsa2.metal, qsa_merge2; FORWARD_MSL, attn_combine):
+ *   out[t][h][d] = merge(...)[t][h][d] / (1 + exp(-gate[(t * n_heads + h) * gate_stride + d]))
+ * gate: device fp32, 8-byte aligned; gate_stride even and >= head_dim (head_dim for a plain
+ * [n_tok][n_heads][head_dim] gate; 2 * head_dim with gate = qfull + head_dim for the pages'
+ * per-head [query | gate] pairs).  Other arguments as attn_merge.
+ */
+gqa_status attn_merge_gated(const float* part, const int32_t* n_valid, int n_split, int n_tok,
+                            int n_heads, int head_dim, const float* gate, int64_t gate_stride,
+                            float* out, cudaStream_t stream);
 
 /* Human-readable name of a status; static storage. */
 const char* gqa_status_string(gqa_status s);

@@ -17,6 +17,7 @@ from .gqa_oracle import (  # noqa: F401
     decode_q8,
     dequant_f16,
     dequant_q8,
+    gated_merge,
     lse_merge,
     order_key,
     quantize_q8,

@@ -288,3 +288,11 @@ def quantize_q8(x) -> tuple[np.ndarray, np.ndarray]:
         q = np.where(d[..., None] > 0, np.rint(g / d[..., None]), np.float32(0))
     q = np.clip(q, -127, 127).astype(np.int8).reshape(x.shape)
     return q, d.astype(np.float16)
+
+
+def gated_merge(acc, m, l, n_valid, gate) -> np.ndarray:
+    """The merge followed by the sigmoid output gate (qsa2.metal, qsa_merge2; FORWARD_MSL,
+    attn_combine): out = lse_merge(...) * 1 / (1 + exp(-gate)), gate [T][H][D] (the second half
+    of each head's [query | gate] pair on those pages)."""
+    g = np.asarray(gate, np.float64)
+    return lse_merge(acc, m, l, n_valid) * (1.0 / (1.0 + np.exp(-g)))

@@ -300,3 +300,28 @@ def test_rows_grouped_long_runs(G):
                            n_seq=2, scale=0.125)
     got = run_case(case).cpu().numpy()
     assert_close(got, oracle_ref(case), TOL_F16, f"long runs G{G}")
+
+
+@pytest.mark.parametrize("pair_layout", [False, True])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_merge_with_sigmoid_gate(D, pair_layout):
+    """attn_merge_gated: the merge times sigmoid(gate), for a plain [T][H][D] gate and for the
+    gate half of per-head [query | gate] pairs (stride 2 D)."""
+    rng = np.random.default_rng(D + 7)
+    T, S, H = 3, 6, 4
+    acc = rng.standard_normal((T, S, H, D))
+    m = rng.standard_normal((T, S, H)) * 2
+    l = rng.uniform(0.5, 9, (T, S, H))
+    n_valid = np.array([6, 2, 0], dtype=np.int32)
+    part = np.concatenate([acc, m[..., None], l[..., None]], axis=-1).astype(np.float32)
+    g = (rng.standard_normal((T, H, D)) * 3).astype(np.float32)
+    if pair_layout:
+        qfull = np.concatenate([rng.standard_normal((T, H, D)).astype(np.float32), g], axis=-1)
+        gate_t = dev(qfull).view(-1)[D:]  # the gate half of each [query | gate] pair
+        stride = 2 * D
+    else:
+        gate_t, stride = dev(g), D
+    got = _gd().attn_merge(dev(part), dev(n_valid), gate=gate_t, gate_stride=stride)
+    ref = oracle.gated_merge(part[..., :D].astype(np.float64), part[..., D].astype(np.float64),
+                             part[..., D + 1].astype(np.float64), n_valid, g)
+    assert_close(got.cpu().numpy(), ref, 1e-5, "gated merge")

@@ -281,3 +281,18 @@ def test_quantize_closed_cases():
     x[0, :4] = [127.0, 2.5, 3.5, -2.5]
     q, _ = oracle.quantize_q8(x)
     assert list(q[0, :4]) == [127, 2, 4, -2]
+
+
+def test_gated_merge_closed_forms():
+    rng = np.random.default_rng(4)
+    acc = rng.standard_normal((1, 2, 1, 64))
+    m = np.array([[[0.0], [np.log(3.0)]]])
+    l = np.ones((1, 2, 1))
+    base = oracle.lse_merge(acc, m, l, [2])
+    # gate 0 halves the row; a large gate passes it, a very negative one closes it
+    assert np.allclose(oracle.gated_merge(acc, m, l, [2], np.zeros((1, 1, 64))), base / 2)
+    assert np.allclose(oracle.gated_merge(acc, m, l, [2], np.full((1, 1, 64), 40.0)), base)
+    assert np.allclose(oracle.gated_merge(acc, m, l, [2], np.full((1, 1, 64), -40.0)), 0,
+                       atol=1e-16)
+    g = np.full((1, 1, 64), np.log(3.0))  # sigmoid(ln 3) = 3/4
+    assert np.allclose(oracle.gated_merge(acc, m, l, [2], g), 0.75 * base, rtol=1e-14)
