@@ -145,6 +145,20 @@ def _ncu_traffic(workload):
     return None
 
 
+def max_over_ranks(values):
+    """Element-wise max of per-rank timings across the process group (the slowest rank sets the
+    job's time); the identity without one.  Uses the group's own device: CUDA under NCCL, the
+    CPU under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def _device_inputs(case, torch):
     d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
     t = {"q": d(case.q), "kv_len": d(case.kv_len), "seq_of": d(case.seq_of)}
@@ -271,11 +285,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eve]))
 
-    ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([float(step_ms.mean()), e2e_ms])
     if rank != 0:
         return
     alg = case.algorithmic_bytes()
