@@ -87,7 +87,7 @@ constexpr int kCtasPerSm = 2;
 constexpr long long kMaxChunk = 8192;
 // Rows whose whole visited list is at most this many bytes of K/V (and scales) are not split:
 // one CTA streams them in a few microseconds, less than a split's merge step costs.
-constexpr long long kMinSplitBytes = 256 << 10;
+constexpr long long kMinSplitBytes = 128 << 10;
 
 // Shapes that do not depend on the device.
 gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
@@ -227,6 +227,10 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   const long long slots = (long long)kCtasPerSm * num_sms;
   long long chunk = (units + slots - 1) / slots;
   chunk = std::min(chunk, kMaxChunk);
+  // a split chunk spans at least two stages, so its pipeline has something to overlap
+  // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
+  // D=64 4096 positions 14.7 against 16.1)
+  chunk = std::max(chunk, 2LL * tile);
   const long long row_bytes = kind == GQA_KIND_F16 ? 4LL * head_dim : 2LL * (head_dim + head_dim / 32);
   if (nmax * row_bytes <= kMinSplitBytes) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");

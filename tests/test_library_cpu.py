@@ -69,9 +69,10 @@ def test_plan_long_context_chunked(gd):
     part = 16 * 4 * 32 * 130 * 4
     counters = -(-16 * 8 * 4 // 256) * 256          # per-(row, KV head) arrival counters
     assert p.ws_bytes == counters + -(-part // 256) * 256 + 16 * 4
-    # short rows: enough chunks for a wave (1 row x 8 KV heads x 4096 positions, D=64)
+    # short rows: chunks of at least two 128-position stages (1 row x 8 KV heads x 4096
+    # positions, D=64)
     q = gd.plan(1, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
-    assert q.chunk == 128 and q.n_split == 32
+    assert q.chunk == 256 and q.n_split == 16
     r = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
     assert r.n_split == 1 and r.merge == 0 and r.ws_bytes == 0 and r.chunk == 128
 
@@ -81,7 +82,7 @@ def test_plan_selected_width_caps_chunks(gd):
     # the 12 query heads of a KV head spread over 3 CTAs of 4 heads each
     p = gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
     assert p.streamk == 0 and p.tile == 64 and p.n_split == -(-1024 // p.chunk)
-    assert p.grid_y == 4 * 3 and p.chunk == 64
+    assert p.grid_y == 4 * 3 and p.chunk == 128
 
 
 def test_plan_groups_rows_sharing_a_sequence(gd):
@@ -101,10 +102,10 @@ def test_plan_groups_rows_sharing_a_sequence(gd):
 
 
 def test_plan_small_rows_are_not_split(gd):
-    # 256 positions of f16 D=64 are 64 KB of K/V: below the split threshold
+    # 256 positions of f16 D=64 are 64 KB of K/V: below the 128 KB split threshold
     p = gd.plan(1, 4, 1, 64, 256, -1, gd.KIND_F16, num_sms=152)
     assert p.n_split == 1 and p.merge == 0
-    q = gd.plan(1, 4, 1, 64, 1025, -1, gd.KIND_F16, num_sms=152)   # 262 400 bytes: split
+    q = gd.plan(1, 4, 1, 64, 513, -1, gd.KIND_F16, num_sms=152)   # 131 328 bytes: split
     assert q.n_split > 1
 
 
