@@ -207,6 +207,79 @@ def make_q8_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, budget=None
                 vsc=vsc, ids=ids, budget=budget, seed=seed)
 
 
+LLOYD_MAX_2BIT = (-1.5104, -0.4528, 0.4528, 1.5104)  # 2-bit Gaussian quantiser points
+
+
+@dataclass
+class TqCase:
+    """A decode problem over a TurboQuant-compressed cache (host arrays)."""
+    name: str
+    q_rot: np.ndarray      # [T][H][D] fp32
+    q_jl: np.ndarray       # [T][H][D] fp32
+    k_polar: np.ndarray    # [n_seq][cap][Hk][D/16] uint32
+    k_jl: np.ndarray       # [n_seq][cap][Hk][D/32] uint32
+    k_norms: np.ndarray    # [n_seq][cap][Hk] uint32: f16 norm | f16 residual norm << 16
+    v_polar: np.ndarray    # [n_seq][cap][Hk][D/16] uint32
+    v_norms: np.ndarray    # [n_seq][cap][Hk] uint32: f16 norm
+    centroids: np.ndarray  # [4] fp32
+    signs: np.ndarray      # [D] fp32, +-1
+    qjl_scale: float
+    scale: float
+    kv_len: np.ndarray
+    seq_of: np.ndarray
+    seed: int = 0
+
+    @property
+    def n_kv_heads(self):
+        return self.k_polar.shape[2]
+
+    def kv_bytes(self) -> int:
+        D = self.q_rot.shape[2]
+        per_pos = 4 * (D // 16 + D // 32 + 1) + 4 * (D // 16 + 1)
+        return int(sum(max(int(l), 0) for l in self.kv_len)) * self.n_kv_heads * per_pos
+
+
+def _half_bits(x) -> np.ndarray:
+    return np.asarray(x, np.float16).view(np.uint16).astype(np.uint32)
+
+
+def make_tq_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=None,
+                 seq_of=None, n_seq=None, scale=None, name="tq") -> TqCase:
+    """Random TurboQuant problem: q_rot, q_jl N(0, 1); uniform random 2-bit indices and sign
+    bits; K norms U[0.5, 2], residual norms U[0, 0.5], V norms U[0.5, 2] (f16); centroids the
+    2-bit Gaussian Lloyd-Max points over sqrt(D); random +-1 signs; qjl_scale sqrt(pi/2) / D
+    (the factor flash_attention_tq.metal's header gives).  Norm words past a sequence's length
+    hold f16 NaN."""
+    D = head_dim
+    if D % 32:
+        raise ValueError("head_dim must be a multiple of 32")
+    kv_len = np.asarray(kv_len, dtype=np.int32).reshape(n_tok)
+    seq_of = (np.arange(n_tok, dtype=np.int32) if seq_of is None
+              else np.asarray(seq_of, dtype=np.int32).reshape(n_tok))
+    n_seq = int(seq_of.max()) + 1 if n_seq is None else n_seq
+    cap = int(max(1, kv_len.max())) if cache_cap is None else int(cache_cap)
+    g = _gen(np.random.SeedSequence(seed).spawn(1)[0])
+    q_rot = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
+    q_jl = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
+    shp = (n_seq, cap, n_kv_heads)
+    k_polar = g.integers(0, 2 ** 32, size=shp + (D // 16,), dtype=np.uint64).astype(np.uint32)
+    k_jl = g.integers(0, 2 ** 32, size=shp + (D // 32,), dtype=np.uint64).astype(np.uint32)
+    v_polar = g.integers(0, 2 ** 32, size=shp + (D // 16,), dtype=np.uint64).astype(np.uint32)
+    k_norms = _half_bits(g.uniform(0.5, 2.0, shp)) | (_half_bits(g.uniform(0.0, 0.5, shp)) << 16)
+    v_norms = _half_bits(g.uniform(0.5, 2.0, shp))
+    nan = _half_bits(np.float16(np.nan))
+    for s in range(n_seq):
+        L = max([int(kv_len[t]) for t in range(n_tok) if seq_of[t] == s] + [0])
+        k_norms[s, L:] = nan | (nan << 16)
+        v_norms[s, L:] = nan
+    signs = np.where(g.integers(0, 2, D) == 1, 1.0, -1.0).astype(np.float32)
+    cents = (np.array(LLOYD_MAX_2BIT) / math.sqrt(D)).astype(np.float32)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    return TqCase(name, q_rot, q_jl, k_polar, k_jl, k_norms.astype(np.uint32), v_polar,
+                  v_norms.astype(np.uint32), cents, signs, float(math.sqrt(math.pi / 2) / D),
+                  scale, kv_len, seq_of, seed)
+
+
 def make_block_scores(seed, n_tok, stride, levels=None) -> np.ndarray:
     """Block scores [n_tok][stride] fp32 for the top-k selection: N(0, 1), or (``levels``) drawn
     from that many distinct values so that equal scores cross the selection threshold."""

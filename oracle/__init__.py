@@ -15,6 +15,8 @@ from .gqa_oracle import (  # noqa: F401
     attend_positions,
     decode_f16,
     decode_q8,
+    decode_tq,
+    hadamard,
     dequant_f16,
     dequant_q8,
     gated_merge,
@@ -25,4 +27,6 @@ from .gqa_oracle import (  # noqa: F401
     selected_positions,
     split_partials_f16,
     split_partials_q8,
+    unpack_polar,
+    unpack_signs,
 )

@@ -28,6 +28,8 @@ Passages followed (page title, then the part of it):
   * flash_attention_tq.metal (cera 0.4.0 sources): a causal row at position p attends to [0, p].
   * qsa2.metal (regolith), qsa_topk2: the selected-cell id list, top `budget` cells by block score.
   * FORWARD_MSL (cherenkov docs), kv_append_q8: quantise-on-append, amax / 127 and rint.
+  * flash_attention_tq.metal (cera 0.4.0 sources): decode over a TurboQuant cache (PolarQuant
+    centroid dot plus QJL sign correction, rotated-space accumulation, inverse Hadamard).
 
 Readings taken where the pages leave a step open are listed in DESIGN.md ("Readings").
 """
@@ -296,3 +298,85 @@ def gated_merge(acc, m, l, n_valid, gate) -> np.ndarray:
     of each head's [query | gate] pair on those pages)."""
     g = np.asarray(gate, np.float64)
     return lse_merge(acc, m, l, n_valid) * (1.0 / (1.0 + np.exp(-g)))
+
+
+# ----------------------------------------------------------------------------- TurboQuant KV
+
+def unpack_polar(words, D: int) -> np.ndarray:
+    """2-bit centroid indices, 16 per uint32, index k of a word in bits 2k..2k+1
+    (flash_attention_tq.metal, the PolarQuant fields)."""
+    w = np.asarray(words, dtype=np.uint64)[..., :, None]
+    return ((w >> (2 * np.arange(16, dtype=np.uint64))) & 3).reshape(w.shape[:-2] + (D,))
+
+
+def unpack_signs(words, D: int) -> np.ndarray:
+    """QJL sign bits, 32 per uint32, bit k of a word for dim 32 w + k, as +-1."""
+    w = np.asarray(words, dtype=np.uint64)[..., :, None]
+    b = ((w >> np.arange(32, dtype=np.uint64)) & 1).reshape(w.shape[:-2] + (D,))
+    return 2.0 * b.astype(np.float64) - 1.0
+
+
+def half_pair(words):
+    """(low f16, high f16) of uint32 words, widened to float64."""
+    w = np.asarray(words, dtype=np.uint32)
+    lo = (w & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+    hi = (w >> 16).astype(np.uint16).view(np.float16).astype(np.float64)
+    return lo, hi
+
+
+def hadamard(D: int) -> np.ndarray:
+    """Walsh-Hadamard matrix in Sylvester order, H[i, j] = (-1)^popcount(i & j) (unnormalised;
+    the butterfly of flash_attention_tq.metal's epilogue computes H x)."""
+    i = np.arange(D)
+    bits = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    return np.where(bits % 2 == 0, 1.0, -1.0)
+
+
+def decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, signs,
+              qjl_scale, scale, kv_len, seq_of=None, rows=None) -> np.ndarray:
+    """Decode attention over a TurboQuant-compressed cache (flash_attention_tq.metal); float64.
+
+    Layouts (position-major like the other caches): k_polar, v_polar [n_seq][cap][Hk][D/16]
+    uint32; k_jl [n_seq][cap][Hk][D/32] uint32; k_norms [n_seq][cap][Hk] uint32 = (f16 norm,
+    f16 residual norm) in the (low, high) halves; v_norms [n_seq][cap][Hk] uint32, f16 norm in
+    the low half.  q_rot, q_jl [T][H][D] fp32 (the query already rotated and JL-projected).
+    For row t, head h (KV head g = h // G) and visited position j:
+
+        polar_j = sum_d q_rot[d] c[kidx_j(d)]
+        signed_j = sum_d q_jl[d] s_j(d)                 (s = +-1 from the sign bits)
+        x_j = (norm_j polar_j + norm_j rn_j qjl_scale signed_j) scale
+        acc[d] = sum_j softmax(x)_j vnorm_j c[vidx_j(d)]            (rotated space)
+        out = signs * (H acc) / sqrt(D)                  (the inverse randomized Hadamard)
+
+    The page's precomputed per-head sum of q_jl is the sum over d of q_jl[d]: with it, twice the
+    sum over set bits minus that sum is signed_j.  An empty row gives zeros.
+    """
+    q_rot = np.asarray(q_rot, np.float64)
+    q_jl = np.asarray(q_jl, np.float64)
+    T, H, D = q_rot.shape
+    Hk = k_polar.shape[2]
+    G = H // Hk
+    c = np.asarray(centroids, np.float64)
+    Hd = hadamard(D)
+    sg = np.asarray(signs, np.float64)
+    rows = range(T) if rows is None else list(rows)
+    out = np.zeros((len(rows), H, D))
+    for i, t in enumerate(rows):
+        s = t if seq_of is None else int(seq_of[t])
+        L = max(int(kv_len[t]), 0)
+        if L == 0:
+            continue
+        for h in range(H):
+            g = _kv_head_of(h, G)
+            kidx = unpack_polar(k_polar[s, :L, g], D)
+            ks = unpack_signs(k_jl[s, :L, g], D)
+            norm, rn = half_pair(k_norms[s, :L, g])
+            vidx = unpack_polar(v_polar[s, :L, g], D)
+            vnorm, _ = half_pair(v_norms[s, :L, g])
+            polar = c[kidx] @ q_rot[t, h]
+            signed = ks @ q_jl[t, h]
+            x = (norm * polar + norm * rn * qjl_scale * signed) * scale
+            w = _softmax_rows(x[None, :])[0]
+            acc = w @ (vnorm[:, None] * c[vidx])
+            out[i, h] = sg * (Hd @ acc) / np.sqrt(D)
+    return out

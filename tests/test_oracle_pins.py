@@ -296,3 +296,80 @@ def test_gated_merge_closed_forms():
                        atol=1e-16)
     g = np.full((1, 1, 64), np.log(3.0))  # sigmoid(ln 3) = 3/4
     assert np.allclose(oracle.gated_merge(acc, m, l, [2], g), 0.75 * base, rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------- TurboQuant
+
+def _tq_oracle(c, rows=None):
+    return oracle.decode_tq(c.q_rot, c.q_jl, c.k_polar, c.k_jl, c.k_norms, c.v_polar, c.v_norms,
+                            c.centroids, c.signs, c.qjl_scale, c.scale, c.kv_len, c.seq_of, rows)
+
+
+def _tq_dense_reference(c):
+    """The same attention built another way: keys and values reconstructed element by element
+    with Python integer bit operations, the query as the concatenation [q_rot | q_jl], the
+    (pinned) dense oracle's attend_positions, then the inverse rotation as an explicit sum."""
+    T, H, D = c.q_rot.shape
+    G = H // c.n_kv_heads
+    out = np.zeros((T, H, D))
+    f16 = lambda bits: float(np.uint16(bits).view(np.float16))  # noqa: E731
+    for t in range(T):
+        s, L = int(c.seq_of[t]), int(c.kv_len[t])
+        for h in range(H):
+            g = h // G
+            K2, V = [], []
+            for j in range(L):
+                kw = int(c.k_norms[s, j, g])
+                norm, rn = f16(kw & 0xFFFF), f16(kw >> 16)
+                vn = f16(int(c.v_norms[s, j, g]) & 0xFFFF)
+                kp = [float(c.centroids[(int(c.k_polar[s, j, g, d // 16]) >> (2 * (d % 16))) & 3])
+                      for d in range(D)]
+                sb = [1.0 if (int(c.k_jl[s, j, g, d // 32]) >> (d % 32)) & 1 else -1.0
+                      for d in range(D)]
+                vp = [float(c.centroids[(int(c.v_polar[s, j, g, d // 16]) >> (2 * (d % 16))) & 3])
+                      for d in range(D)]
+                K2.append([norm * x for x in kp] + [norm * rn * c.qjl_scale * x for x in sb])
+                V.append([vn * x for x in vp])
+            q2 = np.concatenate([c.q_rot[t, h], c.q_jl[t, h]]).astype(np.float64)[None]
+            acc = oracle.attend_positions(q2, np.array(K2), np.array(V), c.scale)[0] if L else \
+                np.zeros(D)
+            for i in range(D):
+                hs = sum((acc[j] if bin(i & j).count("1") % 2 == 0 else -acc[j]) for j in range(D))
+                out[t, h, i] = float(c.signs[i]) * hs / np.sqrt(D)
+    return out
+
+
+def test_tq_matches_dense_reconstruction():
+    c = W.make_tq_case(31, 3, 4, 2, 32, [9, 0, 4], cache_cap=10)
+    np.testing.assert_allclose(_tq_oracle(c), _tq_dense_reference(c), rtol=1e-12, atol=1e-13)
+
+
+def test_tq_constant_values_rotate_to_one_spike():
+    # every V index the same centroid and equal V norms: acc is constant, so H acc = D acc e_0
+    c = W.make_tq_case(32, 1, 2, 1, 64, [12])
+    c.v_polar[:] = np.uint32(0xAAAAAAAA)            # index 2 in every field
+    c.v_norms[0, :12] = W._half_bits(1.25)
+    got = _tq_oracle(c)
+    spike = float(c.signs[0]) * 64 * 1.25 * float(c.centroids[2]) / np.sqrt(64)
+    assert np.allclose(got[0, :, 0], spike, rtol=1e-12) and np.allclose(got[0, :, 1:], 0, atol=1e-14)
+
+
+def test_hadamard_is_self_inverse_up_to_d():
+    for D in (32, 64, 128):
+        H = oracle.hadamard(D)
+        assert np.array_equal(H @ H, D * np.eye(D)) and (H[0] == 1).all()
+
+
+@pytest.mark.parametrize("name", ["polar bit order", "signs as bits", "no sqrt(D)"])
+def test_planted_tq_mistakes_are_caught(name, monkeypatch):
+    c = W.make_tq_case(33, 2, 4, 2, 32, [6, 3], cache_cap=6)
+    ref = _tq_dense_reference(c)
+    if name == "polar bit order":
+        monkeypatch.setattr(OG, "unpack_polar", lambda w, D: ((np.asarray(w, np.uint64)[..., :, None] >> (30 - 2 * np.arange(16, dtype=np.uint64))) & 3).reshape(np.asarray(w).shape[:-1] + (D,)))  # noqa: E501
+    elif name == "signs as bits":
+        orig = OG.unpack_signs
+        monkeypatch.setattr(OG, "unpack_signs", lambda w, D: (orig(w, D) + 1) / 2)
+    else:
+        orig = OG.hadamard
+        monkeypatch.setattr(OG, "hadamard", lambda D: orig(D) * np.sqrt(D))
+    assert not np.allclose(_tq_oracle(c), ref, rtol=1e-9, atol=1e-12)
