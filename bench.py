@@ -34,6 +34,8 @@ from gqa_decode_attention_03_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention µs/step and KV-read GB/s (% of GB300 HBM peak), 1 GPU"
 FLUSH_BYTES = 512 << 20
+# fp32 FMA peak of a GB300: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 L2_BYTES = 129 << 20
 
 
@@ -161,6 +163,12 @@ def max_over_ranks(values):
 
 def _device_inputs(case, torch):
     d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    if case.kind == "tq":
+        w = lambda x: d(np.ascontiguousarray(x).view(np.int32))  # noqa: E731
+        return {"q": d(case.q_rot), "q_jl": d(case.q_jl), "kv_len": d(case.kv_len),
+                "seq_of": d(case.seq_of), "k_polar": w(case.k_polar), "k_jl": w(case.k_jl),
+                "k_norms": w(case.k_norms), "v_polar": w(case.v_polar),
+                "v_norms": w(case.v_norms), "signs": d(case.signs)}
     t = {"q": d(case.q), "kv_len": d(case.kv_len), "seq_of": d(case.seq_of)}
     if case.kind == "f16":
         t.update(k=d(case.k), v=d(case.v))
@@ -176,6 +184,8 @@ def _merge_launch(plan):
 
 
 def _kernel_name(case, plan):
+    if case.kind == "tq":
+        return "tq_decode_kernel" + (" (split-KV, merge fused)" if plan.merge else "")
     if plan.streamk:
         return "streamk_mma_kernel (stream-K split, merge fused)"
     if plan.row_group > 1:
@@ -204,7 +214,7 @@ def run_gpu(args):
     x = _device_inputs(case, torch)
     T, H, D, Hk = case.n_tok, case.n_heads, case.head_dim, case.n_kv_heads
     max_len = int(min(case.cache_cap, case.kv_len.max()))
-    kind = gd.KIND_F16 if case.kind == "f16" else gd.KIND_Q8
+    kind = {"f16": gd.KIND_F16, "q8": gd.KIND_Q8, "tq": gd.KIND_TQ}[case.kind]
     budget = -1 if case.ids is None else int(case.budget)
     plan = gd.plan(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
     ws = gd.alloc_workspace(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
@@ -216,9 +226,16 @@ def run_gpu(args):
         x["scores"] = torch.from_numpy(scores).cuda()
         x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
 
-    def step(q=None, kv=None):
+    def step(q=None, kv=None, q_jl=None):
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
+        if case.kind == "tq":
+            gd.attn_decode_tq(q, x["q_jl"] if q_jl is None else q_jl, x["k_polar"], x["k_jl"],
+                              x["k_norms"], x["v_polar"], x["v_norms"], case.centroids,
+                              x["signs"], case.qjl_scale, kv, scale=case.scale,
+                              seq_of=x["seq_of"], max_kv_len=max_len, out=out, ws=ws,
+                              stream=stream)
+            return
         if scores is not None:
             gd.attn_select_topk(x["scores"], kv, case.budget, max_kv_len=case.cache_cap,
                                 ids=x["ids"], stream=stream)
@@ -266,10 +283,13 @@ def run_gpu(args):
         torch.distributed.barrier()
 
     # end to end through host buffers: pinned q / kv_len in, out back, every step
-    q_h = torch.from_numpy(case.q).pin_memory()
+    q_host = case.q_rot if case.kind == "tq" else case.q
+    q_h = torch.from_numpy(q_host).pin_memory()
+    qj_h = torch.from_numpy(case.q_jl).pin_memory() if case.kind == "tq" else None
     kv_h = torch.from_numpy(case.kv_len).pin_memory()
     out_h = torch.empty((T, H, D), dtype=torch.float32).pin_memory()
     q_d, kv_d = torch.empty_like(x["q"]), torch.empty_like(x["kv_len"])
+    qj_d = torch.empty_like(x["q"]) if qj_h is not None else None
     Ke = min(K, 500)
     eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(Ke)]
@@ -278,8 +298,10 @@ def run_gpu(args):
             flush.zero_()
         a.record(stream)
         q_d.copy_(q_h, non_blocking=True)
+        if qj_d is not None:
+            qj_d.copy_(qj_h, non_blocking=True)
         kv_d.copy_(kv_h, non_blocking=True)
-        step(q_d, kv_d)
+        step(q_d, kv_d, qj_d)
         out_h.copy_(out, non_blocking=True)
         b.record(stream)
     torch.cuda.synchronize()
@@ -295,22 +317,37 @@ def run_gpu(args):
     achieved = alg / (ms * 1e-3) / 1e9
     traffic = _ncu_traffic(case.name)
     gbs = world * alg / (ms * 1e-3) / 1e9
+    h2d = int(q_host.nbytes + case.kv_len.nbytes + (case.q_jl.nbytes if qj_h is not None else 0))
+    data = ("synthetic: seeded N(0,1) q and f16 K/V, NaN past each sequence's length"
+            if case.kind != "tq" else
+            "synthetic: seeded N(0,1) rotated / JL queries, uniform random 2-bit indices and sign "
+            "bits, f16 norms, Lloyd-Max 2-bit centroids; NaN norms past each length")
+    if case.kind == "tq":
+        tflops = case.flops() / (ms * 1e-3) / 1e12
+        roofline = {"bound": "alu", "kernel": _kernel_name(case, plan),
+                    "achieved": round(tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 2),
+                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
+                    "unit": "TFLOP/s", "frac": round(tflops / FP32_PEAK_TFLOPS, 4),
+                    "traffic": traffic, "hbm_achieved_gbs": round(achieved, 1),
+                    "hbm_frac": round(achieved / peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": _kernel_name(case, plan),
+                    "achieved": round(achieved, 1),
+                    "peak": peak, "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)"
+                    if peak_src == "measured" else "fallback 6.8 TB/s",
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic}
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s",
         "us_per_step": round(ms * 1e3, 3), "frac_of_hbm_peak": round(gbs / world / peak, 4),
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic: seeded N(0,1) q and f16 K/V, NaN past each sequence's length",
+        "data": data,
         "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
                                  "n_split": plan.n_split, "parallelism": f"replicas x{world}"}),
-        "roofline": {"bound": "hbm", "kernel": _kernel_name(case, plan),
-                     "achieved": round(achieved, 1),
-                     "peak": peak, "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)"
-                     if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic},
+        "roofline": roofline,
         "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
-                "h2d_bytes_per_step": int(case.q.nbytes + case.kv_len.nbytes),
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(T * H * D * 4)},
         "gpu_launches": int(K * (1 + (scores is not None) + _merge_launch(plan))),
         "clocks": clk.summary(),
@@ -329,10 +366,15 @@ def _oracle_pair(case, t, g):
     """The oracle on one (row, KV head) of the case: the G query heads of KV head g."""
     import oracle
     G = case.n_heads // case.n_kv_heads
-    q = case.q[t:t + 1, g * G:(g + 1) * G]
     s = int(case.seq_of[t])
     L = case.kv_len[t:t + 1]
-    if case.kind == "f16":
+    if case.kind == "tq":
+        sl = (slice(s, s + 1), slice(None), slice(g, g + 1))
+        return oracle.decode_tq(case.q_rot[t:t + 1, g * G:(g + 1) * G],
+                                case.q_jl[t:t + 1, g * G:(g + 1) * G], case.k_polar[sl],
+                                case.k_jl[sl], case.k_norms[sl], case.v_polar[sl],
+                                case.v_norms[sl], case.centroids, case.signs, case.qjl_scale,
+                                case.scale, L, seq_of=[0])
         return oracle.decode_f16(q, case.k[s:s + 1, :, g:g + 1], case.v[s:s + 1, :, g:g + 1], L,
                                  case.scale, seq_of=[0])
     ids = None if case.ids is None else case.ids[t:t + 1]
@@ -342,6 +384,8 @@ def _oracle_pair(case, t, g):
 
 
 def _pair_bytes(case, t):
+    if case.kind == "tq":
+        return case.visited(t) * case.pos_bytes()
     D = case.head_dim
     per_pos = 2 * D * 2 if case.kind == "f16" else 2 * (D + 2 * (D // 64))
     return case.visited(t) * per_pos

@@ -92,7 +92,8 @@ constexpr long long kMinSplitBytes = 128 << 10;
 // Shapes that do not depend on the device.
 gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                        int kind) {
-  if (kind != GQA_KIND_F16 && kind != GQA_KIND_Q8) return fail(GQA_EINVAL, "kind must be 0 or 1");
+  if (kind != GQA_KIND_F16 && kind != GQA_KIND_Q8 && kind != GQA_KIND_TQ)
+    return fail(GQA_EINVAL, "kind must be 0, 1 or 2");
   if (n_tok < 0 || n_tok > 65535) return fail(GQA_EINVAL, "n_tok %d outside [0, 65535]", n_tok);
   if (n_heads <= 0 || n_kv_heads <= 0 || n_kv_heads > 65535)
     return fail(GQA_EINVAL, "n_heads %d / n_kv_heads %d", n_heads, n_kv_heads);
@@ -124,6 +125,7 @@ Variant pick_variant(int heads_per_cta) {
 // size that gets there -- so a wide group (12 heads) spreads over three times as many CTAs.
 // The tensor-core kernels serve the whole group in one CTA.
 int head_split_for(int kind, int group) {
+  if (kind == GQA_KIND_TQ) return 1;  // the TurboQuant kernel serves the whole group
   const char* k = std::getenv("GQA_F16_KERNEL");
   const bool fma = kind == GQA_KIND_Q8 || (k && std::strcmp(k, "fma") == 0);
   if (!fma) return 1;
@@ -156,6 +158,7 @@ int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
 }
 
 int stage_rows(int kind, int head_dim) {
+  if (kind == GQA_KIND_TQ) return 128;  // 4 warps x 32 positions per pass
   if (kind == GQA_KIND_F16) return head_dim == 64 ? 128 : (head_dim == 128 ? 64 : 32);
   return head_dim == 256 ? 64 : 128;
 }
@@ -231,7 +234,10 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
   // D=64 4096 positions 14.7 against 16.1)
   chunk = std::max(chunk, 2LL * tile);
-  const long long row_bytes = kind == GQA_KIND_F16 ? 4LL * head_dim : 2LL * (head_dim + head_dim / 32);
+  const long long row_bytes =
+      kind == GQA_KIND_F16   ? 4LL * head_dim
+      : kind == GQA_KIND_Q8 ? 2LL * (head_dim + head_dim / 32)
+                             : 4LL * (head_dim / 16 + head_dim / 32 + 1) + 4LL * (head_dim / 16 + 1);
   if (nmax * row_bytes <= kMinSplitBytes) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");
   if (forced > 0) chunk = forced;

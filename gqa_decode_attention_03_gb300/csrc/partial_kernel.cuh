@@ -203,9 +203,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 // on the last ticket, so every call leaves it at zero.  Nobody waits for anybody: the CTAs that
 // are not last simply finish.  One warp per head; lane c holds chunk c's (m, l) and weight and
 // broadcasts the weight by shuffle, so a head's loads go out in one round.
-template <int D>
+struct NoEpilogue {  // merge_if_last writes the merged rows as they are
+  template <int N>
+  __device__ __forceinline__ void operator()(float (&)[N], int /*head*/, int /*lane*/) const {}
+};
+
+template <int D, class Epi = NoEpilogue>
 __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int head0,
-                                              int nheads, size_t counter, int nv, int ncw) {
+                                              int nheads, size_t counter, int nv, int ncw,
+                                              const Epi& epi = Epi()) {
   __shared__ int s_last;
   __threadfence();  // this thread's partial stores, visible device-wide before the ticket
   named_bar_sync(1, ncw * 32);
@@ -253,8 +259,10 @@ __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
-    for (int k = 0; k < DPL; k += 2)
-      *reinterpret_cast<float2*>(o + k) = make_float2(a[k] * inv, a[k + 1] * inv);
+    for (int k = 0; k < DPL; ++k) a[k] *= inv;
+    epi(a, head, lane);  // e.g. the inverse rotation of a rotated-space accumulator
+#pragma unroll
+    for (int k = 0; k < DPL; k += 2) *reinterpret_cast<float2*>(o + k) = make_float2(a[k], a[k + 1]);
   }
 }
 

@@ -1,0 +1,403 @@
+// tq_decode.cu -- decode attention over a TurboQuant-compressed KV cache.
+//
+// flash_attention_tq.metal (cera 0.4.0 sources).  Keys are never reconstructed: a key's score
+// is a PolarQuant term, its 2-bit centroid indices dotted with the rotated query, plus a QJL
+// correction from its sign bits and residual norm:
+//   x_j = (norm_j sum_d q_rot[d] c[kidx_j(d)] + norm_j rn_j qjl_scale sum_d q_jl[d] s_j(d)) scale
+// and values are accumulated in the rotated basis, vnorm_j c[vidx_j(d)], so the inverse
+// rotation -- 1/sqrt(D), a Walsh-Hadamard transform, the sign flip -- runs once on the merged
+// row.  The page's per-head sum of q_jl turns the sum over set sign bits into the signed sum.
+//
+// GB300 layout of the work: one CTA per (KV chunk, KV head, query row), like the other decode
+// kernels, with every query head of the KV head's group served from the same decoded key: q.k
+// gives each lane one cache position (its 2-bit fields and sign bits decoded once, dotted with
+// every head's rotated query, broadcast from shared memory), p.v gives each lane D/32 dims of
+// the rotated accumulator.  Rows longer than a chunk write rotated partials and the last CTA
+// of the (row, KV head) merges them (merge_if_last) and applies the inverse rotation.
+// Packed format as on the page (16 two-bit indices per uint32, index k in bits 2k..2k+1; 32
+// sign bits per uint32; f16 norm pairs), stored position-major like the other caches.
+#include <cuda_fp16.h>
+#include <cuda_runtime_api.h>
+
+#include <cmath>
+
+#include "dispatch.h"
+
+namespace gqa {
+
+void set_last_error(const char* msg);
+
+constexpr int kTqWarps = 4;
+constexpr int kTqMaxGroup = 8;
+
+struct TqParams {
+  PartialParams base;          // q unused; out, part, counters, n_valid, lengths, sizes
+  const float* q_rot;          // [T][H][D]
+  const float* q_jl;           // [T][H][D]
+  const uint32_t* k_polar;     // [n_seq][cap][Hk][D/16]
+  const uint32_t* k_jl;        // [n_seq][cap][Hk][D/32]
+  const uint32_t* k_norms;     // [n_seq][cap][Hk]
+  const uint32_t* v_polar;     // [n_seq][cap][Hk][D/16]
+  const uint32_t* v_norms;     // [n_seq][cap][Hk]
+  const float* signs;          // [D]
+  float c0, c1, c2, c3;        // centroids
+  float qjl_scale;
+};
+
+__device__ __forceinline__ float tq_centroid(uint32_t idx, float c0, float c1, float c2, float c3) {
+  return (idx & 2u) ? ((idx & 1u) ? c3 : c2) : ((idx & 1u) ? c1 : c0);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// Inverse rotation of a merged rotated row held D/32 consecutive dims per lane: scale by
+// 1/sqrt(D), the Walsh-Hadamard butterflies (within the lane for strides below D/32, across
+// lanes by shuffle above), then the sign flip.
+template <int D>
+struct TqRotateBack {
+  const float* signs;
+  __device__ __forceinline__ void operator()(float (&a)[D / 32], int /*head*/, int lane) const {
+    constexpr int DPL = D / 32;
+    const float s = rsqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a[k] *= s;
+#pragma unroll
+    for (int stride = 1; stride < DPL; stride <<= 1)
+#pragma unroll
+      for (int k = 0; k < DPL; ++k)
+        if ((k & stride) == 0) {
+          const float x = a[k], y = a[k + stride];
+          a[k] = x + y;
+          a[k + stride] = x - y;
+        }
+#pragma unroll
+    for (int stride = DPL; stride < D; stride <<= 1) {
+      const int lmask = stride / DPL;
+      const bool high = (lane & lmask) != 0;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) {
+        const float other = __shfl_xor_sync(0xffffffffu, a[k], lmask);
+        a[k] = high ? other - a[k] : a[k] + other;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a[k] *= __ldg(signs + lane * DPL + k);
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams tp) {
+  constexpr int DPL = D / 32, PW = D / 16, JW = D / 32;
+  const PartialParams& p = tp.base;
+  __shared__ __align__(16) float qr[kTqMaxGroup][D];
+  __shared__ __align__(16) float qj[kTqMaxGroup][D];
+  __shared__ float qjsum[kTqMaxGroup];
+  __shared__ uint32_t vbuf[kTqWarps][32][PW];
+  __shared__ float mg[kTqWarps][kTqMaxGroup][D + 2];
+  const int c = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
+  const int G = p.group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int L = __ldg(p.kv_len + t);
+  int errbits = 0;
+  const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
+  if (L < 0 || L > lmax) {
+    errbits |= GQA_ERR_KVLEN_RANGE;
+    L = L < 0 ? 0 : lmax;
+  }
+  const int s = p.seq_of ? __ldg(p.seq_of + t) : t;
+  if (s < 0 || s >= p.n_seq) {
+    errbits |= GQA_ERR_SEQ_RANGE;
+    L = 0;
+  }
+  const int c0 = c * p.chunk, c1 = min(c0 + p.chunk, L);
+  if (c == 0 && g == 0 && threadIdx.x == 0) {
+    if (errbits) flag_error(p.err, errbits);
+    if (p.merge) p.n_valid[t] = (L + p.chunk - 1) / p.chunk;
+  }
+  if (c0 >= L) {
+    if (c == 0)  // empty context: zeros (flash_attention_tq.metal, seq_len == 0)
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+        p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
+    return;
+  }
+
+  // the group's rotated and JL queries, and the per-head sum of q_jl
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const size_t qi = ((size_t)t * p.n_heads + g * G) * D + i;
+    qr[i / D][i % D] = __ldg(tp.q_rot + qi);
+    qj[i / D][i % D] = __ldg(tp.q_jl + qi);
+  }
+  __syncthreads();
+  for (int h = warp; h < G; h += kTqWarps) {
+    float x = 0.f;
+    for (int d = lane; d < D; d += 32) x += qj[h][d];
+    x = warp_sum(x);
+    if (lane == 0) qjsum[h] = x;
+  }
+  __syncthreads();
+
+  const float kx = p.scale_log2;  // scores in log2 units
+  float m_run[kTqMaxGroup], l_run[kTqMaxGroup], acc[kTqMaxGroup][DPL];
+#pragma unroll
+  for (int h = 0; h < kTqMaxGroup; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
+  }
+
+  for (int base = c0 + warp * 32; base < c1; base += kTqWarps * 32) {
+    const int pos = base + lane;
+    const bool valid = pos < c1;
+    const int nvb = min(32, c1 - base);  // valid positions of the block, a prefix
+    const size_t row = ((size_t)s * p.cache_cap + (valid ? pos : c0)) * p.n_kv_heads + g;
+    float x[kTqMaxGroup];
+    float vn = 0.f;
+    {
+      uint32_t kp[PW], kj[JW], vp[PW];
+#pragma unroll
+      for (int w = 0; w < PW; w += 4) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(tp.k_polar + row * PW + w));
+        kp[w] = u.x; kp[w + 1] = u.y; kp[w + 2] = u.z; kp[w + 3] = u.w;
+        const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(tp.v_polar + row * PW + w));
+        vp[w] = v4.x; vp[w + 1] = v4.y; vp[w + 2] = v4.z; vp[w + 3] = v4.w;
+      }
+#pragma unroll
+      for (int w = 0; w < JW; w += 2) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(tp.k_jl + row * JW + w));
+        kj[w] = u.x; kj[w + 1] = u.y;
+      }
+      const uint32_t kn = __ldg(tp.k_norms + row);
+      vn = half_lo(__ldg(tp.v_norms + row));
+#pragma unroll
+      for (int w = 0; w < PW; ++w) vbuf[warp][lane][w] = vp[w];
+      float polar[kTqMaxGroup], pos_sum[kTqMaxGroup];
+#pragma unroll
+      for (int h = 0; h < kTqMaxGroup; ++h) polar[h] = pos_sum[h] = 0.f;
+#pragma unroll
+      for (int w = 0; w < PW; ++w) {
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          float cv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            cv[e] = tq_centroid((kp[w] >> (2 * (k4 + e))) & 3u, tp.c0, tp.c1, tp.c2, tp.c3);
+#pragma unroll
+          for (int h = 0; h < kTqMaxGroup; ++h) {
+            if (h >= G) break;
+            const float4 q4 = *reinterpret_cast<const float4*>(&qr[h][w * 16 + k4]);
+            polar[h] = fmaf(q4.x, cv[0], fmaf(q4.y, cv[1], fmaf(q4.z, cv[2], fmaf(q4.w, cv[3], polar[h]))));
+          }
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < JW; ++w) {
+#pragma unroll
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+          float b[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) b[e] = static_cast<float>((kj[w] >> (k4 + e)) & 1u);
+#pragma unroll
+          for (int h = 0; h < kTqMaxGroup; ++h) {
+            if (h >= G) break;
+            const float4 q4 = *reinterpret_cast<const float4*>(&qj[h][w * 32 + k4]);
+            pos_sum[h] = fmaf(q4.x, b[0], fmaf(q4.y, b[1], fmaf(q4.z, b[2], fmaf(q4.w, b[3], pos_sum[h]))));
+          }
+        }
+      }
+      const float norm = half_lo(kn), rn = half_hi(kn);
+#pragma unroll
+      for (int h = 0; h < kTqMaxGroup; ++h) {
+        const float signed_sum = 2.f * pos_sum[h] - qjsum[h < G ? h : 0];
+        const float sc = (norm * polar[h] + norm * rn * tp.qjl_scale * signed_sum) * kx;
+        x[h] = (valid && h < G) ? sc : -INFINITY;  // masked by selection: no NaN gets through
+      }
+    }
+    __syncwarp();
+    // online softmax per head over the block (every block holds at least one valid position)
+    float pr[kTqMaxGroup];
+#pragma unroll
+    for (int h = 0; h < kTqMaxGroup; ++h) {
+      if (h >= G) break;
+      const float m_new = fmaxf(m_run[h], warp_max(x[h]));
+      const float corr = fast_exp2(m_run[h] - m_new);  // first block: exp2(-inf) = 0
+      pr[h] = fast_exp2(x[h] - m_new);
+      l_run[h] = fmaf(l_run[h], corr, warp_sum(pr[h]));
+      m_run[h] = m_new;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) acc[h][k] *= corr;
+    }
+    // p.v in the rotated basis: this lane's dims lane*DPL .. + DPL-1
+    const int vw = (lane * DPL) / 16, vsh = 2 * ((lane * DPL) % 16);
+    for (int j = 0; j < nvb; ++j) {
+      const uint32_t word = vbuf[warp][j][vw] >> vsh;
+      const float vnj = __shfl_sync(0xffffffffu, vn, j);
+      float cv[DPL];
+#pragma unroll
+      for (int k = 0; k < DPL; ++k)
+        cv[k] = vnj * tq_centroid((word >> (2 * k)) & 3u, tp.c0, tp.c1, tp.c2, tp.c3);
+#pragma unroll
+      for (int h = 0; h < kTqMaxGroup; ++h) {
+        if (h >= G) break;
+        const float ph = __shfl_sync(0xffffffffu, pr[h], j);
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(ph, cv[k], acc[h][k]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- merge the warps' states, then write the output or the chunk's partial
+#pragma unroll
+  for (int h = 0; h < kTqMaxGroup; ++h) {
+    if (h >= G) break;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) mg[warp][h][lane * DPL + k] = acc[h][k];
+    if (lane == 0) {
+      mg[warp][h][D] = m_run[h];
+      mg[warp][h][D + 1] = l_run[h];
+    }
+  }
+  __syncthreads();
+  const TqRotateBack<D> rot{tp.signs};
+  for (int h = warp; h < G; h += kTqWarps) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kTqWarps; ++w) M = fmaxf(M, mg[w][h][D]);
+    float a[DPL], Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a[k] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kTqWarps; ++w) {
+      const float e = mg[w][h][D] == -INFINITY ? 0.f : fast_exp2(mg[w][h][D] - M);
+      Ls = fmaf(mg[w][h][D + 1], e, Ls);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) a[k] = fmaf(mg[w][h][lane * DPL + k], e, a[k]);
+    }
+    const int head = g * G + h;
+    if (p.merge) {
+      float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) pr[lane * DPL + k] = a[k];
+      if (lane == 0) {
+        pr[D] = M == -INFINITY ? -INFINITY : M * kLn2;
+        pr[D + 1] = Ls;
+      }
+    } else {
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) a[k] *= inv;
+      rot(a, head, lane);
+      float* o = p.out + ((size_t)t * p.n_heads + head) * D + lane * DPL;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[k] = a[k];
+    }
+  }
+  if (p.merge) {
+    merge_if_last<D>(p, t, g * G, G, (size_t)t * p.n_kv_heads + g, (L + p.chunk - 1) / p.chunk,
+                     kTqWarps, rot);
+  }
+}
+
+}  // namespace gqa
+
+// ------------------------------------------------------------------------------ C ABI
+
+static gqa_status tq_fail(gqa_status st, const char* msg) {
+  gqa::set_last_error(msg);
+  return st;
+}
+
+static bool tq_aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
+                                     const uint32_t* k_polar, const uint32_t* k_jl,
+                                     const uint32_t* k_norms, const uint32_t* v_polar,
+                                     const uint32_t* v_norms, const float* centroids,
+                                     const float* signs, float qjl_scale, float scale, float* out,
+                                     const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                     int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                     int64_t cache_cap, int max_kv_len, void* ws, size_t ws_bytes,
+                                     int32_t* err_word, cudaStream_t stream) {
+  if (head_dim != 64 && head_dim != 128)
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: head_dim must be 64 or 128");
+  if (n_kv_heads <= 0 || n_heads % n_kv_heads)
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: n_heads must be a positive multiple of n_kv_heads");
+  if (n_heads / n_kv_heads > gqa::kTqMaxGroup)
+    return tq_fail(GQA_EUNSUPPORTED, "attn_decode_tq: group size above 8");
+  if (n_tok < 0 || n_tok > 65535) return tq_fail(GQA_EINVAL, "attn_decode_tq: n_tok outside [0, 65535]");
+  if (n_tok == 0) return GQA_OK;
+  if (!q_rot || !q_jl || !k_polar || !k_jl || !k_norms || !v_polar || !v_norms || !centroids ||
+      !signs || !out || !kv_len)
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: a required pointer is NULL");
+  if (!tq_aligned16(k_polar) || !tq_aligned16(v_polar) || !tq_aligned16(k_jl) ||
+      (reinterpret_cast<uintptr_t>(out) & 7))
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: packed caches 16-byte, out 8-byte aligned");
+  if (n_seq <= 0 || cache_cap <= 0 || max_kv_len < 0)
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: n_seq, cache_cap > 0, max_kv_len >= 0");
+  if (!seq_of && n_seq < n_tok) return tq_fail(GQA_EINVAL, "seq_of NULL needs n_seq >= n_tok");
+  if (!std::isfinite(scale) || !std::isfinite(qjl_scale))
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: scale and qjl_scale must be finite");
+  const int max_len = (int)(max_kv_len < cache_cap ? max_kv_len : cache_cap);
+  gqa_plan plan;
+  gqa_status st = attn_decode_plan(n_tok, n_seq, n_heads, n_kv_heads, head_dim, max_len, -1,
+                                   GQA_KIND_TQ, 0, &plan);
+  if (st != GQA_OK) return st;
+  if (plan.merge && (!ws || ws_bytes < plan.ws_bytes || !tq_aligned16(ws)))
+    return tq_fail(GQA_EWORKSPACE, "attn_decode_tq: workspace too small or misaligned");
+
+  gqa::TqParams tp{};
+  gqa::PartialParams& p = tp.base;
+  p.out = out;
+  p.kv_len = kv_len;
+  p.seq_of = seq_of;
+  p.err = err_word;
+  p.n_tok = n_tok;
+  p.n_seq = n_seq;
+  p.n_heads = n_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.group = n_heads / n_kv_heads;
+  p.head_split = 1;
+  p.cache_cap = cache_cap;
+  p.max_kv_len = max_len;
+  p.budget = INT32_MAX;
+  p.chunk = plan.chunk;
+  p.n_split = plan.n_split;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.merge = plan.merge;
+  if (plan.merge) {
+    const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
+    const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);
+    p.counters = static_cast<unsigned int*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
+    p.n_valid =
+        reinterpret_cast<int32_t*>(static_cast<char*>(ws) + cnt + (part + 255) / 256 * 256);
+  }
+  tp.q_rot = q_rot;
+  tp.q_jl = q_jl;
+  tp.k_polar = k_polar;
+  tp.k_jl = k_jl;
+  tp.k_norms = k_norms;
+  tp.v_polar = v_polar;
+  tp.v_norms = v_norms;
+  tp.signs = signs;
+  tp.c0 = centroids[0];
+  tp.c1 = centroids[1];
+  tp.c2 = centroids[2];
+  tp.c3 = centroids[3];
+  tp.qjl_scale = qjl_scale;
+  const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
+  if (head_dim == 64)
+    gqa::tq_decode_kernel<64><<<grid, 32 * gqa::kTqWarps, 0, stream>>>(tp);
+  else
+    gqa::tq_decode_kernel<128><<<grid, 32 * gqa::kTqWarps, 0, stream>>>(tp);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
+  return GQA_OK;
+}

@@ -17,13 +17,14 @@ import torch
 _LIB_PATH = Path(__file__).resolve().parent / "lib" / "libgqadecode.so"
 
 GQA_OK, GQA_EINVAL, GQA_EWORKSPACE, GQA_EUNSUPPORTED, GQA_ECUDA = range(5)
-KIND_F16, KIND_Q8 = 0, 1
+KIND_F16, KIND_Q8, KIND_TQ = 0, 1, 2
 ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
-           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8", "attn_merge_gated")
+           "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8", "attn_merge_gated",
+           "attn_decode_tq")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -63,6 +64,9 @@ def _load():
     lib.kv_append_q8.restype = I
     lib.attn_merge_gated.argtypes = [P, P, I, I, I, I, P, I64, P, P]
     lib.attn_merge_gated.restype = I
+    lib.attn_decode_tq.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(F), P, F, F, P, P, P, I,
+                                   I, I, I, I, I64, I, P, SZ, P, P]
+    lib.attn_decode_tq.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -181,6 +185,48 @@ def attn_decode_f16_noalloc(q, k_cache, v_cache, kv_len, scale=None, seq_of=None
     _check(LIB.attn_decode_f16_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
                                        _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
                                        max_kv_len, scale, _ptr(err), _stream(stream)))
+    return out
+
+
+def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, signs,
+                   qjl_scale, kv_len, scale=None, seq_of=None, max_kv_len=None, out=None, ws=None,
+                   err=None, stream=None):
+    """Decode attention over a TurboQuant-compressed cache; returns ``out [T][H][D]`` fp32.
+
+    q_rot, q_jl [T][H][D] fp32 (the rotated and JL-projected query); packed words as int32 bit
+    patterns: k_polar, v_polar [n_seq][cap][Hk][D/16], k_jl [n_seq][cap][Hk][D/32], k_norms,
+    v_norms [n_seq][cap][Hk]; centroids: 4 host floats; signs [D] fp32 on the device.
+    """
+    _need(q_rot, torch.float32, "q_rot", 3)
+    _need(q_jl, torch.float32, "q_jl", 3)
+    _need(k_polar, torch.int32, "k_polar", 4)
+    _need(k_jl, torch.int32, "k_jl", 4)
+    _need(k_norms, torch.int32, "k_norms", 3)
+    _need(v_polar, torch.int32, "v_polar", 4)
+    _need(v_norms, torch.int32, "v_norms", 3)
+    _need(signs, torch.float32, "signs", 1)
+    _need(kv_len, torch.int32, "kv_len", 1)
+    if seq_of is not None:
+        _need(seq_of, torch.int32, "seq_of", 1)
+    T, H, D = q_rot.shape
+    n_seq, cap, Hk, _ = k_polar.shape
+    if (q_jl.shape != q_rot.shape or v_polar.shape != k_polar.shape or k_polar.shape[3] != D // 16
+            or k_jl.shape != (n_seq, cap, Hk, D // 32) or k_norms.shape != (n_seq, cap, Hk)
+            or v_norms.shape != (n_seq, cap, Hk) or signs.numel() != D or kv_len.numel() != T):
+        raise ValueError("shape mismatch between the queries, the packed caches and kv_len")
+    cents = (ctypes.c_float * 4)(*[float(x) for x in centroids])
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    max_kv_len = cap if max_kv_len is None else int(max_kv_len)
+    if out is None:
+        out = torch.empty_like(q_rot)
+    _need(out, torch.float32, "out", 3)
+    if ws is None:
+        ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_TQ, q_rot.device, n_seq)
+    _check(LIB.attn_decode_tq(_ptr(q_rot), _ptr(q_jl), _ptr(k_polar), _ptr(k_jl), _ptr(k_norms),
+                              _ptr(v_polar), _ptr(v_norms), cents, _ptr(signs), float(qjl_scale),
+                              scale, _ptr(out), _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D,
+                              cap, max_kv_len, _ptr(ws), ws.numel() * ws.element_size(),
+                              _ptr(err), _stream(stream)))
     return out
 
 

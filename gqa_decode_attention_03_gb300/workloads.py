@@ -228,15 +228,59 @@ class TqCase:
     kv_len: np.ndarray
     seq_of: np.ndarray
     seed: int = 0
+    kind: str = "tq"
+    ids = None
+    budget = None
+    meta: dict = field(default_factory=dict)
 
     @property
     def n_kv_heads(self):
         return self.k_polar.shape[2]
 
+    @property
+    def n_tok(self):
+        return self.q_rot.shape[0]
+
+    @property
+    def n_heads(self):
+        return self.q_rot.shape[1]
+
+    @property
+    def head_dim(self):
+        return self.q_rot.shape[2]
+
+    @property
+    def n_seq(self):
+        return self.k_polar.shape[0]
+
+    @property
+    def cache_cap(self):
+        return self.k_polar.shape[1]
+
+    def visited(self, t: int) -> int:
+        return max(int(self.kv_len[t]), 0)
+
+    def pos_bytes(self) -> int:
+        """Packed bytes of one (position, KV head): K polar + sign words + norm pair, V polar +
+        norm."""
+        D = self.head_dim
+        return 4 * (D // 16 + D // 32 + 1) + 4 * (D // 16 + 1)
+
     def kv_bytes(self) -> int:
-        D = self.q_rot.shape[2]
-        per_pos = 4 * (D // 16 + D // 32 + 1) + 4 * (D // 16 + 1)
-        return int(sum(max(int(l), 0) for l in self.kv_len)) * self.n_kv_heads * per_pos
+        """Packed cache bytes the rows must read once per KV head (rows sharing a sequence
+        need each position once)."""
+        tot = 0
+        for s in set(self.seq_of.tolist()):
+            tot += max([self.visited(t) for t in range(self.n_tok) if self.seq_of[t] == s] + [0])
+        return tot * self.n_kv_heads * self.pos_bytes()
+
+    def algorithmic_bytes(self) -> int:
+        """Packed cache + q_rot + q_jl + out (fp32) + signs."""
+        return self.kv_bytes() + 3 * self.q_rot.size * 4 + self.head_dim * 4
+
+    def flops(self) -> int:
+        """6*D flops per (query head, visited position): q_rot.c, q_jl.s and p.v, 2*D each."""
+        return sum(self.visited(t) for t in range(self.n_tok)) * self.n_heads * 6 * self.head_dim
 
 
 def _half_bits(x) -> np.ndarray:
@@ -248,8 +292,8 @@ def make_tq_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=N
     """Random TurboQuant problem: q_rot, q_jl N(0, 1); uniform random 2-bit indices and sign
     bits; K norms U[0.5, 2], residual norms U[0, 0.5], V norms U[0.5, 2] (f16); centroids the
     2-bit Gaussian Lloyd-Max points over sqrt(D); random +-1 signs; qjl_scale sqrt(pi/2) / D
-    (the factor flash_attention_tq.metal's header gives).  Norm words past a sequence's length
-    hold f16 NaN."""
+    (the factor flash_attention_tq.metal's header gives).  Past a sequence's length the packed
+    words are zero and the norm words hold f16 NaN.  Each sequence draws from its own stream."""
     D = head_dim
     if D % 32:
         raise ValueError("head_dim must be a multiple of 32")
@@ -262,22 +306,40 @@ def make_tq_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=N
     q_rot = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
     q_jl = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
     shp = (n_seq, cap, n_kv_heads)
-    k_polar = g.integers(0, 2 ** 32, size=shp + (D // 16,), dtype=np.uint64).astype(np.uint32)
-    k_jl = g.integers(0, 2 ** 32, size=shp + (D // 32,), dtype=np.uint64).astype(np.uint32)
-    v_polar = g.integers(0, 2 ** 32, size=shp + (D // 16,), dtype=np.uint64).astype(np.uint32)
-    k_norms = _half_bits(g.uniform(0.5, 2.0, shp)) | (_half_bits(g.uniform(0.0, 0.5, shp)) << 16)
-    v_norms = _half_bits(g.uniform(0.5, 2.0, shp))
-    nan = _half_bits(np.float16(np.nan))
-    for s in range(n_seq):
-        L = max([int(kv_len[t]) for t in range(n_tok) if seq_of[t] == s] + [0])
+    k_polar = np.zeros(shp + (D // 16,), np.uint32)
+    k_jl = np.zeros(shp + (D // 32,), np.uint32)
+    v_polar = np.zeros(shp + (D // 16,), np.uint32)
+    k_norms = np.empty(shp, np.uint32)
+    v_norms = np.empty(shp, np.uint32)
+    seq_len = [max([int(kv_len[t]) for t in range(n_tok) if seq_of[t] == s] + [0])
+               for s in range(n_seq)]
+    streams = np.random.SeedSequence(seed).spawn(2 + n_seq)[2:]
+    nan = int(_half_bits(np.float16(np.nan)))
+
+    def halves(gs, n, lo, hi):  # f16 bit patterns of U[lo, hi) draws
+        x = gs.random((n, n_kv_heads), dtype=np.float32) * np.float32(hi - lo) + np.float32(lo)
+        return x.astype(np.float16).view(np.uint16).astype(np.uint32)
+
+    def one(s):  # sequence s: random words and norms below its length, NaN norms past it
+        L = seq_len[s]
         k_norms[s, L:] = nan | (nan << 16)
         v_norms[s, L:] = nan
+        if L == 0:
+            return
+        gs = _gen(streams[s])
+        for arr in (k_polar, k_jl, v_polar):
+            arr[s, :L] = gs.integers(0, 0xFFFFFFFF, size=arr[s, :L].shape, dtype=np.uint32,
+                                     endpoint=True)
+        k_norms[s, :L] = halves(gs, L, 0.5, 2.0) | (halves(gs, L, 0.0, 0.5) << 16)
+        v_norms[s, :L] = halves(gs, L, 0.5, 2.0)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(n_seq)))
     signs = np.where(g.integers(0, 2, D) == 1, 1.0, -1.0).astype(np.float32)
     cents = (np.array(LLOYD_MAX_2BIT) / math.sqrt(D)).astype(np.float32)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    return TqCase(name, q_rot, q_jl, k_polar, k_jl, k_norms.astype(np.uint32), v_polar,
-                  v_norms.astype(np.uint32), cents, signs, float(math.sqrt(math.pi / 2) / D),
-                  scale, kv_len, seq_of, seed)
+    return TqCase(name, q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, cents, signs,
+                  float(math.sqrt(math.pi / 2) / D), scale, kv_len, seq_of, seed)
 
 
 def make_block_scores(seed, n_tok, stride, levels=None) -> np.ndarray:
@@ -351,6 +413,22 @@ def prefill_chunk(start_pos=8176, n_rows=16) -> Case:
                          name=f"prefill_chunk_r{n_rows}_pos{start_pos}_h32_hk8_d128")
 
 
+def tq_long_context() -> TqCase:
+    """The long-context shape over a TurboQuant-compressed cache: 16 sequences, lengths uniform
+    in [1024, 32768], 32 heads / 8 KV heads, D=128, cap 32768."""
+    return make_tq_case(1009, 16, 32, 8, 128, long_context_lengths(), cache_cap=32768,
+                        name="tq_long_ctx_b16_h32_hk8_d128_cap32768")
+
+
+def tq_prefill_chunk(start_pos=8176, n_rows=16) -> TqCase:
+    """Chunked prefill over a TurboQuant cache: 16 causal rows of one sequence (row r sees
+    start_pos + r + 1 positions), 32 heads / 8 KV heads, D=128."""
+    L = [start_pos + r + 1 for r in range(n_rows)]
+    return make_tq_case(1010, n_rows, 32, 8, 128, L, cache_cap=start_pos + n_rows,
+                        seq_of=[0] * n_rows, n_seq=1,
+                        name=f"tq_prefill_chunk_r{n_rows}_pos{start_pos}_h32_hk8_d128")
+
+
 NAMED = {
     "tiny": tiny,
     "gqa_d64_L1024": lambda: gqa_d64(1024),
@@ -361,4 +439,6 @@ NAMED = {
     "q8_topk_sel": q8_topk_selected,
     "batched": batched,
     "prefill_chunk": prefill_chunk,
+    "tq_long_ctx": tq_long_context,
+    "tq_prefill_chunk": tq_prefill_chunk,
 }

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 6
+#define GQA_ABI_VERSION 7
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -70,6 +70,7 @@ typedef enum gqa_status {
 /* Kinds for the planner and the workspace query. */
 #define GQA_KIND_F16 0
 #define GQA_KIND_Q8 1
+#define GQA_KIND_TQ 2 /* TurboQuant-compressed caches (attn_decode_tq) */
 
 /* The split plan the decode calls use (exposed so hosts and tests can inspect it). */
 typedef struct gqa_plan {
@@ -184,6 +185,35 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
 gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
                             const int32_t* kv_len, int n_tok, int max_kv_len, int budget,
                             int32_t* ids, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * attn_decode_tq -- decode attention over a TurboQuant-compressed cache
+ * (flash_attention_tq.metal, cera 0.4.0).  Keys are scored without reconstruction:
+ *   x_j = (norm_j * sum_d q_rot[d] c[kidx_j(d)]
+ *          + norm_j * rn_j * qjl_scale * sum_d q_jl[d] s_j(d)) * scale
+ * (c = the four centroids, kidx = 2-bit indices, s = +-1 from the QJL sign bits); values are
+ * accumulated in the rotated basis, vnorm_j c[vidx_j(d)], and the merged row is rotated back:
+ * out = signs * H(acc) / sqrt(D), H the Walsh-Hadamard transform in Sylvester order.  The
+ * page's precomputed per-head sum of q_jl is formed in the kernel.
+ *   q_rot, q_jl   device fp32 [n_tok][n_heads][head_dim]: the query rotated and JL-projected
+ *   k_polar, v_polar  device uint32 [n_seq][cache_cap][n_kv_heads][head_dim/16], 16-byte
+ *                 aligned; 16 two-bit indices per word, index k in bits 2k..2k+1
+ *   k_jl          device uint32 [n_seq][cache_cap][n_kv_heads][head_dim/32], 16-byte aligned;
+ *                 sign bit of dim 32w + k in bit k of word w
+ *   k_norms       device uint32 [n_seq][cache_cap][n_kv_heads]: f16 norm in the low half,
+ *                 f16 residual norm in the high half; v_norms likewise, f16 norm low
+ *   centroids     HOST fp32 [4]; signs device fp32 [head_dim] (the rotation's sign flips)
+ *   head_dim 64 or 128 (the page's limit is 128), group size <= 8 (else GQA_EUNSUPPORTED).
+ *   Other arguments as attn_decode_f16; the workspace is attn_decode_workspace_bytes(...,
+ *   GQA_KIND_TQ), zeroed once like attn_decode_f16's.
+ */
+gqa_status attn_decode_tq(const float* q_rot, const float* q_jl, const uint32_t* k_polar,
+                          const uint32_t* k_jl, const uint32_t* k_norms, const uint32_t* v_polar,
+                          const uint32_t* v_norms, const float* centroids, const float* signs,
+                          float qjl_scale, float scale, float* out, const int32_t* kv_len,
+                          const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                          int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                          void* ws, size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
 
 /*
  * kv_append_q8 -- quantise new K/V rows into the int8 cache (FORWARD_MSL, kv_append_q8, with

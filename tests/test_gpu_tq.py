@@ -1,0 +1,124 @@
+"""GPU parity of attn_decode_tq (decode over a TurboQuant-compressed cache) against the fp64
+oracle's decode_tq on the same seeded inputs: one CTA per row, split rows merged by the last
+CTA, empty and ragged rows, rows sharing a sequence, every supported group size and head_dim,
+workspace reuse, and out-of-range lengths flagged.
+
+Tolerance: both sides decode the same packed words, f16 norms and fp32 centroids exactly; they
+differ only by fp32 rounding of the dot products, the exp2 approximation and the order of the
+sums.  |gpu - ref| <= 1e-4 * max(1, |ref|), the bound the int8 path uses."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import dev, forced_chunk
+from gqa_decode_attention_03_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_TQ = 1e-4
+
+
+def _i32(a):
+    return dev(np.ascontiguousarray(a).view(np.int32))
+
+
+def run_tq(c, max_kv_len=None, ws=None, err=None, out=None, seq_of="case"):
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+    so = dev(c.seq_of) if isinstance(seq_of, str) else seq_of
+    return gd.attn_decode_tq(dev(c.q_rot), dev(c.q_jl), _i32(c.k_polar), _i32(c.k_jl),
+                             _i32(c.k_norms), _i32(c.v_polar), _i32(c.v_norms), c.centroids,
+                             dev(c.signs), c.qjl_scale, dev(c.kv_len), scale=c.scale, seq_of=so,
+                             max_kv_len=max_kv_len, ws=ws, err=err, out=out)
+
+
+def ref_tq(c, kv_len=None, rows=None):
+    return oracle.decode_tq(c.q_rot, c.q_jl, c.k_polar, c.k_jl, c.k_norms, c.v_polar, c.v_norms,
+                            c.centroids, c.signs, c.qjl_scale, c.scale,
+                            c.kv_len if kv_len is None else kv_len, c.seq_of, rows=rows)
+
+
+def check(got, ref, tol=TOL_TQ):
+    got = got.detach().cpu().numpy().astype(np.float64) if isinstance(got, torch.Tensor) else got
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    assert err.max() <= tol, f"max scaled error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (16, 4), (32, 4)])
+def test_tq_group_sizes(D, H, Hk):
+    c = W.make_tq_case(2100 + D + H, 2, H, Hk, D, [300, 77])
+    check(run_tq(c), ref_tq(c))
+
+
+@pytest.mark.parametrize("chunk", [None, 128, 256, 384])
+def test_tq_split_ragged_rows(chunk):
+    # lengths straddling chunk and pass edges, an empty row, a one-position row; NaN norms past
+    # every length
+    L = [1000, 1, 0, 129, 511, 640]
+    c = W.make_tq_case(2201, len(L), 16, 2, 128, L, cache_cap=1024)
+    with forced_chunk(chunk):
+        got = run_tq(c)
+    ref = ref_tq(c)
+    check(got, ref)
+    assert torch.count_nonzero(got[2]) == 0
+
+
+@pytest.mark.parametrize("chunk", [None, 128])
+def test_tq_shared_sequence_causal_rows(chunk):
+    # chunked-prefill rows over one sequence: row r sees start + r + 1 positions
+    L = [600 + r + 1 for r in range(6)]
+    c = W.make_tq_case(2202, 6, 8, 2, 64, L, seq_of=[0] * 6, n_seq=1)
+    with forced_chunk(chunk):
+        check(run_tq(c), ref_tq(c))
+
+
+def test_tq_named_prefill_chunk():
+    c = W.tq_prefill_chunk()
+    check(run_tq(c), ref_tq(c))
+
+
+def test_tq_long_context_sampled_rows():
+    # the full-size workload in the launch configuration the benchmark times; the oracle
+    # recomputes three rows (the shortest, the longest, one between)
+    c = W.tq_long_context()
+    got = run_tq(c).cpu().numpy()
+    order = np.argsort(c.kv_len)
+    rows = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    check(got[rows], ref_tq(c, rows=rows))
+
+
+def test_tq_workspace_reuse_and_two_calls():
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+    c = W.make_tq_case(2203, 3, 32, 8, 128, [3000, 2000, 10], cache_cap=3000)
+    ws = gd.alloc_workspace(3, 32, 8, 128, 3000, -1, gd.KIND_TQ, "cuda", 3)
+    with forced_chunk(256):
+        a = run_tq(c, ws=ws).clone()
+        b = run_tq(c, ws=ws)
+    assert torch.equal(a, b)
+    check(a, ref_tq(c))
+    cnt = -(-3 * 8 * 4 // 256) * 256
+    assert torch.count_nonzero(ws[:cnt]) == 0   # arrival counters back at zero
+
+
+def test_tq_length_out_of_range_is_flagged():
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+    c = W.make_tq_case(2204, 2, 8, 2, 64, [200, 50], cache_cap=200)
+    bad = c.kv_len.copy()
+    bad[1] = 250   # beyond the cache: clamped to 200, bit flagged
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gd.attn_decode_tq(dev(c.q_rot), dev(c.q_jl), _i32(c.k_polar), _i32(c.k_jl),
+                            _i32(c.k_norms), _i32(c.v_polar), _i32(c.v_norms), c.centroids,
+                            dev(c.signs), c.qjl_scale, dev(bad), scale=c.scale,
+                            seq_of=dev(c.seq_of), err=err)
+    assert int(err.item()) & gd.ERR_KVLEN_RANGE
+    check(got[0:1], ref_tq(c, rows=[0]))
+
+
+def test_tq_rejects_large_group():
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+    c = W.make_tq_case(2205, 1, 16, 1, 64, [64])
+    with pytest.raises(gd.GqaError, match="GQA_EUNSUPPORTED"):
+        run_tq(c)

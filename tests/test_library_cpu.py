@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(gd):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in the header but not exported"
     assert set(declared_functions()) <= set(gd.EXPORTS) | set(declared_functions())
-    assert gd.LIB.gqa_abi_version() == 6
+    assert gd.LIB.gqa_abi_version() == 7
 
 
 def test_status_strings(gd):
@@ -152,3 +152,29 @@ def test_decode_rejects_bad_arguments_before_any_launch(gd):
     assert st == gd.GQA_OK
     # merge: bad head_dim
     assert L.attn_merge(good, good, 2, 1, 4, 100, good, None) == gd.GQA_EINVAL
+
+
+def test_plan_turboquant(gd):
+    # TurboQuant cache, D=128: 88 bytes per (position, KV head); 8 KV heads over 32768
+    # positions split into chunks of whole 128-position passes, merged by the last CTA
+    p = gd.plan(1, 32, 8, 128, 32768, -1, gd.KIND_TQ, num_sms=152)
+    assert p.tile == 128 and p.streamk == 0 and p.row_group == 1
+    assert p.grid_y == 8 and p.grid_z == 1 and p.chunk % 128 == 0
+    assert p.n_split == -(-32768 // p.chunk) and p.merge == 1
+    # a row of at most 128 KB (1489 positions of 88 bytes) is not split
+    q = gd.plan(1, 32, 8, 128, 1489, -1, gd.KIND_TQ, num_sms=152)
+    assert q.n_split == 1 and q.merge == 0 and q.ws_bytes == 0
+
+
+def test_turboquant_argument_checks(gd):
+    # rejected on the host before any device call
+    cents = (ctypes.c_float * 4)(0.0, 0.0, 0.0, 0.0)
+    def call(head_dim=128, n_heads=32, n_kv_heads=8, ptr=16):
+        P = ctypes.c_void_p(ptr)
+        return gd.LIB.attn_decode_tq(P, P, P, P, P, P, P, cents, P, 1.0, 1.0, P, P, None, 1, 1,
+                                     n_heads, n_kv_heads, head_dim, 64, 64, None, 0, None, None)
+    assert call(head_dim=256) == gd.GQA_EINVAL
+    assert call(n_heads=30) == gd.GQA_EINVAL
+    assert call(n_heads=80, n_kv_heads=8) == gd.GQA_EUNSUPPORTED   # group of 10
+    assert call(ptr=0) == gd.GQA_EINVAL
+    assert call(ptr=8) == gd.GQA_EINVAL                           # caches 16-byte aligned
