@@ -122,25 +122,30 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def _source_hash():
+def _source_hash(sources=None):
+    """Hash of the kernel sources a capture was taken on: the named files under csrc/ (all of
+    them when none are named) and the public header."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "gqa_decode_attention_03_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = sorted(sources) if sources else sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "gqa_decode.h"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def _ncu_traffic(workload):
-    """DRAM bytes per launch of the partial kernel from the committed ncu summary, when it was
-    taken on the current kernel sources; otherwise None."""
+    """DRAM bytes per launch of the step's kernel from the committed ncu summary, when it was
+    taken on the current sources of that kernel; otherwise None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         ent = d.get(workload)
-        if ent and ent.get("source_hash") == _source_hash():
+        if ent and ent.get("source_hash") == _source_hash(ent.get("sources")):
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -185,7 +190,8 @@ def _merge_launch(plan):
 
 def _kernel_name(case, plan):
     if case.kind == "tq":
-        return "tq_decode_kernel" + (" (split-KV, merge fused)" if plan.merge else "")
+        name = "tq_decode_kernel" if os.environ.get("GQA_TQ_KERNEL") == "fma" else "tq_mma_kernel"
+        return name + (" (split-KV, merge fused)" if plan.merge else "")
     if plan.streamk:
         return "streamk_mma_kernel (stream-K split, merge fused)"
     if plan.row_group > 1:
@@ -369,7 +375,7 @@ def _oracle_pair(case, t, g):
     s = int(case.seq_of[t])
     L = case.kv_len[t:t + 1]
     if case.kind == "tq":
-        sl = (slice(s, s + 1), slice(None), slice(g, g + 1))
+        sl = (slice(s, s + 1), slice(g, g + 1))
         return oracle.decode_tq(case.q_rot[t:t + 1, g * G:(g + 1) * G],
                                 case.q_jl[t:t + 1, g * G:(g + 1) * G], case.k_polar[sl],
                                 case.k_jl[sl], case.k_norms[sl], case.v_polar[sl],

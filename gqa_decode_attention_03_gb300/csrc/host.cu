@@ -88,6 +88,12 @@ constexpr long long kMaxChunk = 8192;
 // Rows whose whole visited list is at most this many bytes of K/V (and scales) are not split:
 // one CTA streams them in a few microseconds, less than a split's merge step costs.
 constexpr long long kMinSplitBytes = 128 << 10;
+// TurboQuant caches: 88 bytes per position and KV head at D = 128 against ~8 KB of decode and
+// tensor work, so the split is sized by compute: more, shorter chunks (8 CTAs per SM, at most
+// 2048 positions) and a split from 32 KB of packed row up.
+constexpr int kTqCtasPerSm = 8;
+constexpr long long kTqMaxChunk = 2048;
+constexpr long long kTqMinSplitBytes = 32 << 10;
 
 // Shapes that do not depend on the device.
 gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
@@ -227,9 +233,10 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
       rgroup > 1 ? std::max<long long>((n_tok + rgroup - 1) / rgroup, std::min(n_seq, n_tok)) : n_tok;
   plan->row_group = rgroup;
   const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
-  const long long slots = (long long)kCtasPerSm * num_sms;
+  const bool tq = kind == GQA_KIND_TQ;
+  const long long slots = (long long)(tq ? kTqCtasPerSm : kCtasPerSm) * num_sms;
   long long chunk = (units + slots - 1) / slots;
-  chunk = std::min(chunk, kMaxChunk);
+  chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
   // a split chunk spans at least two stages, so its pipeline has something to overlap
   // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
   // D=64 4096 positions 14.7 against 16.1)
@@ -238,7 +245,7 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
       kind == GQA_KIND_F16   ? 4LL * head_dim
       : kind == GQA_KIND_Q8 ? 2LL * (head_dim + head_dim / 32)
                              : 4LL * (head_dim / 16 + head_dim / 32 + 1) + 4LL * (head_dim / 16 + 1);
-  if (nmax * row_bytes <= kMinSplitBytes) chunk = std::max(nmax, 1LL);
+  if (nmax * row_bytes <= (tq ? kTqMinSplitBytes : kMinSplitBytes)) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");
   if (forced > 0) chunk = forced;
   chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;

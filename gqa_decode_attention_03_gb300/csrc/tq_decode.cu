@@ -1,94 +1,28 @@
-// tq_decode.cu -- decode attention over a TurboQuant-compressed KV cache.
+// tq_decode.cu -- TurboQuant decode on the CUDA cores, and the attn_decode_tq entry point.
 //
-// flash_attention_tq.metal (cera 0.4.0 sources).  Keys are never reconstructed: a key's score
-// is a PolarQuant term, its 2-bit centroid indices dotted with the rotated query, plus a QJL
-// correction from its sign bits and residual norm:
-//   x_j = (norm_j sum_d q_rot[d] c[kidx_j(d)] + norm_j rn_j qjl_scale sum_d q_jl[d] s_j(d)) scale
-// and values are accumulated in the rotated basis, vnorm_j c[vidx_j(d)], so the inverse
-// rotation -- 1/sqrt(D), a Walsh-Hadamard transform, the sign flip -- runs once on the merged
-// row.  The page's per-head sum of q_jl turns the sum over set sign bits into the signed sum.
-//
-// GB300 layout of the work: one CTA per (KV chunk, KV head, query row), like the other decode
-// kernels, with every query head of the KV head's group served from the same decoded key: q.k
-// gives each lane one cache position (its 2-bit fields and sign bits decoded once, dotted with
-// every head's rotated query, broadcast from shared memory), p.v gives each lane D/32 dims of
-// the rotated accumulator.  Rows longer than a chunk write rotated partials and the last CTA
-// of the (row, KV head) merges them (merge_if_last) and applies the inverse rotation.
-// Packed format as on the page (16 two-bit indices per uint32, index k in bits 2k..2k+1; 32
-// sign bits per uint32; f16 norm pairs), stored position-major like the other caches.
+// flash_attention_tq.metal (cera 0.4.0 sources); the score and accumulator definitions are in
+// tq_common.cuh.  This kernel gives each lane one cache position for q.k (its 2-bit fields and
+// sign bits decoded once, dotted with every head's rotated query, broadcast from shared memory)
+// and D/32 dims of the rotated accumulator for p.v.  It is the plain form of the path, kept
+// beside the tensor-core kernel (tq_mma.cu, the default) as a cross-check: GQA_TQ_KERNEL=fma
+// selects it.
 #include <cuda_fp16.h>
 #include <cuda_runtime_api.h>
 
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "dispatch.h"
+#include "tq_common.cuh"
 
 namespace gqa {
 
 void set_last_error(const char* msg);
 
-constexpr int kTqWarps = 4;
-constexpr int kTqMaxGroup = 8;
-
-struct TqParams {
-  PartialParams base;          // q unused; out, part, counters, n_valid, lengths, sizes
-  const float* q_rot;          // [T][H][D]
-  const float* q_jl;           // [T][H][D]
-  const uint32_t* k_polar;     // [n_seq][cap][Hk][D/16]
-  const uint32_t* k_jl;        // [n_seq][cap][Hk][D/32]
-  const uint32_t* k_norms;     // [n_seq][cap][Hk]
-  const uint32_t* v_polar;     // [n_seq][cap][Hk][D/16]
-  const uint32_t* v_norms;     // [n_seq][cap][Hk]
-  const float* signs;          // [D]
-  float c0, c1, c2, c3;        // centroids
-  float qjl_scale;
-};
-
 __device__ __forceinline__ float tq_centroid(uint32_t idx, float c0, float c1, float c2, float c3) {
   return (idx & 2u) ? ((idx & 1u) ? c3 : c2) : ((idx & 1u) ? c1 : c0);
 }
-
-__device__ __forceinline__ float half_lo(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
-}
-__device__ __forceinline__ float half_hi(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
-}
-
-// Inverse rotation of a merged rotated row held D/32 consecutive dims per lane: scale by
-// 1/sqrt(D), the Walsh-Hadamard butterflies (within the lane for strides below D/32, across
-// lanes by shuffle above), then the sign flip.
-template <int D>
-struct TqRotateBack {
-  const float* signs;
-  __device__ __forceinline__ void operator()(float (&a)[D / 32], int /*head*/, int lane) const {
-    constexpr int DPL = D / 32;
-    const float s = rsqrtf(static_cast<float>(D));
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a[k] *= s;
-#pragma unroll
-    for (int stride = 1; stride < DPL; stride <<= 1)
-#pragma unroll
-      for (int k = 0; k < DPL; ++k)
-        if ((k & stride) == 0) {
-          const float x = a[k], y = a[k + stride];
-          a[k] = x + y;
-          a[k + stride] = x - y;
-        }
-#pragma unroll
-    for (int stride = DPL; stride < D; stride <<= 1) {
-      const int lmask = stride / DPL;
-      const bool high = (lane & lmask) != 0;
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) {
-        const float other = __shfl_xor_sync(0xffffffffu, a[k], lmask);
-        a[k] = high ? other - a[k] : a[k] + other;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a[k] *= __ldg(signs + lane * DPL + k);
-  }
-};
 
 template <int D>
 __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams tp) {
@@ -98,34 +32,13 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
   __shared__ __align__(16) float qj[kTqMaxGroup][D];
   __shared__ float qjsum[kTqMaxGroup];
   __shared__ uint32_t vbuf[kTqWarps][32][PW];
-  __shared__ float mg[kTqWarps][kTqMaxGroup][D + 2];
+  __shared__ float mg[kTqWarps * kTqMaxGroup * (D + 2)];
   const int c = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
   const int G = p.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int L = __ldg(p.kv_len + t);
-  int errbits = 0;
-  const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
-  if (L < 0 || L > lmax) {
-    errbits |= GQA_ERR_KVLEN_RANGE;
-    L = L < 0 ? 0 : lmax;
-  }
-  const int s = p.seq_of ? __ldg(p.seq_of + t) : t;
-  if (s < 0 || s >= p.n_seq) {
-    errbits |= GQA_ERR_SEQ_RANGE;
-    L = 0;
-  }
-  const int c0 = c * p.chunk, c1 = min(c0 + p.chunk, L);
-  if (c == 0 && g == 0 && threadIdx.x == 0) {
-    if (errbits) flag_error(p.err, errbits);
-    if (p.merge) p.n_valid[t] = (L + p.chunk - 1) / p.chunk;
-  }
-  if (c0 >= L) {
-    if (c == 0)  // empty context: zeros (flash_attention_tq.metal, seq_len == 0)
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
-    return;
-  }
+  int L, s, c0, c1;
+  if (!tq_row_setup(p, t, c, g, G, D, L, s, c0, c1)) return;
 
   // the group's rotated and JL queries, and the per-head sum of q_jl
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
@@ -156,7 +69,7 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
     const int pos = base + lane;
     const bool valid = pos < c1;
     const int nvb = min(32, c1 - base);  // valid positions of the block, a prefix
-    const size_t row = ((size_t)s * p.cache_cap + (valid ? pos : c0)) * p.n_kv_heads + g;
+    const size_t row = ((size_t)s * p.n_kv_heads + g) * p.cache_cap + (valid ? pos : c0);
     float x[kTqMaxGroup];
     float vn = 0.f;
     {
@@ -253,56 +166,28 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
     __syncwarp();
   }
 
-  // ---- merge the warps' states, then write the output or the chunk's partial
+  // ---- the warps' states to shared memory; tq_finish combines them
 #pragma unroll
   for (int h = 0; h < kTqMaxGroup; ++h) {
     if (h >= G) break;
+    float* r = mg + (warp * kTqMaxGroup + h) * (D + 2);
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) mg[warp][h][lane * DPL + k] = acc[h][k];
+    for (int k = 0; k < DPL; ++k) r[lane * DPL + k] = acc[h][k];
     if (lane == 0) {
-      mg[warp][h][D] = m_run[h];
-      mg[warp][h][D + 1] = l_run[h];
+      r[D] = m_run[h];
+      r[D + 1] = l_run[h];
     }
   }
   __syncthreads();
-  const TqRotateBack<D> rot{tp.signs};
-  for (int h = warp; h < G; h += kTqWarps) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kTqWarps; ++w) M = fmaxf(M, mg[w][h][D]);
-    float a[DPL], Ls = 0.f;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a[k] = 0.f;
-#pragma unroll
-    for (int w = 0; w < kTqWarps; ++w) {
-      const float e = mg[w][h][D] == -INFINITY ? 0.f : fast_exp2(mg[w][h][D] - M);
-      Ls = fmaf(mg[w][h][D + 1], e, Ls);
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) a[k] = fmaf(mg[w][h][lane * DPL + k], e, a[k]);
-    }
-    const int head = g * G + h;
-    if (p.merge) {
-      float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) pr[lane * DPL + k] = a[k];
-      if (lane == 0) {
-        pr[D] = M == -INFINITY ? -INFINITY : M * kLn2;
-        pr[D + 1] = Ls;
-      }
-    } else {
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) a[k] *= inv;
-      rot(a, head, lane);
-      float* o = p.out + ((size_t)t * p.n_heads + head) * D + lane * DPL;
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) o[k] = a[k];
-    }
-  }
-  if (p.merge) {
-    merge_if_last<D>(p, t, g * G, G, (size_t)t * p.n_kv_heads + g, (L + p.chunk - 1) / p.chunk,
-                     kTqWarps, rot);
-  }
+  tq_finish<D>(tp, mg, t, g, c, L, G);
+}
+
+cudaError_t launch_tq_fma(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream) {
+  if (head_dim == 64)
+    tq_decode_kernel<64><<<grid, 32 * kTqWarps, 0, stream>>>(tp);
+  else
+    tq_decode_kernel<128><<<grid, 32 * kTqWarps, 0, stream>>>(tp);
+  return cudaGetLastError();
 }
 
 }  // namespace gqa
@@ -337,7 +222,7 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
       !signs || !out || !kv_len)
     return tq_fail(GQA_EINVAL, "attn_decode_tq: a required pointer is NULL");
   if (!tq_aligned16(k_polar) || !tq_aligned16(v_polar) || !tq_aligned16(k_jl) ||
-      (reinterpret_cast<uintptr_t>(out) & 7))
+      !tq_aligned16(k_norms) || !tq_aligned16(v_norms) || (reinterpret_cast<uintptr_t>(out) & 7))
     return tq_fail(GQA_EINVAL, "attn_decode_tq: packed caches 16-byte, out 8-byte aligned");
   if (n_seq <= 0 || cache_cap <= 0 || max_kv_len < 0)
     return tq_fail(GQA_EINVAL, "attn_decode_tq: n_seq, cache_cap > 0, max_kv_len >= 0");
@@ -393,10 +278,12 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
   tp.c3 = centroids[3];
   tp.qjl_scale = qjl_scale;
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-  if (head_dim == 64)
-    gqa::tq_decode_kernel<64><<<grid, 32 * gqa::kTqWarps, 0, stream>>>(tp);
+  const char* kern = std::getenv("GQA_TQ_KERNEL");  // "fma": the CUDA-core kernel
+  const int G = n_heads / n_kv_heads;
+  if (kern && std::strcmp(kern, "fma") == 0)
+    (void)gqa::launch_tq_fma(head_dim, grid, tp, stream);
   else
-    gqa::tq_decode_kernel<128><<<grid, 32 * gqa::kTqWarps, 0, stream>>>(tp);
+    (void)gqa::launch_tq_mma(head_dim, G <= 4 ? 1 : 2, grid, tp, stream);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
   return GQA_OK;

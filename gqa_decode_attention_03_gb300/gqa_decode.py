@@ -194,8 +194,8 @@ def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centro
     """Decode attention over a TurboQuant-compressed cache; returns ``out [T][H][D]`` fp32.
 
     q_rot, q_jl [T][H][D] fp32 (the rotated and JL-projected query); packed words as int32 bit
-    patterns: k_polar, v_polar [n_seq][cap][Hk][D/16], k_jl [n_seq][cap][Hk][D/32], k_norms,
-    v_norms [n_seq][cap][Hk]; centroids: 4 host floats; signs [D] fp32 on the device.
+    patterns, head-major: k_polar, v_polar [n_seq][Hk][cap][D/16], k_jl [n_seq][Hk][cap][D/32],
+    k_norms, v_norms [n_seq][Hk][cap]; centroids: 4 host floats; signs [D] fp32 on the device.
     """
     _need(q_rot, torch.float32, "q_rot", 3)
     _need(q_jl, torch.float32, "q_jl", 3)
@@ -209,10 +209,10 @@ def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centro
     if seq_of is not None:
         _need(seq_of, torch.int32, "seq_of", 1)
     T, H, D = q_rot.shape
-    n_seq, cap, Hk, _ = k_polar.shape
+    n_seq, Hk, cap, _ = k_polar.shape
     if (q_jl.shape != q_rot.shape or v_polar.shape != k_polar.shape or k_polar.shape[3] != D // 16
-            or k_jl.shape != (n_seq, cap, Hk, D // 32) or k_norms.shape != (n_seq, cap, Hk)
-            or v_norms.shape != (n_seq, cap, Hk) or signs.numel() != D or kv_len.numel() != T):
+            or k_jl.shape != (n_seq, Hk, cap, D // 32) or k_norms.shape != (n_seq, Hk, cap)
+            or v_norms.shape != (n_seq, Hk, cap) or signs.numel() != D or kv_len.numel() != T):
         raise ValueError("shape mismatch between the queries, the packed caches and kv_len")
     cents = (ctypes.c_float * 4)(*[float(x) for x in centroids])
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)

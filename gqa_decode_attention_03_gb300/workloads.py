@@ -216,11 +216,11 @@ class TqCase:
     name: str
     q_rot: np.ndarray      # [T][H][D] fp32
     q_jl: np.ndarray       # [T][H][D] fp32
-    k_polar: np.ndarray    # [n_seq][cap][Hk][D/16] uint32
-    k_jl: np.ndarray       # [n_seq][cap][Hk][D/32] uint32
-    k_norms: np.ndarray    # [n_seq][cap][Hk] uint32: f16 norm | f16 residual norm << 16
-    v_polar: np.ndarray    # [n_seq][cap][Hk][D/16] uint32
-    v_norms: np.ndarray    # [n_seq][cap][Hk] uint32: f16 norm
+    k_polar: np.ndarray    # [n_seq][Hk][cap][D/16] uint32 (head-major, as on the page)
+    k_jl: np.ndarray       # [n_seq][Hk][cap][D/32] uint32
+    k_norms: np.ndarray    # [n_seq][Hk][cap] uint32: f16 norm | f16 residual norm << 16
+    v_polar: np.ndarray    # [n_seq][Hk][cap][D/16] uint32
+    v_norms: np.ndarray    # [n_seq][Hk][cap] uint32: f16 norm
     centroids: np.ndarray  # [4] fp32
     signs: np.ndarray      # [D] fp32, +-1
     qjl_scale: float
@@ -235,7 +235,7 @@ class TqCase:
 
     @property
     def n_kv_heads(self):
-        return self.k_polar.shape[2]
+        return self.k_polar.shape[1]
 
     @property
     def n_tok(self):
@@ -255,7 +255,7 @@ class TqCase:
 
     @property
     def cache_cap(self):
-        return self.k_polar.shape[1]
+        return self.k_polar.shape[2]
 
     def visited(self, t: int) -> int:
         return max(int(self.kv_len[t]), 0)
@@ -305,7 +305,7 @@ def make_tq_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=N
     g = _gen(np.random.SeedSequence(seed).spawn(1)[0])
     q_rot = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
     q_jl = g.standard_normal((n_tok, n_heads, D), dtype=np.float32)
-    shp = (n_seq, cap, n_kv_heads)
+    shp = (n_seq, n_kv_heads, cap)
     k_polar = np.zeros(shp + (D // 16,), np.uint32)
     k_jl = np.zeros(shp + (D // 32,), np.uint32)
     v_polar = np.zeros(shp + (D // 16,), np.uint32)
@@ -317,21 +317,21 @@ def make_tq_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=N
     nan = int(_half_bits(np.float16(np.nan)))
 
     def halves(gs, n, lo, hi):  # f16 bit patterns of U[lo, hi) draws
-        x = gs.random((n, n_kv_heads), dtype=np.float32) * np.float32(hi - lo) + np.float32(lo)
+        x = gs.random((n_kv_heads, n), dtype=np.float32) * np.float32(hi - lo) + np.float32(lo)
         return x.astype(np.float16).view(np.uint16).astype(np.uint32)
 
     def one(s):  # sequence s: random words and norms below its length, NaN norms past it
         L = seq_len[s]
-        k_norms[s, L:] = nan | (nan << 16)
-        v_norms[s, L:] = nan
+        k_norms[s, :, L:] = nan | (nan << 16)
+        v_norms[s, :, L:] = nan
         if L == 0:
             return
         gs = _gen(streams[s])
         for arr in (k_polar, k_jl, v_polar):
-            arr[s, :L] = gs.integers(0, 0xFFFFFFFF, size=arr[s, :L].shape, dtype=np.uint32,
-                                     endpoint=True)
-        k_norms[s, :L] = halves(gs, L, 0.5, 2.0) | (halves(gs, L, 0.0, 0.5) << 16)
-        v_norms[s, :L] = halves(gs, L, 0.5, 2.0)
+            arr[s, :, :L] = gs.integers(0, 0xFFFFFFFF, size=arr[s, :, :L].shape,
+                                        dtype=np.uint32, endpoint=True)
+        k_norms[s, :, :L] = halves(gs, L, 0.5, 2.0) | (halves(gs, L, 0.0, 0.5) << 16)
+        v_norms[s, :, :L] = halves(gs, L, 0.5, 2.0)
 
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(one, range(n_seq)))

@@ -196,12 +196,15 @@ gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
  * out = signs * H(acc) / sqrt(D), H the Walsh-Hadamard transform in Sylvester order.  The
  * page's precomputed per-head sum of q_jl is formed in the kernel.
  *   q_rot, q_jl   device fp32 [n_tok][n_heads][head_dim]: the query rotated and JL-projected
- *   k_polar, v_polar  device uint32 [n_seq][cache_cap][n_kv_heads][head_dim/16], 16-byte
+ *   Caches are head-major, as the page's compressed regions are: each (sequence, KV head)
+ *   holds its cache_cap positions contiguously.
+ *   k_polar, v_polar  device uint32 [n_seq][n_kv_heads][cache_cap][head_dim/16], 16-byte
  *                 aligned; 16 two-bit indices per word, index k in bits 2k..2k+1
- *   k_jl          device uint32 [n_seq][cache_cap][n_kv_heads][head_dim/32], 16-byte aligned;
+ *   k_jl          device uint32 [n_seq][n_kv_heads][cache_cap][head_dim/32], 16-byte aligned;
  *                 sign bit of dim 32w + k in bit k of word w
- *   k_norms       device uint32 [n_seq][cache_cap][n_kv_heads]: f16 norm in the low half,
- *                 f16 residual norm in the high half; v_norms likewise, f16 norm low
+ *   k_norms       device uint32 [n_seq][n_kv_heads][cache_cap], 16-byte aligned: f16 norm in
+ *                 the low half, f16 residual norm in the high half; v_norms likewise, f16 norm
+ *                 low
  *   centroids     HOST fp32 [4]; signs device fp32 [head_dim] (the rotation's sign flips)
  *   head_dim 64 or 128 (the page's limit is 128), group size <= 8 (else GQA_EUNSUPPORTED).
  *   Other arguments as attn_decode_f16; the workspace is attn_decode_workspace_bytes(...,

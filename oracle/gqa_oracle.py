@@ -336,9 +336,10 @@ def decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, 
               qjl_scale, scale, kv_len, seq_of=None, rows=None) -> np.ndarray:
     """Decode attention over a TurboQuant-compressed cache (flash_attention_tq.metal); float64.
 
-    Layouts (position-major like the other caches): k_polar, v_polar [n_seq][cap][Hk][D/16]
-    uint32; k_jl [n_seq][cap][Hk][D/32] uint32; k_norms [n_seq][cap][Hk] uint32 = (f16 norm,
-    f16 residual norm) in the (low, high) halves; v_norms [n_seq][cap][Hk] uint32, f16 norm in
+    Layouts (head-major, as the page's compressed regions are: each KV head's positions
+    contiguous): k_polar, v_polar [n_seq][Hk][cap][D/16] uint32; k_jl [n_seq][Hk][cap][D/32]
+    uint32; k_norms [n_seq][Hk][cap] uint32 = (f16 norm, f16 residual norm) in the (low, high)
+    halves; v_norms [n_seq][Hk][cap] uint32, f16 norm in
     the low half.  q_rot, q_jl [T][H][D] fp32 (the query already rotated and JL-projected).
     For row t, head h (KV head g = h // G) and visited position j:
 
@@ -354,7 +355,7 @@ def decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, 
     q_rot = np.asarray(q_rot, np.float64)
     q_jl = np.asarray(q_jl, np.float64)
     T, H, D = q_rot.shape
-    Hk = k_polar.shape[2]
+    Hk = k_polar.shape[1]
     G = H // Hk
     c = np.asarray(centroids, np.float64)
     Hd = hadamard(D)
@@ -368,11 +369,11 @@ def decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, 
             continue
         for h in range(H):
             g = _kv_head_of(h, G)
-            kidx = unpack_polar(k_polar[s, :L, g], D)
-            ks = unpack_signs(k_jl[s, :L, g], D)
-            norm, rn = half_pair(k_norms[s, :L, g])
-            vidx = unpack_polar(v_polar[s, :L, g], D)
-            vnorm, _ = half_pair(v_norms[s, :L, g])
+            kidx = unpack_polar(k_polar[s, g, :L], D)
+            ks = unpack_signs(k_jl[s, g, :L], D)
+            norm, rn = half_pair(k_norms[s, g, :L])
+            vidx = unpack_polar(v_polar[s, g, :L], D)
+            vnorm, _ = half_pair(v_norms[s, g, :L])
             polar = c[kidx] @ q_rot[t, h]
             signed = ks @ q_jl[t, h]
             x = (norm * polar + norm * rn * qjl_scale * signed) * scale

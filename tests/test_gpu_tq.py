@@ -1,7 +1,7 @@
 """GPU parity of attn_decode_tq (decode over a TurboQuant-compressed cache) against the fp64
-oracle's decode_tq on the same seeded inputs: one CTA per row, split rows merged by the last
-CTA, empty and ragged rows, rows sharing a sequence, every supported group size and head_dim,
-workspace reuse, and out-of-range lengths flagged.
+oracle's decode_tq on the same seeded inputs, for the tensor-core kernel and the CUDA-core one:
+one CTA per row, split rows merged by the last CTA, empty and ragged rows, rows sharing a
+sequence, group sizes 1 to 8 and both head_dims, workspace reuse, out-of-range lengths flagged.
 
 Tolerance: both sides decode the same packed words, f16 norms and fp32 centroids exactly; they
 differ only by fp32 rounding of the dot products, the exp2 approximation and the order of the
@@ -18,6 +18,16 @@ from gqa_decode_attention_03_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 TOL_TQ = 1e-4
+
+
+@pytest.fixture(params=["mma", "fma"], autouse=True)
+def tq_kernel(request, monkeypatch):
+    """Every test runs on both kernels: tensor cores (the default) and CUDA cores."""
+    if request.param == "fma":
+        monkeypatch.setenv("GQA_TQ_KERNEL", "fma")
+    else:
+        monkeypatch.delenv("GQA_TQ_KERNEL", raising=False)
+    return request.param
 
 
 def _i32(a):
@@ -47,7 +57,7 @@ def check(got, ref, tol=TOL_TQ):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (16, 4), (32, 4)])
+@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (12, 4), (16, 4), (20, 4), (32, 4)])
 def test_tq_group_sizes(D, H, Hk):
     c = W.make_tq_case(2100 + D + H, 2, H, Hk, D, [300, 77])
     check(run_tq(c), ref_tq(c))

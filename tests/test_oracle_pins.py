@@ -319,14 +319,14 @@ def _tq_dense_reference(c):
             g = h // G
             K2, V = [], []
             for j in range(L):
-                kw = int(c.k_norms[s, j, g])
+                kw = int(c.k_norms[s, g, j])
                 norm, rn = f16(kw & 0xFFFF), f16(kw >> 16)
-                vn = f16(int(c.v_norms[s, j, g]) & 0xFFFF)
-                kp = [float(c.centroids[(int(c.k_polar[s, j, g, d // 16]) >> (2 * (d % 16))) & 3])
+                vn = f16(int(c.v_norms[s, g, j]) & 0xFFFF)
+                kp = [float(c.centroids[(int(c.k_polar[s, g, j, d // 16]) >> (2 * (d % 16))) & 3])
                       for d in range(D)]
-                sb = [1.0 if (int(c.k_jl[s, j, g, d // 32]) >> (d % 32)) & 1 else -1.0
+                sb = [1.0 if (int(c.k_jl[s, g, j, d // 32]) >> (d % 32)) & 1 else -1.0
                       for d in range(D)]
-                vp = [float(c.centroids[(int(c.v_polar[s, j, g, d // 16]) >> (2 * (d % 16))) & 3])
+                vp = [float(c.centroids[(int(c.v_polar[s, g, j, d // 16]) >> (2 * (d % 16))) & 3])
                       for d in range(D)]
                 K2.append([norm * x for x in kp] + [norm * rn * c.qjl_scale * x for x in sb])
                 V.append([vn * x for x in vp])
@@ -348,7 +348,7 @@ def test_tq_constant_values_rotate_to_one_spike():
     # every V index the same centroid and equal V norms: acc is constant, so H acc = D acc e_0
     c = W.make_tq_case(32, 1, 2, 1, 64, [12])
     c.v_polar[:] = np.uint32(0xAAAAAAAA)            # index 2 in every field
-    c.v_norms[0, :12] = W._half_bits(1.25)
+    c.v_norms[0, 0, :12] = W._half_bits(1.25)
     got = _tq_oracle(c)
     spike = float(c.signs[0]) * 64 * 1.25 * float(c.centroids[2]) / np.sqrt(64)
     assert np.allclose(got[0, :, 0], spike, rtol=1e-12) and np.allclose(got[0, :, 1:], 0, atol=1e-14)
