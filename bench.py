@@ -393,7 +393,7 @@ def _pair_bytes(case, t):
     if case.kind == "tq":
         return case.visited(t) * case.pos_bytes()
     D = case.head_dim
-    per_pos = 2 * D * 2 if case.kind == "f16" else 2 * (D + 2 * (D // 64))
+    per_pos = 2 * D * 2 if case.kind == "f16" else 2 * (D + 2 * (D // case.scale_group))
     return case.visited(t) * per_pos
 
 

@@ -287,7 +287,7 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
                          float* out, const int32_t* kv_len, const int32_t* seq_of, int n_tok,
                          int n_seq, int n_heads, int n_kv_heads, int head_dim, int64_t cache_cap,
                          int max_kv_len, float scale, void* ws, size_t ws_bytes,
-                         int32_t* err_word, cudaStream_t stream) {
+                         int32_t* err_word, cudaStream_t stream, int scale_group = 64) {
   gqa_status st = check_shape(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, kind);
   if (st != GQA_OK) return st;
   if (n_tok == 0) return GQA_OK;
@@ -295,8 +295,13 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   if (kind == GQA_KIND_Q8 && (!ksc || !vsc)) return fail(GQA_EINVAL, "scale pointer is NULL");
   if (!aligned16(q) || !aligned16(out) || !aligned16(kc) || !aligned16(vc))
     return fail(GQA_EINVAL, "q, out and the caches must be 16-byte aligned");
-  if (kind == GQA_KIND_Q8 && head_dim >= 128 && (!aligned16(ksc) || !aligned16(vsc)))
-    return fail(GQA_EINVAL, "scales must be 16-byte aligned");
+  if (kind == GQA_KIND_Q8 && scale_group != 32 && scale_group != 64)
+    return fail(GQA_EINVAL, "scale_group %d: 32 or 64 dims per scale", scale_group);
+  if (kind == GQA_KIND_Q8) {  // a row's scales are copied in one piece of nsc * 2 bytes
+    const int piece = std::min(16, 2 * (head_dim / scale_group));
+    if (((reinterpret_cast<uintptr_t>(ksc) | reinterpret_cast<uintptr_t>(vsc)) & (piece - 1)) != 0)
+      return fail(GQA_EINVAL, "scales must be %d-byte aligned", piece);
+  }
   if (n_seq <= 0 || cache_cap <= 0) return fail(GQA_EINVAL, "n_seq and cache_cap must be > 0");
   if ((int64_t)n_seq * cache_cap > INT32_MAX)
     return fail(GQA_EUNSUPPORTED, "n_seq * cache_cap must stay below 2^31 rows");
@@ -319,6 +324,7 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.vc = vc;
   p.ksc = reinterpret_cast<const __half*>(ksc);
   p.vsc = reinterpret_cast<const __half*>(vsc);
+  p.sc_shift = scale_group == 32 ? 5 : 6;
   p.ids = ids;
   p.kv_len = kv_len;
   p.seq_of = seq_of;
@@ -417,6 +423,18 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
   return decode_common(GQA_KIND_Q8, q, kq, vq, ksc, vsc, ids, budget, out, kv_len, seq_of, n_tok,
                        n_seq, n_heads, n_kv_heads, head_dim, cache_cap, max_kv_len, scale, ws,
                        ws_bytes, err_word, stream);
+}
+
+gqa_status attn_decode_q8_sel_sg(const float* q, const int8_t* kq, const int8_t* vq,
+                                 const uint16_t* ksc, const uint16_t* vsc, int scale_group,
+                                 const int32_t* ids, int budget, float* out,
+                                 const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                 int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                 int64_t cache_cap, int max_kv_len, float scale, void* ws,
+                                 size_t ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  return decode_common(GQA_KIND_Q8, q, kq, vq, ksc, vsc, ids, budget, out, kv_len, seq_of, n_tok,
+                       n_seq, n_heads, n_kv_heads, head_dim, cache_cap, max_kv_len, scale, ws,
+                       ws_bytes, err_word, stream, scale_group);
 }
 
 gqa_status attn_merge_gated(const float* part, const int32_t* n_valid, int n_split, int n_tok,

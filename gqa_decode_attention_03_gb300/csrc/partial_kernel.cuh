@@ -34,8 +34,9 @@ struct PartialParams {
   const float* q;          // [T][H][D]
   const void* kc;          // int8 caches (gather path); f16 caches come through tensor maps
   const void* vc;
-  const __half* ksc;       // [n_seq][cap][Hk][D/64] (int8 only)
+  const __half* ksc;       // [n_seq][cap][Hk][D >> sc_shift] (int8 only)
   const __half* vsc;
+  int sc_shift;            // int8: log2 of the dims sharing a scale (6: 64 dims, 5: 32 dims)
   const int32_t* ids;      // [T][budget] or null
   const int32_t* kv_len;   // [T]
   const int32_t* seq_of;   // [T] or null
@@ -77,7 +78,8 @@ struct Cfg {
   static constexpr int NP = TPW / RPP;                     // q.k passes per warp per stage
   static constexpr int NST = 3;                            // pipeline stages
   static constexpr int DPL = D / 32;                       // p.v dims per lane
-  static constexpr int NSC = D / 64;                       // f16 scales per int8 row
+  static constexpr int NSC = D / 32;                       // staged f16 scales per int8 row
+                                                           // (room for 32-dim groups)
   static constexpr int BOX_BYTES = TP * 128;
   static constexpr int KV_BYTES = 2 * NBOX * BOX_BYTES;    // K and V tiles of one stage
   static constexpr int SC_BYTES = (K == Kind::Q8) ? align_up(2 * TP * NSC * 2, 16) : 0;
@@ -346,17 +348,21 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
           cp_async_16(sk + swz_off(r, ch, C::TP), gk + ch * 16);
           cp_async_16(sv + swz_off(r, ch, C::TP), gv + ch * 16);
         }
-        const __half* gks = p.ksc + row * C::NSC;
-        const __half* gvs = p.vsc + row * C::NSC;
-        if constexpr (C::NSC == 4) {
-          cp_async_8(skc + r * 4, gks);
-          cp_async_8(svc + r * 4, gvs);
-        } else if constexpr (C::NSC == 2) {
-          cp_async_4(skc + r * 2, gks);
-          cp_async_4(svc + r * 2, gvs);
+        const int nsc = D >> p.sc_shift;  // scales of this row: 2 .. 8
+        const __half* gks = p.ksc + row * nsc;
+        const __half* gvs = p.vsc + row * nsc;
+        if (nsc == 8) {
+          cp_async_16(skc + r * C::NSC, gks);
+          cp_async_16(svc + r * C::NSC, gvs);
+        } else if (nsc == 4) {
+          cp_async_8(skc + r * C::NSC, gks);
+          cp_async_8(svc + r * C::NSC, gvs);
+        } else if (nsc == 2) {
+          cp_async_4(skc + r * C::NSC, gks);
+          cp_async_4(svc + r * C::NSC, gvs);
         } else {
-          skc[r] = gks[0];
-          svc[r] = gvs[0];
+          skc[r * C::NSC] = gks[0];
+          svc[r * C::NSC] = gvs[0];
         }
       }
       rowok[r] = okr;
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
             v[k][h] = a;
           }
           if constexpr (K == Kind::Q8) {  // qsa_attn3's factoring: scale the group's partial dot
-            const float ks = __half2float(skc[r * C::NSC + (ch * C::DPC) / 64]);
+            const float ks = __half2float(skc[r * C::NSC + ((ch * C::DPC) >> p.sc_shift)]);
 #pragma unroll
             for (int h = 0; h < GW; ++h) v[k][h] *= ks;
           }
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
           for (int h = 0; h < GW; ++h) pj[h] = ps[j * GW + h];
         }
         if constexpr (K == Kind::Q8) {
-          const float vs = __half2float(svc[r * C::NSC + (pv_byte / 64)]);
+          const float vs = __half2float(svc[r * C::NSC + (pv_byte >> p.sc_shift)]);
 #pragma unroll
           for (int h = 0; h < GW; ++h) pj[h] *= vs;
         }

@@ -24,7 +24,7 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
            "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8", "attn_merge_gated",
-           "attn_decode_tq")
+           "attn_decode_tq", "attn_decode_q8_sel_sg", "kv_append_q8_sg")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -62,6 +62,11 @@ def _load():
     lib.attn_select_topk.restype = I
     lib.kv_append_q8.argtypes = [P, P, I, I, I, P, P, P, P, I, I64, I, I, P]
     lib.kv_append_q8.restype = I
+    lib.kv_append_q8_sg.argtypes = [P, P, I, I, I, I, P, P, P, P, I, I64, I, I, P]
+    lib.kv_append_q8_sg.restype = I
+    lib.attn_decode_q8_sel_sg.argtypes = [P, P, P, P, P, I, P, I, P, P, P, I, I, I, I, I, I64, I,
+                                          F, P, SZ, P, P]
+    lib.attn_decode_q8_sel_sg.restype = I
     lib.attn_merge_gated.argtypes = [P, P, I, I, I, I, P, I64, P, P]
     lib.attn_merge_gated.restype = I
     lib.attn_decode_tq.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(F), P, F, F, P, P, P, I,
@@ -234,7 +239,8 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
                        seq_of=None, max_kv_len=None, out=None, ws=None, err=None, stream=None):
     """Decode attention over an int8 cache with per-64-dim f16 scales; optional selected ids.
 
-    kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/64] fp16; ids [T][budget] int32.
+    kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/G] fp16, one scale per G = 64
+    dims, or 32 (FORWARD_MSL's 32-element blocks), read off the shape; ids [T][budget] int32.
     """
     _need(q, torch.float32, "q", 3)
     _need(kq, torch.int8, "kq", 4)
@@ -253,8 +259,10 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
             raise ValueError("ids must be [n_tok][budget]")
     T, H, D = q.shape
     n_seq, cap, Hk, Dk = kq.shape
-    if Dk != D or kv_len.numel() != T or ksc.shape != (n_seq, cap, Hk, D // 64):
+    if (Dk != D or kv_len.numel() != T or ksc.shape[:3] != (n_seq, cap, Hk)
+            or vsc.shape != ksc.shape or ksc.shape[3] not in (D // 64, D // 32)):
         raise ValueError("shape mismatch between q, caches, scales and kv_len")
+    sg = D // ksc.shape[3]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     max_kv_len = cap if max_kv_len is None else int(max_kv_len)
     b = -1 if ids is None else budget
@@ -263,11 +271,11 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
     _need(out, torch.float32, "out", 3)
     if ws is None:
         ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), b, KIND_Q8, q.device, n_seq)
-    _check(LIB.attn_decode_q8_sel(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), _ptr(ids),
-                                  0 if ids is None else budget, _ptr(out), _ptr(kv_len),
-                                  _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale,
-                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
-                                  _stream(stream)))
+    _check(LIB.attn_decode_q8_sel_sg(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), sg,
+                                     _ptr(ids), 0 if ids is None else budget, _ptr(out),
+                                     _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
+                                     max_kv_len, scale, _ptr(ws), ws.numel() * ws.element_size(),
+                                     _ptr(err), _stream(stream)))
     return out
 
 
@@ -290,7 +298,8 @@ def attn_select_topk(block_scores, kv_len, budget, max_kv_len=None, ids=None, er
 
 def kv_append_q8(k_new, v_new, kq, vq, ksc, vsc, seq, t0, stream=None):
     """Quantise fp32 rows k_new / v_new [n_new][Hk][D] into positions t0.. of sequence `seq` of
-    the int8 cache (kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/64] fp16)."""
+    the int8 cache (kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/G] fp16, one
+    scale per G = 64 or 32 dims, read off the shape)."""
     _need(k_new, torch.float32, "k_new", 3)
     _need(v_new, torch.float32, "v_new", 3)
     for name, x, dt in (("kq", kq, torch.int8), ("vq", vq, torch.int8),
@@ -298,10 +307,12 @@ def kv_append_q8(k_new, v_new, kq, vq, ksc, vsc, seq, t0, stream=None):
         _need(x, dt, name, 4)
     n_new, Hk, D = k_new.shape
     n_seq, cap, Hk2, D2 = kq.shape
-    if v_new.shape != k_new.shape or (Hk2, D2) != (Hk, D) or ksc.shape != (n_seq, cap, Hk, D // 64):
+    if (v_new.shape != k_new.shape or (Hk2, D2) != (Hk, D) or ksc.shape[:3] != (n_seq, cap, Hk)
+            or vsc.shape != ksc.shape or ksc.shape[3] not in (D // 64, D // 32)):
         raise ValueError("shape mismatch between new rows and the cache")
-    _check(LIB.kv_append_q8(_ptr(k_new), _ptr(v_new), n_new, Hk, D, _ptr(kq), _ptr(vq), _ptr(ksc),
-                            _ptr(vsc), n_seq, cap, int(seq), int(t0), _stream(stream)))
+    _check(LIB.kv_append_q8_sg(_ptr(k_new), _ptr(v_new), n_new, Hk, D, D // ksc.shape[3],
+                               _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), n_seq, cap, int(seq),
+                               int(t0), _stream(stream)))
 
 
 def attn_merge(part, n_valid, out=None, gate=None, gate_stride=None, stream=None):

@@ -100,6 +100,7 @@ class Case:
     budget: int | None = None
     seed: int = 0
     meta: dict = field(default_factory=dict)
+    scale_group: int = 64              # int8: dims per f16 scale (64, or 32)
 
     @property
     def n_tok(self):
@@ -125,7 +126,7 @@ class Case:
     def kv_bytes(self) -> int:
         """K/V (and scale) bytes the rows must read once per KV head: the algorithmic KV read."""
         D, Hk = self.head_dim, self.n_kv_heads
-        per_pos = 2 * D * 2 if self.kind == "f16" else 2 * (D + 2 * (D // 64))
+        per_pos = 2 * D * 2 if self.kind == "f16" else 2 * (D + 2 * (D // self.scale_group))
         if self.ids is None and len(set(self.seq_of.tolist())) < self.n_tok:
             # rows sharing a sequence (causal prefill rows) need each position once
             tot = 0
@@ -171,10 +172,12 @@ def make_f16_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, cache_cap=
 
 
 def make_q8_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, budget=None,
-                 cache_cap=None, seq_of=None, n_seq=None, scale=None, name="q8") -> Case:
-    """Random int8-cache problem with per-64-dim f16 scales and (if ``budget``) sorted ids."""
-    if head_dim % 64:
-        raise ValueError("int8 caches need head_dim % 64 == 0")
+                 cache_cap=None, seq_of=None, n_seq=None, scale=None, name="q8",
+                 scale_group=64) -> Case:
+    """Random int8-cache problem with one f16 scale per ``scale_group`` dims (64, or 32 as in
+    FORWARD_MSL's q8 planes) and (if ``budget``) sorted ids."""
+    if head_dim % 64 or scale_group not in (32, 64):
+        raise ValueError("int8 caches need head_dim % 64 == 0 and groups of 32 or 64 dims")
     kv_len = np.asarray(kv_len, dtype=np.int32).reshape(n_tok)
     seq_of = (np.arange(n_tok, dtype=np.int32) if seq_of is None
               else np.asarray(seq_of, dtype=np.int32).reshape(n_tok))
@@ -188,7 +191,7 @@ def make_q8_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, budget=None
     shape = (n_seq, cap, n_kv_heads, head_dim)
     kq = np.empty(shape, dtype=np.int8)
     vq = np.empty(shape, dtype=np.int8)
-    ksc = np.empty(shape[:3] + (head_dim // 64,), dtype=np.float16)
+    ksc = np.empty(shape[:3] + (head_dim // scale_group,), dtype=np.float16)
     vsc = np.empty_like(ksc)
     _fill_q8(kq, ksc, ss[3:3 + n_seq], per_seq)
     _fill_q8(vq, vsc, ss[3 + n_seq:], per_seq)
@@ -204,7 +207,7 @@ def make_q8_case(seed, n_tok, n_heads, n_kv_heads, head_dim, kv_len, budget=None
                 ids[t] = np.sort(g.choice(L, size=budget, replace=False)).astype(np.int32)
     scale = 1.0 / math.sqrt(head_dim) if scale is None else float(scale)
     return Case(name, q, kv_len, seq_of, scale, n_kv_heads, cap, "q8", kq=kq, vq=vq, ksc=ksc,
-                vsc=vsc, ids=ids, budget=budget, seed=seed)
+                vsc=vsc, ids=ids, budget=budget, seed=seed, scale_group=scale_group)
 
 
 LLOYD_MAX_2BIT = (-1.5104, -0.4528, 0.4528, 1.5104)  # 2-bit Gaussian quantiser points

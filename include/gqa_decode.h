@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 7
+#define GQA_ABI_VERSION 8
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -168,6 +168,22 @@ gqa_status attn_decode_q8_sel(const float* q, const int8_t* kq, const int8_t* vq
                               cudaStream_t stream);
 
 /*
+ * attn_decode_q8_sel_sg -- attn_decode_q8_sel with scale_group dims per f16 scale: 64 as above,
+ * or 32, the 32-element blocks of FORWARD_MSL's q8 cache (kv_append_q8 / attn_part2_q8), whose
+ * scale plane [max_t][row/32] is ksc here ([n_seq][cap][n_kv_heads][head_dim/32] with n_seq = 1;
+ * a caller holding quants and scales in one buffer passes buffer + scale_off as ksc).
+ *   ksc, vsc aligned to min(16, 2 * head_dim / scale_group) bytes; scale_group not in {32, 64}
+ *   gives GQA_EINVAL.  Other arguments as attn_decode_q8_sel.
+ */
+gqa_status attn_decode_q8_sel_sg(const float* q, const int8_t* kq, const int8_t* vq,
+                                 const uint16_t* ksc, const uint16_t* vsc, int scale_group,
+                                 const int32_t* ids, int budget, float* out,
+                                 const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                 int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                 int64_t cache_cap, int max_kv_len, float scale, void* ws,
+                                 size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+/*
  * attn_select_topk -- the selected-cell id list of attn_decode_q8_sel (qsa2.metal, qsa_topk2).
  * Row t's cells 0..kv_len[t]-1 come in blocks of 4 (the last block holds kv_len[t] % 4 cells);
  * cell c carries the score of its block, block_scores[t * score_stride + c / 4].  The row keeps
@@ -231,6 +247,17 @@ gqa_status attn_decode_tq(const float* q_rot, const float* q_jl, const uint32_t*
 gqa_status kv_append_q8(const float* k_new, const float* v_new, int n_new, int n_kv_heads,
                         int head_dim, int8_t* kq, int8_t* vq, uint16_t* ksc, uint16_t* vsc,
                         int n_seq, int64_t cache_cap, int seq, int t0, cudaStream_t stream);
+
+/*
+ * kv_append_q8_sg -- kv_append_q8 with scale_group dims per scale: 64, or 32 as FORWARD_MSL's
+ * kv_append_q8 quantises (one simdgroup per 32-element block there; one warp per block here).
+ * The scales are [n_seq][cap][n_kv_heads][head_dim / scale_group]; scale_group not in {32, 64}
+ * gives GQA_EINVAL.  Other arguments as kv_append_q8.
+ */
+gqa_status kv_append_q8_sg(const float* k_new, const float* v_new, int n_new, int n_kv_heads,
+                           int head_dim, int scale_group, int8_t* kq, int8_t* vq, uint16_t* ksc,
+                           uint16_t* vsc, int n_seq, int64_t cache_cap, int seq, int t0,
+                           cudaStream_t stream);
 
 /*
  * attn_merge -- log-sum-exp merge of split partials (qsa2.metal, qsa_merge2; FORWARD_MSL's

@@ -38,7 +38,8 @@ from __future__ import annotations
 
 import numpy as np
 
-SCALE_GROUP = 64  # dims sharing one f16 scale in the int8 cache (qsa2.metal, qsa_attn2)
+SCALE_GROUP = 64  # dims sharing one f16 scale in qsa2.metal's int8 cache (qsa_attn2)
+SCALE_GROUPS = (32, 64)  # also FORWARD_MSL's q8 planes: one scale per 32-element block
 
 
 # ----------------------------------------------------------------------------- dequantisation
@@ -48,15 +49,24 @@ def dequant_f16(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float16).astype(np.float64)
 
 
-def dequant_q8(vals, scales) -> np.ndarray:
-    """int8 values times the f16 scale of their 64-dim group, in float64 (exact).
+def _scale_index(D: int, nsc: int) -> np.ndarray:
+    """The scale of each dim: contiguous groups of D / nsc dims (32 or 64)."""
+    if nsc <= 0 or D % nsc or D // nsc not in SCALE_GROUPS:
+        raise ValueError(f"{nsc} scales for {D} dims: groups must hold 32 or 64 dims")
+    return np.arange(D) // (D // nsc)
 
-    ``vals[..., D]`` int8 and ``scales[..., D // 64]`` f16, as in qsa2.metal's qsa_attn2, where a
-    K element is float(int8) * float(scale[row*4 + dim/64]).
+
+def dequant_q8(vals, scales) -> np.ndarray:
+    """int8 values times the f16 scale of their group, in float64 (exact).
+
+    ``vals[..., D]`` int8 and ``scales[..., D // group]`` f16.  The group is read off the shapes:
+    64 dims as in qsa2.metal's qsa_attn2, where a K element is float(int8) *
+    float(scale[row*4 + dim/64]); 32 dims as in FORWARD_MSL's q8 planes (one symmetric scale
+    per 32-element block, read back by attn_part2_q8).
     """
     v = np.asarray(vals, dtype=np.int8).astype(np.float64)
     s = np.asarray(scales, dtype=np.float16).astype(np.float64)
-    return v * np.repeat(s, SCALE_GROUP, axis=-1)
+    return v * s[..., _scale_index(v.shape[-1], s.shape[-1])]
 
 
 # ----------------------------------------------------------------------------- the definition
@@ -269,9 +279,9 @@ def select_topk_cells(block_scores_row, n_kv: int, budget: int) -> np.ndarray:
 
 # ----------------------------------------------------------------------------- quantise on append
 
-def quantize_q8(x) -> tuple[np.ndarray, np.ndarray]:
-    """int8 codes and f16 scales of fp32 rows ``x[..., D]``, one scale per 64 dims
-    (FORWARD_MSL, kv_append_q8, with the 64-dim groups of the int8 cache read by qsa2.metal):
+def quantize_q8(x, group: int = SCALE_GROUP) -> tuple[np.ndarray, np.ndarray]:
+    """int8 codes and f16 scales of fp32 rows ``x[..., D]``, one scale per ``group`` dims
+    (FORWARD_MSL, kv_append_q8: 32-element blocks; 64 for the int8 cache read by qsa2.metal):
 
         d = amax|x_group| / 127,  q = rint(x / d) clamped to [-127, 127] (0 when d = 0),
         scale = f16(d)
@@ -281,9 +291,9 @@ def quantize_q8(x) -> tuple[np.ndarray, np.ndarray]:
     """
     x = np.asarray(x, dtype=np.float32)
     D = x.shape[-1]
-    if D % SCALE_GROUP:
-        raise ValueError("head_dim must be a multiple of 64")
-    g = x.reshape(x.shape[:-1] + (D // SCALE_GROUP, SCALE_GROUP))
+    if group not in SCALE_GROUPS or D % group:
+        raise ValueError("group must be 32 or 64 and divide head_dim")
+    g = x.reshape(x.shape[:-1] + (D // group, group))
     amax = np.abs(g).max(axis=-1)                                   # fp32
     d = (amax / np.float32(127)).astype(np.float32)                 # fp32 division
     with np.errstate(divide="ignore", invalid="ignore"):

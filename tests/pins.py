@@ -122,8 +122,8 @@ def brute_force(case):
                 kr = [[Decimal(float(x)) for x in case.k[s, j, g]] for j in cells]
                 vr = [[Decimal(float(x)) for x in case.v[s, j, g]] for j in cells]
             else:
-                def deq(vals, scl):
-                    return [Decimal(int(vals[d])) * Decimal(float(scl[d // 64])) for d in range(D)]
+                def deq(vals, scl, grp=case.scale_group):
+                    return [Decimal(int(vals[d])) * Decimal(float(scl[d // grp])) for d in range(D)]
                 kr = [deq(case.kq[s, j, g], case.ksc[s, j, g]) for j in cells]
                 vr = [deq(case.vq[s, j, g], case.vsc[s, j, g]) for j in cells]
             out[t, h] = [float(x) for x in _brute_row(qh, kr, vr, case.scale)]
@@ -136,7 +136,9 @@ def tiny_cases():
                         scale=0.35, name="brute_f16")
     q = W.make_q8_case(8, 2, 4, 2, 128, [6, 3], budget=4, cache_cap=7, scale=0.0625,
                        name="brute_q8")
-    return [f, q]
+    q32 = W.make_q8_case(9, 2, 4, 2, 64, [5, 4], cache_cap=5, scale=0.125, scale_group=32,
+                         name="brute_q8_g32")
+    return [f, q, q32]
 
 
 def oracle_case(case, rows=None):

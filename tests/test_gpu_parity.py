@@ -130,6 +130,32 @@ def test_q8_dense(D):
     assert_close(got, oracle_ref(case), TOL_Q8, f"q8 dense D{D}")
 
 
+@pytest.mark.parametrize("chunk", [None, 128])
+@pytest.mark.parametrize("ids", [False, True])
+@pytest.mark.parametrize("D,G", [(64, 4), (128, 4), (256, 12), (128, 3)])
+def test_q8_scale_blocks_of_32(D, G, ids, chunk):
+    # FORWARD_MSL's q8 cache: one f16 scale per 32-element block
+    case = W.make_q8_case(330 + D + G, 3, 2 * G, 2, D, [700, 5, 260],
+                          budget=300 if ids else None, cache_cap=720, scale=1 / math.sqrt(D),
+                          scale_group=32)
+    assert case.ksc.shape[-1] == D // 32
+    with forced_chunk(chunk):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, f"q8/32 D{D} G{G} ids{ids} chunk{chunk}")
+
+
+def test_q8_scale_blocks_of_32_differ_from_64():
+    # the same codes read with their own 32-blocks and with the 64-dim reading differ: the
+    # kernel really takes the group from the scale layout
+    case = W.make_q8_case(341, 1, 8, 2, 128, [300], cache_cap=300, scale=0.1, scale_group=32)
+    got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_Q8, "q8/32")
+    wrong = W.make_q8_case(341, 1, 8, 2, 128, [300], cache_cap=300, scale=0.1)
+    wrong.kq, wrong.vq, wrong.q = case.kq, case.vq, case.q
+    wrong.ksc, wrong.vsc = case.ksc[..., ::2].copy(), case.vsc[..., ::2].copy()
+    assert np.abs(run_case(wrong).cpu().numpy() - got).max() > 1e-3
+
+
 # ----------------------------------------------------------------------------- properties
 
 def test_gather_is_bit_exact():

@@ -142,7 +142,10 @@ def _mutants():
         "width off by one": ("_width",
                              lambda n, budget: max(int(n), 0) if budget is None
                              else max(0, min(max(int(n), 0), int(budget)) - 1)),
-        "scale group of 32": ("SCALE_GROUP", 32),
+        "scale groups interleaved": ("_scale_index",
+                                     lambda D, nsc: np.arange(D) % nsc),
+        "scale groups reversed": ("_scale_index",
+                                  lambda D, nsc: (nsc - 1) - np.arange(D) // (D // nsc)),
     }
 
 
@@ -281,6 +284,42 @@ def test_quantize_closed_cases():
     x[0, :4] = [127.0, 2.5, 3.5, -2.5]
     q, _ = oracle.quantize_q8(x)
     assert list(q[0, :4]) == [127, 2, 4, -2]
+
+
+def test_quantize_32_element_blocks():
+    # FORWARD_MSL's kv_append_q8 block: 32 elements share d = amax / 127
+    x = np.zeros((1, 64), np.float32)
+    x[0, :32] = np.linspace(-2, 2, 32, dtype=np.float32)   # amax 2
+    x[0, 32:] = np.linspace(-0.5, 0.25, 32, dtype=np.float32)  # amax 0.5
+    q, s = oracle.quantize_q8(x, group=32)
+    assert s.shape == (1, 2)
+    assert s[0, 0] == np.float16(np.float32(2) / np.float32(127))
+    assert s[0, 1] == np.float16(np.float32(0.5) / np.float32(127))
+    assert q[0, 0] == -127 and q[0, 31] == 127 and q[0, 32] == -127
+    assert q[0, 63] == np.rint(np.float32(0.25) / (np.float32(0.5) / np.float32(127)))
+    # 32-groups of a row equal the 64-group code of each half quantised alone
+    rng = np.random.default_rng(12)
+    y = rng.standard_normal((3, 128)).astype(np.float32)
+    q32, s32 = oracle.quantize_q8(y, group=32)
+    for b in range(4):
+        qb, sb = oracle.quantize_q8(np.tile(y[:, 32 * b:32 * (b + 1)], 2), group=64)
+        assert np.array_equal(q32[:, 32 * b:32 * (b + 1)], qb[:, :32])
+        assert np.array_equal(s32[:, b], sb[:, 0])
+    with pytest.raises(ValueError):
+        oracle.quantize_q8(y, group=16)
+
+
+def test_dequant_reads_the_group_off_the_shapes():
+    vals = np.arange(-64, 64, dtype=np.int8).reshape(1, 128)
+    s64 = np.array([[0.5, 2.0]], np.float16)
+    s32 = np.array([[0.5, 1.0, 2.0, 4.0]], np.float16)
+    d64 = oracle.dequant_q8(vals, s64)
+    d32 = oracle.dequant_q8(vals, s32)
+    assert d64[0, 63] == -1 * 0.5 and d64[0, 64] == 0 * 2.0 and d64[0, 127] == 63 * 2.0
+    assert d32[0, 31] == -33 * 0.5 and d32[0, 32] == -32 * 1.0 and d32[0, 95] == 31 * 2.0
+    assert d32[0, 96] == 32 * 4.0
+    with pytest.raises(ValueError):
+        oracle.dequant_q8(vals, np.ones((1, 8), np.float16))
 
 
 def test_gated_merge_closed_forms():
