@@ -379,6 +379,13 @@ def long_context() -> Case:
                          name="long_ctx_b16_U1024-32768_h32_hk8_d128")
 
 
+def long_context_full() -> Case:
+    """The long-context shape with every sequence at the full 32768 positions (16 x 32768,
+    32 heads / 8 KV heads, D=128): the fixed-length sub-case of the long-context workload."""
+    return make_f16_case(1011, 16, 32, 8, 128, [32768] * 16, cache_cap=32768,
+                         scale=1 / math.sqrt(128), name="long_ctx_full_b16_L32768_h32_hk8_d128")
+
+
 def long_context_4() -> Case:
     """The long-context shape with 4 sequences (a smaller case for profiler captures)."""
     L = long_context_lengths(seed=1007, n=4)
@@ -438,6 +445,7 @@ NAMED = {
     "gqa_d64_L4096": lambda: gqa_d64(4096),
     "long_ctx": long_context,
     "long_ctx_4": long_context_4,
+    "long_ctx_full": long_context_full,
     "q8_sel": q8_selected,
     "q8_topk_sel": q8_topk_selected,
     "batched": batched,

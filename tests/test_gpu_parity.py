@@ -57,6 +57,15 @@ def test_batched_sampled_rows():
     assert np.isfinite(got).all()
 
 
+def test_long_ctx_full_sampled_rows():
+    """16 x 32768 (the fixed-length long-context sub-case): full launch, sampled rows."""
+    case = W.long_context_full()
+    got = run_case(case).cpu().numpy()
+    rows = [0, 9, 15]
+    assert_close(got[rows], oracle_ref(case, rows=rows), TOL_F16, "long_ctx_full")
+    assert np.isfinite(got).all()
+
+
 def test_prefill_chunk_rows():
     """16 causal rows at 8176.. of one sequence (row r sees 8177 + r positions)."""
     case = W.prefill_chunk()
