@@ -160,7 +160,7 @@ int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
   const char* r = std::getenv("GQA_F16_ROWS");  // "off": one CTA per row (tests, comparison)
   if (r && std::strcmp(r, "off") == 0) return 1;
   if (head_dim == 256 || (group != 1 && group != 2 && group != 4 && group != 8)) return 1;
-  return 32 / group;  // 4 consumer warps x 8 (row, head) pairs
+  return 32 / group;  // 2 pair sets x 16 (row, head) pairs
 }
 
 int stage_rows(int kind, int head_dim) {

@@ -24,15 +24,19 @@ cudaError_t ensure_smem(const void* fn, int bytes) {
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,
                          int n_tok, int n_heads, float* out, cudaStream_t s, const float* gate,
                          long long gate_stride) {
-  const dim3 grid(n_heads, n_tok);  // one CTA of head_dim / 2 threads per (head, row)
+  // one warp per (row, head), kMergeWarps per CTA
+  const long long pairs = (long long)n_tok * n_heads;
+  const unsigned grid = static_cast<unsigned>((pairs + kMergeWarps - 1) / kMergeWarps);
+  const int threads = 32 * kMergeWarps;
   if (head_dim == 64)
-    merge_kernel<64><<<grid, 32, 0, s>>>(part, n_valid, n_split, n_heads, gate, gate_stride, out);
+    merge_kernel<64><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
+                                              gate_stride, out);
   else if (head_dim == 128)
-    merge_kernel<128><<<grid, 64, 0, s>>>(part, n_valid, n_split, n_heads, gate, gate_stride,
-                                          out);
+    merge_kernel<128><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
+                                               gate_stride, out);
   else
-    merge_kernel<256><<<grid, 128, 0, s>>>(part, n_valid, n_split, n_heads, gate, gate_stride,
-                                           out);
+    merge_kernel<256><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
+                                               gate_stride, out);
   return cudaGetLastError();
 }
 

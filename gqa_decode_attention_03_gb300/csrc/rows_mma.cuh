@@ -4,26 +4,32 @@
 // position p attends to [0, p], flash_attention_tq.metal's per-query window), or decode rows of
 // one sequence.  Served one CTA per row, each row re-reads the sequence's K/V.  Here one CTA
 // serves a run of up to R consecutive rows with the same seq_of[] value: it stages every K/V
-// tile of its chunk once (TMA, three-stage mbarrier ring, as in partial_mma.cuh) and all rows'
+// tile of its chunk once (TMA, two-stage mbarrier ring, as in partial_mma.cuh) and all rows'
 // heads read it there -- attention_gqa.metal's "load K/V once, reuse across the group",
 // extended from the heads of a group to the rows of a sequence.
 //
-// Warps.  The A operand of a consumer warp's m16n8k16 MMAs holds 8 (row, head) pairs: rows
-// 0-7 the f16 hi parts of q, rows 8-15 the lo parts (so 8 / G query rows per warp), and the warp
-// walks every position of every stage.  Each thread owns one (row, head) pair: its row's own
-// length masks its scores (positions at or past L_row become -inf), its online softmax is its
-// own, and at the end it writes its own output or chunk partial.  V fragment halves of
-// positions past the group's longest row are zeroed in registers, as cache garbage may sit
-// there.  Split rows are merged afterwards by merge_kernel (one CTA per row and head): a
-// group's rows bring many partials at once, too many for one last CTA to merge quickly.
+// Warps.  The A operand of a consumer warp's m16n8k16 MMAs holds 16 (row, head) pairs, q in
+// f16 with the scale folded in (16 / G query rows per pair set); the softmax weights go back
+// into the p.v MMAs as f16 straight from the score fragments.  (The per-row decode kernels
+// carry q and the weights as f16 hi + lo pairs; this kernel is compute-bound, and single f16
+// keeps its error near 3e-5, inside the f16 path's 2e-3, for half the MMAs.)  Two pair sets
+// per CTA, and two warps per set, each taking half of every stage's 16-position blocks with its
+// own online softmax; at the end of a chunk the second half hands its (m, l, acc) to the first
+// through shared memory, which combines them.  Each thread owns two pairs (fragment rows gid
+// and gid + 8): a pair's row length masks its scores (positions at or past L_row become -inf).
+// V fragment halves of positions past the group's longest row are zeroed in registers, as
+// cache garbage may sit there.  Split rows are merged afterwards by merge_kernel (one warp per
+// row and head): a group's rows bring many partials at once, too many for one last CTA to
+// merge quickly.  (Merging inside a thread-block cluster of the chunks measured slower on
+// GB300: clusters of 16 CTAs could not all be resident at once.)
 //
 // Rows.  Groups of consecutive rows with equal seq_of[] start at every multiple of R and
 // wherever seq_of[] changes.  The grid is (chunks, KV heads, slots): slot z serves groups
 // z, z + slots, ..., found on the device by a warp-wide ballot over seq_of[], with the TMA ring
-// running on from one group to the next.  The host sizes the slots from the sequence count, so
-// a prefill chunk (one sequence) is one slot and no CTA is launched only to exit.  A row keeps
-// its own chunk count ceil(L / chunk) (n_valid), so a row shorter than the group's longest
-// simply has no partials for the chunks past its end.
+// running on from one group to the next.  The host sizes the slots from the row and sequence
+// counts, so that no CTA is launched only to exit.  A row keeps its own chunk count
+// ceil(L / chunk) (n_valid), so a row shorter than the group's longest simply has no partials
+// for the chunks past its end.
 #pragma once
 
 #include "partial_mma.cuh"
@@ -37,17 +43,21 @@ struct RowsCfg {
   static constexpr int NB16 = TP / 16;            // 16-position blocks per stage
   static constexpr int NT = D / 8;                // O n-tiles per warp
   static constexpr int KS = D / 16;               // q.k k-steps
-  static constexpr int NST = 3;
+  static constexpr int NST = 2;
   static constexpr int BOX_BYTES = TP * 128;
   static constexpr int KV_BYTES = 2 * NBOX * BOX_BYTES;
   static constexpr int STAGE_BYTES = KV_BYTES;
-  static constexpr int NCW = 4;                   // consumer warps: 32 (row, head) pairs, so
-                                                  // two CTAs fit an SM (16 warps to hide the
-                                                  // MMA / softmax latency of each block)
+  static constexpr int NPSET = 2;                 // pair sets: 16 (row, head) pairs each
+  static constexpr int NHALF = 2;                 // warps per pair set, each on half of a stage
+  static constexpr int NCW = NPSET * NHALF;       // consumer warps
+  static constexpr int NBH = NB16 / NHALF;        // 16-position blocks per warp and stage
+  static constexpr int XF = 2 * (2 * NT + 2);     // floats a thread hands to its partner warp
+  static constexpr int X_BYTES = NPSET * 32 * XF * 4;
   static constexpr int MAX_THREADS = 32 * (NCW + 1);
-  static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + 2 * NST * 8;
+  static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + X_BYTES + 2 * NST * 8;
   static constexpr float RESCALE_LOG2 = 8.f;
   static_assert(D == 64 || D == 128, "row grouping serves head_dim 64 and 128");
+  static_assert(NB16 % NHALF == 0, "whole blocks per half");
 };
 
 __device__ __forceinline__ int rows_seq(const PartialParams& p, int t) {
@@ -123,6 +133,8 @@ __device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, i
   return gr;
 }
 
+// Two CTAs per SM: 168 registers a thread, so that three warps fit one SM sub-partition's
+// 16K registers (200 registers measured 20 % slower: one CTA per SM)
 template <int D>
 __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
     partial_mma_rows_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -131,14 +143,15 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y, slot = blockIdx.z, nslots = gridDim.z;
   const int G = p.group;             // 1, 2, 4 or 8
-  const int rpw = 8 / G;             // rows per warp
-  const int R = rpw * C::NCW;        // rows per group at most
+  const int rpw = 16 / G;            // rows per warp
+  const int R = rpw * C::NPSET;      // rows per group at most
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c0 = c * p.chunk;
 
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
-  uint64_t* full = reinterpret_cast<uint64_t*>(stages + C::NST * C::STAGE_BYTES);
+  float* xbuf = reinterpret_cast<float*>(stages + C::NST * C::STAGE_BYTES);  // [pset][XF][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + C::NST * C::STAGE_BYTES + C::X_BYTES);
   uint64_t* empty = full + C::NST;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
@@ -164,8 +177,7 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
       const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
       if (t0 < 0) break;
       const RowGroup gr = rows_group(p, t0, R, lane);
-      if (c0 >= gr.lmax) continue;
-      const int c1 = min(c0 + p.chunk, gr.lmax);
+      const int c1 = min(c0 + p.chunk, gr.lmax);  // nothing to issue when c1 <= c0
       const int zb = gr.s * static_cast<int>(p.cache_cap) + c0;
       for (int pos = c0; pos < c1; pos += C::TP, ++it) {
         const int st = it % C::NST;
@@ -197,15 +209,18 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
     return;
   }
 
-  // ---- consumer warps: pairs (row j, head h) with j = warp * rpw + gid / G, h = gid % G
+  // ---- consumer warps: pair set ps = warp % 4 holds 16 (row, head) pairs, pair i = A row i
+  //      with row j = ps * rpw + i / G and head h = i % G; half hf = warp / 4 takes blocks
+  //      [hf * NBH, (hf + 1) * NBH) of every stage.  Thread (gid, tig) owns pairs gid, gid + 8.
+  const int ps = warp % C::NPSET, hf = warp / C::NPSET;
   const int gid = lane >> 2, tig = lane & 3;
-  const int h = gid % G;
-  const int head = g * G + h;
   const int mi = lane >> 3, rr = lane & 7;
   int it = 0;
   bool ok = true;
 
-  for (int k = slot; ok; k += nslots) {
+  // Every consumer warp walks every group, also after a failed wait (then computing nothing),
+  // so that the CTA's named barriers stay in step.
+  for (int k = slot;; k += nslots) {
     const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
     if (t0 < 0) break;
     const RowGroup gr = rows_group(p, t0, R, lane);
@@ -225,165 +240,225 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
         }
       }
     }
-    if (c0 >= gr.lmax) continue;
-    const int c1 = min(c0 + p.chunk, gr.lmax);
-    const int j = warp * rpw + gid / G;
-    const bool rv = j < gr.nr;               // this thread's pair is a real row
-    const int t = t0 + (rv ? j : 0);
-    int dummy = 0;
-    const int Lr = rv ? rows_len(p, t, seq_ok, &dummy) : 0;  // this row's length
-    const bool active = warp * rpw < gr.nr;  // the warp has rows in this group
-
-    uint32_t qa[C::KS][4];
-    {
-      const float* qrow = p.q + ((size_t)t * p.n_heads + head) * D;
-      const float f = rv ? p.scale_log2 : 0.f;
+    if (c0 < gr.lmax) {  // the same for every consumer warp
+      const int c1 = min(c0 + p.chunk, gr.lmax);
+      bool rv[2];
+      int tr[2], Lr[2], hd[2];
 #pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        const int d0 = ks * 16 + 2 * tig;
-        const float2 x0 = __ldg(reinterpret_cast<const float2*>(qrow + d0));
-        const float2 x1 = __ldg(reinterpret_cast<const float2*>(qrow + d0 + 8));
-        split_hi_lo(x0.x * f, x0.y * f, qa[ks][0], qa[ks][1]);
-        split_hi_lo(x1.x * f, x1.y * f, qa[ks][2], qa[ks][3]);
+      for (int u = 0; u < 2; ++u) {
+        const int i = gid + 8 * u;
+        const int j = ps * rpw + i / G;
+        rv[u] = j < gr.nr;  // this pair is a real row
+        tr[u] = t0 + (rv[u] ? j : 0);
+        int dummy = 0;
+        Lr[u] = rv[u] ? rows_len(p, tr[u], seq_ok, &dummy) : 0;  // the row's own length
+        hd[u] = g * G + i % G;
       }
-    }
-    float o[C::NT][4];
-#pragma unroll
-    for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+      const bool active = ps * rpw < gr.nr;  // the pair set has rows in this group
 
-    for (int pos0 = c0; pos0 < c1; pos0 += C::TP, ++it) {
-      const int st = it % C::NST;
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (it / C::NST) & 1));
-      if (!ok) break;
-      if (active) {
-        const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
-        const uint32_t sv = sk + C::NBOX * C::BOX_BYTES;
-        // q.k^T for every 16-position block of the stage first (independent MMA chains), then the
-        // softmax and p.v of each block: the scheduler can overlap one block's softmax with
-        // another's MMAs
-        float sc[C::NB16][2][4];
+      // q in f16 with scale * log2(e) folded in: rows gid and gid + 8 of the A fragments
+      uint32_t qa[C::KS][4];
+      {
+        const float* q0 = p.q + ((size_t)tr[0] * p.n_heads + hd[0]) * D;
+        const float* q1 = p.q + ((size_t)tr[1] * p.n_heads + hd[1]) * D;
+        const float f0 = rv[0] ? p.scale_log2 : 0.f, f1 = rv[1] ? p.scale_log2 : 0.f;
 #pragma unroll
-        for (int b = 0; b < C::NB16; ++b) {
-          const int r0 = b * 16;
-          float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[b][nt][e] = 0.f;
-          if (pos0 + r0 >= c1) continue;  // block past the chunk end
-#pragma unroll
-          for (int ks = 0; ks < C::KS; ks += 2) {
-            uint32_t kb[4], kc[4];
-            ldsm_x4(kb, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + (mi & 1), C::TP));
-            ldsm_x4(kc, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + 2 + (mi & 1), C::TP));
-            mma_f16(sc[b][0], qa[ks], kb[0], kb[1]);
-            mma_f16(sc[b][1], qa[ks], kb[2], kb[3]);
-            mma_f16(sd[0], qa[ks + 1], kc[0], kc[1]);
-            mma_f16(sd[1], qa[ks + 1], kc[2], kc[3]);
-          }
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[b][nt][e] += sd[nt][e];
-        }
-#pragma unroll
-        for (int b = 0; b < C::NB16; ++b) {
-          const int r0 = b * 16;
-          const int base = pos0 + r0;  // cache position of the block's row 0
-          const int nv = min(max(c1 - base, 0), 16);         // rows holding data for some row
-          if (nv == 0) continue;
-          const int nrow = min(max(Lr - base, 0), 16);       // rows inside this thread's window
-          float x[2][2];
-          float mt = -INFINITY;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              const float v = sc[b][nt][jj] + sc[b][nt][2 + jj];
-              x[nt][jj] = (nt * 8 + 2 * tig + jj) < nrow ? v : -INFINITY;
-              mt = fmaxf(mt, x[nt][jj]);
-            }
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-          // a pair whose row ends before this block keeps mt = -inf: nothing to add
-          const bool grow = mt != -INFINITY && mt > m_run + C::RESCALE_LOG2;
-          if (__any_sync(0xffffffffu, grow)) {
-            const float m_new = grow ? mt : m_run;
-            const float corr = grow ? fast_exp2(m_run - m_new) : 1.f;
-            m_run = m_new;
-            l_run *= corr;
-#pragma unroll
-            for (int n = 0; n < C::NT; ++n) {
-              o[n][0] *= corr;
-              o[n][1] *= corr;
-              o[n][2] *= corr;
-              o[n][3] *= corr;
-            }
-          }
-          float pr[2][2];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              pr[nt][jj] = m_run == -INFINITY ? 0.f : fast_exp2(x[nt][jj] - m_run);
-              l_run += pr[nt][jj];
-            }
-          uint32_t pa[4];
-          split_hi_lo(pr[0][0], pr[0][1], pa[0], pa[1]);
-          split_hi_lo(pr[1][0], pr[1][1], pa[2], pa[3]);
-          const bool tail = nv < 16;
-          const uint32_t mk0 =
-              ((2 * tig < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 1 < nv) ? 0xffff0000u : 0u);
-          const uint32_t mk1 =
-              ((2 * tig + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 9 < nv) ? 0xffff0000u : 0u);
-#pragma unroll
-          for (int np = 0; np < C::NT / 2; ++np) {
-            uint32_t vb[4];
-            ldsm_x4_t(vb, sv + swz_off(r0 + (mi & 1) * 8 + rr, np * 2 + (mi >> 1), C::TP));
-            if (tail) {
-              vb[0] &= mk0;
-              vb[1] &= mk1;
-              vb[2] &= mk0;
-              vb[3] &= mk1;
-            }
-            mma_f16(o[2 * np], pa, vb[0], vb[1]);
-            mma_f16(o[2 * np + 1], pa, vb[2], vb[3]);
-          }
+        for (int ks = 0; ks < C::KS; ++ks) {
+          const int d0 = ks * 16 + 2 * tig;
+          const float2 x0 = __ldg(reinterpret_cast<const float2*>(q0 + d0));
+          const float2 x1 = __ldg(reinterpret_cast<const float2*>(q0 + d0 + 8));
+          const float2 y0 = __ldg(reinterpret_cast<const float2*>(q1 + d0));
+          const float2 y1 = __ldg(reinterpret_cast<const float2*>(q1 + d0 + 8));
+          qa[ks][0] = h2_bits(__floats2half2_rn(x0.x * f0, x0.y * f0));
+          qa[ks][1] = h2_bits(__floats2half2_rn(y0.x * f1, y0.y * f1));
+          qa[ks][2] = h2_bits(__floats2half2_rn(x1.x * f0, x1.y * f0));
+          qa[ks][3] = h2_bits(__floats2half2_rn(y1.x * f1, y1.y * f1));
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    if (!ok) break;
-    if (!active) continue;
+      float o[C::NT][4];
+#pragma unroll
+      for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    // ---- this thread's (row, head): the output, or the chunk's partial (merged afterwards by
-    //      merge_kernel)
-    if (!rv || c0 >= Lr) continue;
-    if (!p.merge) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* orow = p.out + ((size_t)t * p.n_heads + head) * D;
+      for (int pos0 = c0; ok && pos0 < c1; pos0 += C::TP, ++it) {
+        const int st = it % C::NST;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (it / C::NST) & 1));
+        if (!ok) break;
+        if (active) {
+          const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
+          const uint32_t sv = sk + C::NBOX * C::BOX_BYTES;
+          // q.k^T for this warp's blocks of the stage first (independent MMA chains), then the
+          // softmax and p.v of each block
+          float sc[C::NBH][2][4];
 #pragma unroll
-      for (int n = 0; n < C::NT; ++n) {
-        const int d = n * 8 + 2 * tig;
-        *reinterpret_cast<float2*>(orow + d) =
-            make_float2((o[n][0] + o[n][2]) * inv, (o[n][1] + o[n][3]) * inv);
-      }
-    } else {
-      float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
+          for (int bb = 0; bb < C::NBH; ++bb) {
+            const int r0 = (hf * C::NBH + bb) * 16;
+            float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int n = 0; n < C::NT; ++n) {
-        const int d = n * 8 + 2 * tig;
-        *reinterpret_cast<float2*>(pr + d) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sc[bb][nt][e] = 0.f;
+            if (pos0 + r0 >= c1) continue;  // block past the chunk end
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ks += 2) {
+              uint32_t kb[4], kc[4];
+              ldsm_x4(kb, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + (mi & 1), C::TP));
+              ldsm_x4(kc, sk + swz_off(r0 + (mi >> 1) * 8 + rr, ks * 2 + 2 + (mi & 1), C::TP));
+              mma_f16(sc[bb][0], qa[ks], kb[0], kb[1]);
+              mma_f16(sc[bb][1], qa[ks], kb[2], kb[3]);
+              mma_f16(sd[0], qa[ks + 1], kc[0], kc[1]);
+              mma_f16(sd[1], qa[ks + 1], kc[2], kc[3]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sc[bb][nt][e] += sd[nt][e];
+          }
+#pragma unroll
+          for (int bb = 0; bb < C::NBH; ++bb) {
+            const int r0 = (hf * C::NBH + bb) * 16;
+            const int base = pos0 + r0;  // cache position of the block's row 0
+            const int nv = min(max(c1 - base, 0), 16);  // rows holding data for some row
+            if (nv == 0) continue;
+            float x[2][2][2], mt[2];
+            bool grow[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int nrow = min(max(Lr[u] - base, 0), 16);  // rows inside the pair's window
+              mt[u] = -INFINITY;
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                  x[u][nt][jj] = (nt * 8 + 2 * tig + jj) < nrow ? sc[bb][nt][2 * u + jj] : -INFINITY;
+                  mt[u] = fmaxf(mt[u], x[u][nt][jj]);
+                }
+              mt[u] = fmaxf(mt[u], __shfl_xor_sync(0xffffffffu, mt[u], 1));
+              mt[u] = fmaxf(mt[u], __shfl_xor_sync(0xffffffffu, mt[u], 2));
+              // a pair whose row ends before this block keeps mt = -inf: nothing to add
+              grow[u] = mt[u] != -INFINITY && mt[u] > m_run[u] + C::RESCALE_LOG2;
+            }
+            if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const float m_new = grow[u] ? mt[u] : m_run[u];
+                const float corr = grow[u] ? fast_exp2(m_run[u] - m_new) : 1.f;
+                m_run[u] = m_new;
+                l_run[u] *= corr;
+#pragma unroll
+                for (int n = 0; n < C::NT; ++n) {
+                  o[n][2 * u] *= corr;
+                  o[n][2 * u + 1] *= corr;
+                }
+              }
+            }
+            float pr[2][2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                  pr[u][nt][jj] = m_run[u] == -INFINITY ? 0.f : fast_exp2(x[u][nt][jj] - m_run[u]);
+                  l_run[u] += pr[u][nt][jj];
+                }
+            // the weights straight from the score fragments: A rows gid / gid + 8, k = positions
+            uint32_t pa[4];
+            pa[0] = h2_bits(__floats2half2_rn(pr[0][0][0], pr[0][0][1]));
+            pa[1] = h2_bits(__floats2half2_rn(pr[1][0][0], pr[1][0][1]));
+            pa[2] = h2_bits(__floats2half2_rn(pr[0][1][0], pr[0][1][1]));
+            pa[3] = h2_bits(__floats2half2_rn(pr[1][1][0], pr[1][1][1]));
+            const bool tail = nv < 16;
+            const uint32_t mk0 =
+                ((2 * tig < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 1 < nv) ? 0xffff0000u : 0u);
+            const uint32_t mk1 =
+                ((2 * tig + 8 < nv) ? 0x0000ffffu : 0u) | ((2 * tig + 9 < nv) ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int np = 0; np < C::NT / 2; ++np) {
+              uint32_t vb[4];
+              ldsm_x4_t(vb, sv + swz_off(r0 + (mi & 1) * 8 + rr, np * 2 + (mi >> 1), C::TP));
+              if (tail) {
+                vb[0] &= mk0;
+                vb[1] &= mk1;
+                vb[2] &= mk0;
+                vb[3] &= mk1;
+              }
+              mma_f16(o[2 * np], pa, vb[0], vb[1]);
+              mma_f16(o[2 * np + 1], pa, vb[2], vb[3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
       }
-      if (tig == 0) {
-        pr[D] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;  // natural-log units
-        pr[D + 1] = l_run;
+
+      // ---- the second half's states join the first's: half 1 hands its (m, l, o) over in
+      //      shared memory, thread by thread; half 0 combines them
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        l_run[u] += __shfl_xor_sync(0xffffffffu, l_run[u], 1);
+        l_run[u] += __shfl_xor_sync(0xffffffffu, l_run[u], 2);
       }
-    }
+      float* xb = xbuf + ps * C::XF * 32 + lane;  // element f at xb[f * 32]
+      if (hf == 1) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          xb[(u * (2 * C::NT + 2)) * 32] = m_run[u];
+          xb[(u * (2 * C::NT + 2) + 1) * 32] = l_run[u];
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n) {
+            xb[(u * (2 * C::NT + 2) + 2 + 2 * n) * 32] = o[n][2 * u];
+            xb[(u * (2 * C::NT + 2) + 3 + 2 * n) * 32] = o[n][2 * u + 1];
+          }
+        }
+      }
+      named_bar_sync(1, 32 * C::NCW);
+      if (hf == 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float m1 = xb[(u * (2 * C::NT + 2)) * 32];
+          const float l1 = xb[(u * (2 * C::NT + 2) + 1) * 32];
+          const float M = fmaxf(m_run[u], m1);
+          const float e0 = m_run[u] == -INFINITY ? 0.f : fast_exp2(m_run[u] - M);
+          const float e1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+          l_run[u] = l_run[u] * e0 + l1 * e1;
+          m_run[u] = M;
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n) {
+            o[n][2 * u] = o[n][2 * u] * e0 + xb[(u * (2 * C::NT + 2) + 2 + 2 * n) * 32] * e1;
+            o[n][2 * u + 1] = o[n][2 * u + 1] * e0 + xb[(u * (2 * C::NT + 2) + 3 + 2 * n) * 32] * e1;
+          }
+        }
+      }
+      named_bar_sync(1, 32 * C::NCW);  // half 1 may refill its slots for the next group
+
+      // ---- each of this thread's pairs (half 0): the output, or the chunk's partial (merged
+      //      afterwards by merge_kernel)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (!ok || !active || hf != 0) break;
+        if (!rv[u] || c0 >= Lr[u]) continue;
+        const float l = l_run[u];
+        if (!p.merge) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          float* orow = p.out + ((size_t)tr[u] * p.n_heads + hd[u]) * D;
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n)
+            *reinterpret_cast<float2*>(orow + n * 8 + 2 * tig) =
+                make_float2(o[n][2 * u] * inv, o[n][2 * u + 1] * inv);
+        } else {
+          float* prt = p.part + (((size_t)tr[u] * p.n_split + c) * p.n_heads + hd[u]) * (D + 2);
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n)
+            *reinterpret_cast<float2*>(prt + n * 8 + 2 * tig) =
+                make_float2(o[n][2 * u], o[n][2 * u + 1]);
+          if (tig == 0) {
+            prt[D] = m_run[u] == -INFINITY ? -INFINITY : m_run[u] * kLn2;  // natural-log units
+            prt[D + 1] = l;
+          }
+        }
+      }
+    }  // this chunk's work on the group
   }
   if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
 }

@@ -325,7 +325,7 @@ def _rows_off():
     return _env(GQA_F16_ROWS="off")
 
 
-@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("G", [1, 2, 4])
 def test_rows_grouped_long_runs(G):
     """Runs longer than a group (32 / G rows: 32 for G = 1), split at multiples of the group
     size, with a second sequence starting mid-group."""

@@ -86,8 +86,9 @@ def test_plan_selected_width_caps_chunks(gd):
 
 
 def test_plan_groups_rows_sharing_a_sequence(gd):
-    # 16 causal rows over one sequence (n_seq 1): two groups of 8 rows (G=4); chunks sized for
-    # 2 groups x 8 KV heads on two CTAs per SM: 16 * 8192 / 304 -> 432 -> 448 positions
+    # 16 causal rows over one sequence (n_seq 1): two groups of 8 rows (G=4: 2 sets of 16
+    # (row, head) pairs); chunks sized for 2 groups x 8 KV heads on two CTAs per SM:
+    # 16 * 8192 / 304 -> 432 -> 448 positions
     p = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1)
     assert p.row_group == 8 and p.chunk == 448 and p.n_split == 19
     assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 2)   # two group slots
