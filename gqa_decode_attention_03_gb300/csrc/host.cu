@@ -393,7 +393,8 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
   if (plan.merge && !plan.streamk && plan.row_group > 1) {
     // grouped rows: their partials are merged by merge_kernel, one CTA per (head, row)
-    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream);
+    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
+                          nullptr, 0, /*after_partials=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   }
   return GQA_OK;  // otherwise split rows were merged inside the kernel by their last CTA

@@ -23,21 +23,29 @@ cudaError_t ensure_smem(const void* fn, int bytes) {
 
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,
                          int n_tok, int n_heads, float* out, cudaStream_t s, const float* gate,
-                         long long gate_stride) {
+                         long long gate_stride, bool after_partials) {
   // one warp per (row, head), kMergeWarps per CTA
   const long long pairs = (long long)n_tok * n_heads;
-  const unsigned grid = static_cast<unsigned>((pairs + kMergeWarps - 1) / kMergeWarps);
-  const int threads = 32 * kMergeWarps;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>((pairs + kMergeWarps - 1) / kMergeWarps));
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.stream = s;
+  // Right after the kernel that writes the partials, as a programmatic dependent launch: the
+  // merge CTAs are scheduled while that kernel drains and wait (griddepcontrol.wait) for its
+  // completion and memory, so no launch gap separates the two.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_partials ? 1 : 0;
   if (head_dim == 64)
-    merge_kernel<64><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
-                                              gate_stride, out);
-  else if (head_dim == 128)
-    merge_kernel<128><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
-                                               gate_stride, out);
-  else
-    merge_kernel<256><<<grid, threads, 0, s>>>(part, n_valid, n_split, n_tok, n_heads, gate,
-                                               gate_stride, out);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, merge_kernel<64>, part, n_valid, n_split, n_tok, n_heads,
+                              gate, gate_stride, out);
+  if (head_dim == 128)
+    return cudaLaunchKernelEx(&cfg, merge_kernel<128>, part, n_valid, n_split, n_tok, n_heads,
+                              gate, gate_stride, out);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<256>, part, n_valid, n_split, n_tok, n_heads, gate,
+                            gate_stride, out);
 }
 
 }  // namespace gqa

@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps)
                  int n_tok, int n_heads, const float* __restrict__ gate, long long gate_stride,
                  float* __restrict__ out) {
   constexpr int DPL = D / 32;  // output dims per lane
+  // launched as a programmatic dependent of the partials' kernel: wait for that grid's
+  // completion and memory (a no-op after an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long pair = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (pair >= (long long)n_tok * n_heads) return;

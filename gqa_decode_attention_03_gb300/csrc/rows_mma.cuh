@@ -461,6 +461,9 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
     }  // this chunk's work on the group
   }
   if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
+  // this CTA's partials are written: the merge kernel launched after this one may be scheduled
+  // (it waits for this grid's completion and memory before reading anything)
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 }  // namespace gqa
