@@ -392,7 +392,7 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
                            : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
   if (plan.merge && !plan.streamk && plan.row_group > 1) {
-    // grouped rows: their partials are merged by merge_kernel, one CTA per (head, row)
+    // grouped rows: their partials are merged by merge_kernel, one warp per (row, head)
     e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
                           nullptr, 0, /*after_partials=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");

@@ -83,7 +83,7 @@ typedef struct gqa_plan {
                                  stream-K (CTAs, 1, 1) */
   int merge;         /* 1 when rows may be split: partials go to ws and are merged inside the
                         same kernel by whichever CTA finishes a row's KV head last, or (rows
-                        grouped by sequence) by a second kernel, one CTA per (head, row) */
+                        grouped by sequence) by a second kernel, one warp per (row, head) */
   int streamk;       /* 1: stream-K split (f16 caches): the (row, KV head, position) stream is
                         cut into equal shares, one per CTA of a persistent grid */
   int row_group;     /* rows one CTA serves from a shared K/V tile: > 1 when rows may share a
