@@ -400,6 +400,8 @@ def _oracle_pair(case, t, g):
                                 case.k_jl[sl], case.k_norms[sl], case.v_polar[sl],
                                 case.v_norms[sl], case.centroids, case.signs, case.qjl_scale,
                                 case.scale, L, seq_of=[0])
+    q = case.q[t:t + 1, g * G:(g + 1) * G]
+    if case.kind == "f16":
         return oracle.decode_f16(q, case.k[s:s + 1, :, g:g + 1], case.v[s:s + 1, :, g:g + 1], L,
                                  case.scale, seq_of=[0])
     ids = None if case.ids is None else case.ids[t:t + 1]
