@@ -12,7 +12,11 @@ When the KV read of a step is at least 4x the 129 MB L2 (the default workload re
 the K steps run back to back between two events ("inputs larger than L2"); smaller workloads get
 a 512 MiB device write between steps, outside each step's own pair of events.
 ``value`` = algorithmic bytes per step (KV rows read once per KV head + q + out) / mean step time.
-``e2e`` repeats the step through host buffers: pinned q and kv_len copied in, out copied back.
+``e2e`` repeats the step through host buffers: pinned q and kv_len copied in, out copied back
+every step.  For the large workloads it runs as a decode loop does, the copies on their own
+stream with two device buffer sets so that they overlap the neighbouring steps' kernels (the
+time is first upload to last download, over the steps); small workloads time one step at a
+time, copies included.
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded sample per step.
 """
 
@@ -215,6 +219,54 @@ def _kernel_name(case, plan):
     return name + (" (split-KV, merge fused)" if plan.merge else "")
 
 
+def _e2e_pipelined(torch, step, stream, x, out, q_h, qj_h, kv_h, out_h, steps):
+    """A decode loop through host buffers, as a server runs it: each step's inputs go up from
+    pinned memory and its output comes back, on a copy stream with two device buffer sets, so
+    that step i + 1's upload and step i's download overlap step i's and i + 1's kernels.
+    Returns milliseconds per step over the whole loop (first upload to last download)."""
+    copy = torch.cuda.Stream()
+    nb = 2
+    qd = [torch.empty_like(x["q"]) for _ in range(nb)]
+    kvd = [torch.empty_like(x["kv_len"]) for _ in range(nb)]
+    qjd = [torch.empty_like(x["q"]) if qj_h is not None else None for _ in range(nb)]
+    od = [torch.empty_like(out) for _ in range(nb)]
+    up = [torch.cuda.Event() for _ in range(nb)]
+    comp = [torch.cuda.Event() for _ in range(nb)]
+    down = [torch.cuda.Event() for _ in range(nb)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def upload(i):
+        j = i % nb
+        with torch.cuda.stream(copy):
+            if i >= nb:
+                copy.wait_event(comp[j])  # step i - nb has read this buffer set
+            qd[j].copy_(q_h, non_blocking=True)
+            if qjd[j] is not None:
+                qjd[j].copy_(qj_h, non_blocking=True)
+            kvd[j].copy_(kv_h, non_blocking=True)
+            up[j].record(copy)
+
+    torch.cuda.synchronize()
+    t0.record(copy)
+    upload(0)
+    for i in range(steps):
+        j = i % nb
+        if i + 1 < steps:
+            upload(i + 1)
+        stream.wait_event(up[j])
+        if i >= nb:
+            stream.wait_event(down[j])  # step i - nb's output has left this buffer
+        step(qd[j], kvd[j], qjd[j], od[j])
+        comp[j].record(stream)
+        with torch.cuda.stream(copy):
+            copy.wait_event(comp[j])
+            out_h.copy_(od[j], non_blocking=True)
+            down[j].record(copy)
+    t1.record(copy)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_gpu(args):
     import torch
     world, rank, local = _dist()
@@ -240,14 +292,15 @@ def run_gpu(args):
         x["scores"] = torch.from_numpy(scores).cuda()
         x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
 
-    def step(q=None, kv=None, q_jl=None):
+    def step(q=None, kv=None, q_jl=None, o=None):
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
+        o = out if o is None else o
         if case.kind == "tq":
             gd.attn_decode_tq(q, x["q_jl"] if q_jl is None else q_jl, x["k_polar"], x["k_jl"],
                               x["k_norms"], x["v_polar"], x["v_norms"], case.centroids,
                               x["signs"], case.qjl_scale, kv, scale=case.scale,
-                              seq_of=x["seq_of"], max_kv_len=max_len, out=out, ws=ws,
+                              seq_of=x["seq_of"], max_kv_len=max_len, out=o, ws=ws,
                               stream=stream)
             return
         if scores is not None:
@@ -255,12 +308,12 @@ def run_gpu(args):
                                 ids=x["ids"], stream=stream)
         if case.kind == "f16":
             gd.attn_decode_f16(q, x["k"], x["v"], kv, scale=case.scale, seq_of=x["seq_of"],
-                               max_kv_len=max_len, out=out, ws=ws, stream=stream)
+                               max_kv_len=max_len, out=o, ws=ws, stream=stream)
         else:
             gd.attn_decode_q8_sel(q, x["kq"], x["vq"], x["ksc"], x["vsc"], kv, ids=x["ids"],
                                   budget=None if x["ids"] is None else case.budget,
                                   scale=case.scale, seq_of=x["seq_of"], max_kv_len=max_len,
-                                  out=out, ws=ws, stream=stream)
+                                  out=o, ws=ws, stream=stream)
 
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
@@ -302,24 +355,27 @@ def run_gpu(args):
     qj_h = torch.from_numpy(case.q_jl).pin_memory() if case.kind == "tq" else None
     kv_h = torch.from_numpy(case.kv_len).pin_memory()
     out_h = torch.empty((T, H, D), dtype=torch.float32).pin_memory()
-    q_d, kv_d = torch.empty_like(x["q"]), torch.empty_like(x["kv_len"])
-    qj_d = torch.empty_like(x["q"]) if qj_h is not None else None
     Ke = min(K, 500)
-    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(Ke)]
-    for a, b in eve:
-        if not big:
+    if big:
+        e2e_ms = _e2e_pipelined(torch, step, stream, x, out, q_h, qj_h, kv_h, out_h, Ke)
+    else:
+        # small steps, L2 flushed before each: one step at a time, its copies in its events
+        q_d, kv_d = torch.empty_like(x["q"]), torch.empty_like(x["kv_len"])
+        qj_d = torch.empty_like(x["q"]) if qj_h is not None else None
+        eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(Ke)]
+        for a, b in eve:
             flush.zero_()
-        a.record(stream)
-        q_d.copy_(q_h, non_blocking=True)
-        if qj_d is not None:
-            qj_d.copy_(qj_h, non_blocking=True)
-        kv_d.copy_(kv_h, non_blocking=True)
-        step(q_d, kv_d, qj_d)
-        out_h.copy_(out, non_blocking=True)
-        b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eve]))
+            a.record(stream)
+            q_d.copy_(q_h, non_blocking=True)
+            if qj_d is not None:
+                qj_d.copy_(qj_h, non_blocking=True)
+            kv_d.copy_(kv_h, non_blocking=True)
+            step(q_d, kv_d, qj_d)
+            out_h.copy_(out, non_blocking=True)
+            b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eve]))
 
     ms, e2e_ms = max_over_ranks([float(step_ms.mean()), e2e_ms])
     if rank != 0:
@@ -373,6 +429,8 @@ def run_gpu(args):
         "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "h2d_bytes_per_step": h2d,
+                "timing": "pipelined loop: copies on a second stream, two buffer sets"
+                if big else "one step at a time, copies inside its events",
                 "d2h_bytes_per_step": int(T * H * D * 4)},
         "gpu_launches": int(K * (1 + (scores is not None) + _merge_launch(plan))),
         "clocks": clk.summary(),
