@@ -135,6 +135,8 @@ int head_split_for(int kind, int group) {
   const char* k = std::getenv("GQA_F16_KERNEL");
   const bool fma = kind == GQA_KIND_Q8 || (k && std::strcmp(k, "fma") == 0);
   if (!fma) return 1;
+  const int forced = env_int("GQA_HEAD_SPLIT");  // tuning sweeps: a divisor of the group size
+  if (forced > 0 && group % forced == 0) return forced;
   for (int hs = 1; hs <= group; ++hs)
     if (group % hs == 0 && group / hs <= 4) return hs;
   return group;
