@@ -105,8 +105,10 @@ gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int
     return fail(GQA_EINVAL, "n_heads %d / n_kv_heads %d", n_heads, n_kv_heads);
   if (n_heads % n_kv_heads)
     return fail(GQA_EINVAL, "n_heads %d is not a multiple of n_kv_heads %d", n_heads, n_kv_heads);
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
-    return fail(GQA_EINVAL, "head_dim %d not in {64, 128, 256}", head_dim);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256 &&
+      !(kind == GQA_KIND_TQ && head_dim == 32))
+    return fail(GQA_EINVAL, "head_dim %d not in {64, 128, 256} (TurboQuant: 32, 64, 128)",
+                head_dim);
   if (max_kv_len < 0) return fail(GQA_EINVAL, "max_kv_len %d < 0", max_kv_len);
   if (n_heads / n_kv_heads > 16)
     return fail(GQA_EUNSUPPORTED, "group size %d > 16", n_heads / n_kv_heads);

@@ -249,11 +249,15 @@ __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int
         for (int j = 0; j < nb; ++j) {
           const float ej = __shfl_sync(0xffffffffu, e, j);
           const float* ac = base + (c0 + j) * rec + lane * DPL;
+          if constexpr (DPL == 1) {  // D = 32: one dim a lane, 4-byte loads
+            a[0] = fmaf(ej, __ldcg(ac), a[0]);
+          } else {
 #pragma unroll
-          for (int k = 0; k < DPL; k += 2) {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(ac + k));
-            a[k] = fmaf(ej, v.x, a[k]);
-            a[k + 1] = fmaf(ej, v.y, a[k + 1]);
+            for (int k = 0; k < DPL; k += 2) {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(ac + k));
+              a[k] = fmaf(ej, v.x, a[k]);
+              a[k + 1] = fmaf(ej, v.y, a[k + 1]);
+            }
           }
         }
       }
@@ -263,8 +267,12 @@ __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int
 #pragma unroll
     for (int k = 0; k < DPL; ++k) a[k] *= inv;
     epi(a, head, lane);  // e.g. the inverse rotation of a rotated-space accumulator
+    if constexpr (DPL == 1) {
+      o[0] = a[0];
+    } else {
 #pragma unroll
-    for (int k = 0; k < DPL; k += 2) *reinterpret_cast<float2*>(o + k) = make_float2(a[k], a[k + 1]);
+      for (int k = 0; k < DPL; k += 2) *reinterpret_cast<float2*>(o + k) = make_float2(a[k], a[k + 1]);
+    }
   }
 }
 

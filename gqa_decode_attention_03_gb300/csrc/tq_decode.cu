@@ -74,17 +74,28 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
     float vn = 0.f;
     {
       uint32_t kp[PW], kj[JW], vp[PW];
+      if constexpr (PW >= 4) {  // a row's polar words: 16-byte loads (8 bytes at D = 32)
 #pragma unroll
-      for (int w = 0; w < PW; w += 4) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(tp.k_polar + row * PW + w));
-        kp[w] = u.x; kp[w + 1] = u.y; kp[w + 2] = u.z; kp[w + 3] = u.w;
-        const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(tp.v_polar + row * PW + w));
-        vp[w] = v4.x; vp[w + 1] = v4.y; vp[w + 2] = v4.z; vp[w + 3] = v4.w;
+        for (int w = 0; w < PW; w += 4) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(tp.k_polar + row * PW + w));
+          kp[w] = u.x; kp[w + 1] = u.y; kp[w + 2] = u.z; kp[w + 3] = u.w;
+          const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(tp.v_polar + row * PW + w));
+          vp[w] = v4.x; vp[w + 1] = v4.y; vp[w + 2] = v4.z; vp[w + 3] = v4.w;
+        }
+      } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(tp.k_polar + row * PW));
+        kp[0] = u.x; kp[1] = u.y;
+        const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(tp.v_polar + row * PW));
+        vp[0] = v2.x; vp[1] = v2.y;
       }
+      if constexpr (JW >= 2) {  // sign words: 8-byte loads (4 bytes at D = 32)
 #pragma unroll
-      for (int w = 0; w < JW; w += 2) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(tp.k_jl + row * JW + w));
-        kj[w] = u.x; kj[w + 1] = u.y;
+        for (int w = 0; w < JW; w += 2) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(tp.k_jl + row * JW + w));
+          kj[w] = u.x; kj[w + 1] = u.y;
+        }
+      } else {
+        kj[0] = __ldg(tp.k_jl + row);
       }
       const uint32_t kn = __ldg(tp.k_norms + row);
       vn = half_lo(__ldg(tp.v_norms + row));
@@ -183,7 +194,9 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
 }
 
 cudaError_t launch_tq_fma(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream) {
-  if (head_dim == 64)
+  if (head_dim == 32)
+    tq_decode_kernel<32><<<grid, 32 * kTqWarps, 0, stream>>>(tp);
+  else if (head_dim == 64)
     tq_decode_kernel<64><<<grid, 32 * kTqWarps, 0, stream>>>(tp);
   else
     tq_decode_kernel<128><<<grid, 32 * kTqWarps, 0, stream>>>(tp);
@@ -210,8 +223,8 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
                                      int n_seq, int n_heads, int n_kv_heads, int head_dim,
                                      int64_t cache_cap, int max_kv_len, void* ws, size_t ws_bytes,
                                      int32_t* err_word, cudaStream_t stream) {
-  if (head_dim != 64 && head_dim != 128)
-    return tq_fail(GQA_EINVAL, "attn_decode_tq: head_dim must be 64 or 128");
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128)
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: head_dim must be 32, 64 or 128");
   if (n_kv_heads <= 0 || n_heads % n_kv_heads)
     return tq_fail(GQA_EINVAL, "attn_decode_tq: n_heads must be a positive multiple of n_kv_heads");
   if (n_heads / n_kv_heads > gqa::kTqMaxGroup)
@@ -280,7 +293,9 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
   const char* kern = std::getenv("GQA_TQ_KERNEL");  // "fma": the CUDA-core kernel
   const int G = n_heads / n_kv_heads;
-  if (kern && std::strcmp(kern, "fma") == 0)
+  // head_dim 32 runs on the CUDA cores: a 32-dim polar row is 8 bytes, below the tensor-core
+  // kernel's 16-byte staging pieces
+  if (head_dim == 32 || (kern && std::strcmp(kern, "fma") == 0))
     (void)gqa::launch_tq_fma(head_dim, grid, tp, stream);
   else
     (void)gqa::launch_tq_mma(head_dim, G <= 4 ? 1 : 2, grid, tp, stream);

@@ -222,7 +222,8 @@ gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
  *                 the low half, f16 residual norm in the high half; v_norms likewise, f16 norm
  *                 low
  *   centroids     HOST fp32 [4]; signs device fp32 [head_dim] (the rotation's sign flips)
- *   head_dim 64 or 128 (the page's limit is 128), group size <= 8 (else GQA_EUNSUPPORTED).
+ *   head_dim 32, 64 or 128 (the page's set: a power of two, a multiple of 32, at most 128; 32
+ *   runs on the CUDA cores), group size <= 8 (else GQA_EUNSUPPORTED).
  *   Other arguments as attn_decode_f16; the workspace is attn_decode_workspace_bytes(...,
  *   GQA_KIND_TQ), zeroed once like attn_decode_f16's.
  */

@@ -68,7 +68,7 @@ def test_random_turboquant(i, kernel, monkeypatch):
     if kernel == "fma":
         monkeypatch.setenv("GQA_TQ_KERNEL", "fma")
     r, T, n_seq, seq_of, cap, L, chunk = _draw(9000 + i)
-    D = [64, 128][int(r.integers(0, 2))]
+    D = [32, 64, 128][int(r.integers(0, 3))]
     G = [1, 2, 3, 4, 5, 8][int(r.integers(0, 6))]
     Hk = int(r.integers(1, 3))
     c = W.make_tq_case(9100 + i, T, G * Hk, Hk, D, L, cache_cap=cap, seq_of=seq_of, n_seq=n_seq)

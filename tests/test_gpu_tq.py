@@ -56,7 +56,7 @@ def check(got, ref, tol=TOL_TQ):
     assert err.max() <= tol, f"max scaled error {err.max():.3e}"
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (12, 4), (16, 4), (20, 4), (32, 4)])
 def test_tq_group_sizes(D, H, Hk):
     c = W.make_tq_case(2100 + D + H, 2, H, Hk, D, [300, 77])
@@ -125,6 +125,16 @@ def test_tq_length_out_of_range_is_flagged():
                             seq_of=dev(c.seq_of), err=err)
     assert int(err.item()) & gd.ERR_KVLEN_RANGE
     check(got[0:1], ref_tq(c, rows=[0]))
+
+
+@pytest.mark.parametrize("chunk", [None, 128])
+def test_tq_head_dim_32_split_and_shared(chunk):
+    # head_dim 32 (the CUDA-core kernel): split rows, rows sharing a sequence, an empty row, a
+    # capacity that is not a multiple of 4
+    L = [901, 0, 130, 899]
+    c = W.make_tq_case(2206, 4, 8, 2, 32, L, cache_cap=902, seq_of=[0, 1, 1, 0], n_seq=2)
+    with forced_chunk(chunk):
+        check(run_tq(c), ref_tq(c))
 
 
 def test_tq_rejects_large_group():
