@@ -6,7 +6,10 @@
 // with n_kv <= budget keep every cell.  Scores are compared through an order-preserving fp32 ->
 // uint32 key.
 //
-// One CTA of 1024 threads per row.  The threshold key is found digit by digit, 8 bits per pass
+// One CTA of 1024 threads per row.  The row's block keys are staged in shared memory once when
+// the longest row fits kTopkSmemBlocks blocks; otherwise every pass reads them from global
+// memory (L2 after the first).  The
+// threshold key is found digit by digit, 8 bits per pass
 // over 4 passes: a 256-bin shared histogram counts the cells (4 per block, fewer for the tail)
 // whose key agrees with the digits fixed so far; a block-wide scan of the bins from the top
 // finds the digit at which the running count reaches the number of cells still needed.  The
@@ -22,6 +25,7 @@
 namespace gqa {
 
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkSmemBlocks = 49152;  // 192 KB of staged keys: n_kv up to 196607 cells
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
@@ -58,7 +62,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float* __restrict__ scores, long long stride,
                 const int32_t* __restrict__ kv_len, int budget, int max_kv_len,
-                int32_t* __restrict__ ids, int32_t* err) {
+                int smem_blocks, int32_t* __restrict__ ids, int32_t* err) {
+  extern __shared__ uint32_t s_key[];  // smem_blocks keys: the row's block keys, when they fit
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[32];
   __shared__ uint32_t s_digit, s_need;
@@ -75,6 +80,12 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   const float* row = scores + (size_t)t * stride;
   const int nfull = n_kv >> 2, nb = nfull + 1, tail = n_kv & 3;
+  const bool staged = nb <= smem_blocks;
+  if (staged) {
+    for (int b = tid; b < nb; b += kTopkThreads) s_key[b] = order_key(__ldg(row + b));
+    __syncthreads();
+  }
+  auto key = [&](int b) { return staged ? s_key[b] : order_key(__ldg(row + b)); };
 
   uint32_t prefix = 0, pmask = 0, need = (uint32_t)budget;
   for (int pass = 0; pass < 4; ++pass) {
@@ -82,7 +93,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     if (tid < 256) hist[tid] = 0u;
     __syncthreads();
     for (int b = tid; b < nb; b += kTopkThreads) {
-      const uint32_t k = order_key(__ldg(row + b));
+      const uint32_t k = key(b);
       const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
       if (w && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], w);
     }
@@ -107,7 +118,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
   uint32_t gt = 0, eq = 0;
   for (int b = b0; b < b1; ++b) {
-    const uint32_t k = order_key(__ldg(row + b));
+    const uint32_t k = key(b);
     const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
     if (k > T) gt += w;
     else if (k == T) eq += w;
@@ -118,7 +129,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   uint32_t off = block_exclusive_scan(gt + eq_take, wsum, &total);
   uint32_t left = eq_take;
   for (int b = b0; b < b1; ++b) {
-    const uint32_t k = order_key(__ldg(row + b));
+    const uint32_t k = key(b);
     const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
     uint32_t take = 0;
     if (k > T) {
@@ -135,7 +146,8 @@ __global__ void __launch_bounds__(kTopkThreads)
 }  // namespace gqa
 
 namespace gqa {
-void set_last_error(const char* msg);  // host.cu: the text gqa_last_error() returns
+void set_last_error(const char* msg);          // host.cu: the text gqa_last_error() returns
+cudaError_t ensure_smem(const void* fn, int bytes);  // launch_util.cu: the opt-in, once
 }
 
 static gqa_status topk_fail(gqa_status s, const char* msg) {
@@ -154,8 +166,18 @@ extern "C" gqa_status attn_select_topk(const float* block_scores, int64_t score_
     return topk_fail(GQA_EINVAL, "attn_select_topk: a required pointer is NULL");
   if (score_stride < (int64_t)max_kv_len / 4 + 1)
     return topk_fail(GQA_EINVAL, "attn_select_topk: score_stride < max_kv_len / 4 + 1");
-  gqa::topk_kernel<<<n_tok, gqa::kTopkThreads, 0, stream>>>(
-      block_scores, (long long)score_stride, kv_len, budget, max_kv_len, ids, err_word);
+  // the staged keys: room for the longest row's blocks if they fit, else none (a row stages
+  // only when its own block count fits the room launched)
+  const int nb_max = max_kv_len / 4 + 1;
+  const int smem_blocks = nb_max <= gqa::kTopkSmemBlocks ? nb_max : 0;
+  if (smem_blocks > 0) {  // the opt-in past 48 KB (static + dynamic), once, at the largest size
+    const cudaError_t e = gqa::ensure_smem(reinterpret_cast<const void*>(gqa::topk_kernel),
+                                           gqa::kTopkSmemBlocks * sizeof(uint32_t));
+    if (e != cudaSuccess) return topk_fail(GQA_ECUDA, cudaGetErrorString(e));
+  }
+  gqa::topk_kernel<<<n_tok, gqa::kTopkThreads, (size_t)smem_blocks * sizeof(uint32_t), stream>>>(
+      block_scores, (long long)score_stride, kv_len, budget, max_kv_len, smem_blocks, ids,
+      err_word);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return topk_fail(GQA_ECUDA, cudaGetErrorString(e));
   return GQA_OK;

@@ -58,3 +58,18 @@ def test_topk_feeds_the_selected_int8_path():
     assert np.array_equal(ids.cpu().numpy(), case.ids)
     got = run_case(case, ids=ids).cpu().numpy()
     assert_close(got, oracle_ref(case), TOL_Q8, "topk -> q8_sel")
+
+
+@pytest.mark.parametrize("max_kv", [49147, 60001, 196604, 196608, 200003])
+def test_topk_staged_and_unstaged_rows(max_kv):
+    """Rows whose block keys fit the shared-memory staging (max_kv_len / 4 + 1 <= 49152 blocks,
+    past the 48 KB that needs no opt-in) and rows past it, which read the keys from global
+    memory every pass."""
+    kv_len = np.array([max_kv, max_kv - 3, 20000, 700, 0], np.int32)
+    stride = max_kv // 4 + 1
+    scores = W.make_block_scores(720 + max_kv % 97, len(kv_len), stride, 29)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _gd().attn_select_topk(dev(scores), dev(kv_len), 2048, max_kv_len=max_kv,
+                                 err=err).cpu().numpy()
+    assert int(err.item()) == 0
+    assert np.array_equal(got, _oracle_ids(scores, kv_len, 2048))
