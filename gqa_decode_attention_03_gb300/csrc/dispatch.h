@@ -7,6 +7,7 @@
 #include "gqa_decode.h"
 #include "partial_kernel.cuh"
 #include "rows_mma.cuh"
+#include "rows_umma.cuh"
 #include "streamk_mma.cuh"
 
 namespace gqa {
@@ -22,6 +23,7 @@ int head_split_for(int kind, int group);
 int stage_rows(int kind, int head_dim);
 bool use_streamk(int kind, int n_tok);  // f16 on the tensor cores with few enough rows
 int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim);
+bool rows_on_umma();  // grouped rows on the tcgen05 kernel (default) or the mma.sync one
 
 // Defined in the inst_*.cu files, one per (cache kind, head_dim).
 cudaError_t launch_partial_f16_d64(Variant v, const CUtensorMap&, const CUtensorMap&,

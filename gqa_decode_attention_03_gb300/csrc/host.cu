@@ -85,6 +85,8 @@ int env_int(const char* name) {
 // bandwidth on both the mixed-length and the uniform batch.
 constexpr int kCtasPerSm = 2;
 constexpr long long kMaxChunk = 8192;
+// The tcgen05 row kernel holds ~194 KB of shared memory: one CTA per SM.
+constexpr int kUmmaRowsCtasPerSm = 1;
 // Rows whose whole visited list is at most this many bytes of K/V (and scales) are not split:
 // one CTA streams them in a few microseconds, less than a split's merge step costs.
 constexpr long long kMinSplitBytes = 128 << 10;
@@ -155,8 +157,17 @@ bool use_streamk(int kind, int n_tok) {
   return m && std::strcmp(m, "streamk") == 0;
 }
 
-// Rows sharing a sequence are grouped (32 / group size rows per CTA) on the f16 tensor-core
-// path when the caller's cache holds fewer sequences than there are rows.
+// Grouped rows run on the tcgen05 kernel (rows_umma.cuh) unless GQA_F16_ROWS=mma asks for the
+// mma.sync kernel (rows_mma.cuh; comparison and parity cross-check).
+bool rows_on_umma() {
+  const char* r = std::getenv("GQA_F16_ROWS");
+  return !(r && std::strcmp(r, "mma") == 0);
+}
+
+// Rows sharing a sequence are grouped on the f16 tensor-core path when the caller's cache holds
+// fewer sequences than there are rows: 64 / group size rows per CTA on the tcgen05 kernel (its
+// 128 MMA rows hold each (row, head) pair twice, once per position half), 32 / group size on the
+// mma.sync kernel.
 int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
   if (kind != GQA_KIND_F16 || n_seq >= n_tok || use_streamk(kind, n_tok)) return 1;
   const char* k = std::getenv("GQA_F16_KERNEL");
@@ -164,7 +175,7 @@ int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
   const char* r = std::getenv("GQA_F16_ROWS");  // "off": one CTA per row (tests, comparison)
   if (r && std::strcmp(r, "off") == 0) return 1;
   if (head_dim == 256 || (group != 1 && group != 2 && group != 4 && group != 8)) return 1;
-  return 32 / group;  // 2 pair sets x 16 (row, head) pairs
+  return (rows_on_umma() ? 64 : 32) / group;
 }
 
 int stage_rows(int kind, int head_dim) {
@@ -207,7 +218,7 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
     num_sms = current_sm_count(&st);
     if (num_sms <= 0) return st != GQA_OK ? st : fail(GQA_ECUDA, "no SM count");
   }
-  const int tile = gqa::stage_rows(kind, head_dim);
+  int tile = gqa::stage_rows(kind, head_dim);
   const long long nmax = budget > 0 ? std::min(max_kv_len, budget) : max_kv_len;
   if (gqa::use_streamk(kind, n_tok)) {
     // equal shares of the whole stream, at least 256 positions each, two CTAs per SM at most
@@ -236,9 +247,12 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   const long long groups =
       rgroup > 1 ? std::max<long long>((n_tok + rgroup - 1) / rgroup, std::min(n_seq, n_tok)) : n_tok;
   plan->row_group = rgroup;
+  const bool umma_rows = rgroup > 1 && gqa::rows_on_umma();
+  if (umma_rows) tile = 64;  // the tcgen05 row kernel's tile, whatever head_dim
   const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
   const bool tq = kind == GQA_KIND_TQ;
-  const long long slots = (long long)(tq ? kTqCtasPerSm : kCtasPerSm) * num_sms;
+  const long long slots =
+      (long long)(tq ? kTqCtasPerSm : umma_rows ? kUmmaRowsCtasPerSm : kCtasPerSm) * num_sms;
   long long chunk = (units + slots - 1) / slots;
   chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
   // a split chunk spans at least two stages, so its pipeline has something to overlap

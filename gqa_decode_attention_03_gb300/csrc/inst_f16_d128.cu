@@ -4,6 +4,7 @@
 // cross-check).
 #include "dispatch.h"
 #include "rows_mma.cuh"
+#include "rows_umma.cuh"
 #include "streamk_mma.cuh"
 
 namespace gqa {
@@ -51,6 +52,14 @@ cudaError_t launch_streamk_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv
 
 cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
                                 const PartialParams& p, dim3 grid, cudaStream_t s) {
+  if (rows_on_umma()) {
+    using U = UmmaRowsCfg<128>;
+    const void* fu = reinterpret_cast<const void*>(&umma_rows_kernel<128>);
+    cudaError_t e = ensure_smem(fu, U::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    umma_rows_kernel<128><<<grid, U::THREADS, U::SMEM_BYTES, s>>>(tk, tv, p);
+    return cudaGetLastError();
+  }
   using C = RowsCfg<128>;
   const void* fn = reinterpret_cast<const void*>(&partial_mma_rows_kernel<128>);
   cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);

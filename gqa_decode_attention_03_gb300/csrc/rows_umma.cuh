@@ -1,0 +1,489 @@
+// rows_umma.cuh -- row-grouped f16 decode attention on the fifth-generation tensor cores.
+//
+// The rows of a causal prefill chunk (flash_attention_tq.metal's per-query window: row r at
+// position p attends to [0, p]) or the decode rows of one sequence read the same K/V.  One CTA
+// serves a group of up to 64 / G such rows for one KV head and one chunk of positions, so every
+// K/V tile is read from HBM once for all of the group's (row, head) pairs (attention_gqa.metal's
+// "load K/V once, reuse across the group", widened from the heads of a group to the rows of a
+// sequence).  The group's 64 pairs are the M = 64 rows of the MMAs.
+//
+// Per 64-position tile, flash-attention style:
+//   S  = Q . K^T    M = 64 pairs, N = 64 positions, K = D: Q (f16, scale * log2 e folded in) and
+//                   the K tile K-major in shared memory; S in TMEM (row i in lane
+//                   32 (i / 16) + i % 16).
+//   softmax         two threads per pair: thread (warp w, lane l) owns pair 16 w + l % 16 and
+//                   the tile's positions [32 h, 32 h + 32), h = l / 16 (one tcgen05.ld 16x32bx2).
+//                   It masks positions at or past its row's length; the two halves' maxima meet
+//                   by one shuffle, so both keep the same running max, and each keeps its own
+//                   part of the running sum.  The max moves lazily (only when a tile's max
+//                   exceeds it by more than 2^8, so p <= 256); when it moves, each thread
+//                   rescales its half of the pair's O row in TMEM (ld, scale, st) after the
+//                   previous tile's P.V has completed.
+//   O += P . V      P (f16, written by the softmax threads into shared memory, K-major) times the
+//                   V tile read MN-major (N = D contiguous), accumulated in TMEM.
+// Three S buffers in TMEM and three P buffers in shared memory let the tensor cores run up to two
+// tiles' S ahead of the softmax.  K/V tiles stream through a four-stage TMA ring;
+// the group's fp32 q arrives first, by bulk copies from the producer into a staging area, and is
+// converted there.  V rows past the group's longest row are zeroed in shared memory before the
+// P.V MMA (P is zero there, but cache garbage could be NaN).  At the end of the chunk the O rows
+// go through shared memory so that the records (or outputs) are written row by row, coalesced.
+//
+// Warps: 0-3 softmax and epilogue, 4 TMA producer, 5 MMA issuer (one elected lane) and TMEM
+// owner.  The issuer polls its two inputs and issues whichever MMA is ready first: S(i) once
+// K/V tile i has landed (and S buffer i % 3 is free), P.V(i) once P(i) is written.  Barriers:
+// full/empty per stage (TMA <-> MMA), q_land (q staged), q_full (softmax wrote the group's Q),
+// s_full per S buffer (MMA -> softmax; S(i) is issued after P.V(i - 3), so it also frees P
+// buffer i % 3), p_full per P buffer (softmax -> MMA), pv_done per P buffer (MMA -> softmax: O
+// final for a rescale or the epilogue), x_free (softmax -> producer: the staging area is free for
+// the next group's q).  Every wait is bounded; a wait that runs out flags GQA_ERR_TIMEOUT and its
+// role stops, and before TMEM is freed the issuer waits for all of its MMAs to complete.
+//
+// MMA cost (measured on GB300, one thread issuing back to back): M64 N64 K16 ~56 cycles, M64
+// N128 K16 ~70, M128 N256 K16 ~133 (the dense peak).  M = 64 half-fills the tensor core, which a
+// group of 64 pairs cannot avoid; the kernel is bound by its K/V stream and the softmax, not the
+// MMAs.
+//
+// Groups, slots, the per-row bookkeeping (n_valid, empty rows) and the partial format are those
+// of the mma.sync row kernel (rows_mma.cuh); split rows are merged afterwards by merge_kernel.
+#pragma once
+
+#include "rows_mma.cuh"
+#include "umma.cuh"
+
+namespace gqa {
+
+template <int D>
+struct UmmaRowsCfg {
+  static constexpr int M = 64;                     // MMA rows: (row, head) pairs per group
+  static constexpr int NP = M;
+  static constexpr int TP = 64;                    // positions per tile (one TMA box high)
+  static constexpr int CPT = TP / 2;               // score columns per softmax thread and tile
+  static constexpr int NBOX = D / 64;              // 128-byte boxes across D
+  static constexpr int BOX_BYTES = TP * 128;       // one box: TP rows x 128 bytes
+  static constexpr int KV_BYTES = NBOX * BOX_BYTES;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K boxes, then V boxes
+  static constexpr int NST = 4;
+  static constexpr int Q_BOX = M * 128;            // Q: [box][64 pairs][128 bytes]
+  static constexpr int Q_BYTES = NBOX * Q_BOX;
+  static constexpr int P_BYTES = M * TP * 2;       // P: [64 pairs][64 positions] f16
+  static constexpr int NPB = 3;                    // S buffers (TMEM) and P buffers (smem)
+  static constexpr int S_COL = 0, O_COL = NPB * TP;
+  static constexpr int TMEM_COLS = NPB * TP + D <= 256 ? 256 : 512;
+  static constexpr int KS_S = D / 16;              // k steps of S = Q.K^T
+  static constexpr int KS_O = TP / 16;             // k steps of O += P.V
+  static constexpr int NSW = 4, PRODUCER = 4, ISSUER = 5;
+  static constexpr int THREADS = 192;
+  static constexpr int NBAR = 2 * NST + 3 + 3 * NPB + 1;
+  // staging of the group's fp32 q, then the epilogue's exchange: records [NP][D + 2] + flags
+  static constexpr int X_BYTES = cmax(NP * D * 4, NP * (D + 2) * 4 + NP * 4);
+  static constexpr int BAR_OFF = NST * STAGE_BYTES + Q_BYTES + NPB * P_BYTES;
+  static constexpr int X_OFF = align_up(BAR_OFF + NBAR * 8 + 4, 128);  // bulk copies, float4
+  static constexpr int SMEM_BYTES = 1024 + X_OFF + X_BYTES;
+  static constexpr float RESCALE_LOG2 = 8.f;
+  static_assert(D == 64 || D == 128, "row grouping serves head_dim 64 and 128");
+  static_assert(P_BYTES == M * 128, "P rows are one 128-byte box row");
+  static_assert(CPT == 32, "one 32-column TMEM load per thread and tile");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(STAGE_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && P_BYTES % 1024 == 0,
+                "swizzled tiles start on 1024-byte atoms");
+  static_assert(BAR_OFF % 8 == 0 && X_OFF % 16 == 0, "barrier and staging alignment");
+};
+
+template <int D>
+__global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
+    umma_rows_kernel(const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const PartialParams p) {
+  using C = UmmaRowsCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const int c = blockIdx.x, g = blockIdx.y, slot = blockIdx.z, nslots = gridDim.z;
+  const int G = p.group;    // 1, 2, 4 or 8
+  const int R = C::NP / G;  // rows per group at most
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = c * p.chunk;
+
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  uint8_t* stages = smem_raw + pad;
+  uint8_t* sQ = stages + C::NST * C::STAGE_BYTES;
+  uint8_t* sP = sQ + C::Q_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sP + C::NPB * C::P_BYTES);
+  uint64_t* empty = full + C::NST;
+  uint64_t* q_full = empty + C::NST;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* p_full = s_full + C::NPB;
+  uint64_t* pv_done = p_full + C::NPB;
+  uint64_t* drain = pv_done + C::NPB;
+  uint64_t* q_land = drain + 1;
+  uint64_t* x_free = q_land + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(x_free + 1);
+  uint8_t* sX = stages + C::X_OFF;  // 128-byte aligned
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(q_full, 32 * C::NSW);
+    for (int i = 0; i < C::NPB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 32 * C::NSW);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    mbar_init(q_land, 1);
+    mbar_init(x_free, 32 * C::NSW);
+    mbar_init_fence();
+  }
+  if (threadIdx.x == 32 && p.seq_of)  // the row tables' first lines, for the group search
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p.seq_of) : "memory");
+  if (threadIdx.x == 64) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.kv_len) : "memory");
+  if (warp == C::ISSUER) tmem_alloc(tmem_holder, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  // Every warp walks the same groups (k = slot, slot + nslots, ...) in the same order.
+  int scan_t = 0, scan_cnt = 0;
+  bool ok = true;
+
+  if (warp == C::PRODUCER) {  // ---- TMA producer: lane 0 issues, the warp walks the groups
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    int it = 0, gn = 0;
+    for (int k = slot; ok; k += nslots) {
+      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      if (t0 < 0) break;
+      const RowGroup gr = rows_group(p, t0, R, lane);
+      const int c1 = min(c0 + p.chunk, gr.lmax);
+      if (c1 <= c0) continue;
+      // the group's fp32 q first (one bulk copy per row: its G heads are contiguous), into the
+      // staging area once the previous group's epilogue is done with it
+      if (gn > 0) ok = __all_sync(0xffffffffu, mbar_wait(x_free, (gn - 1) & 1));
+      if (!ok) break;
+      ++gn;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_land, gr.nr * G * D * 4);
+        for (int jj = 0; jj < gr.nr; ++jj)
+          bulk_load(sX + jj * G * D * 4, p.q + ((size_t)(t0 + jj) * p.n_heads + g * G) * D,
+                    G * D * 4, q_land);
+      }
+      const int zb = gr.s * static_cast<int>(p.cache_cap);
+      for (int pos = c0; pos < c1; pos += C::TP, ++it) {
+        const int st = it % C::NST;
+        if (it >= C::NST &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((it / C::NST) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+          uint8_t* sk = stages + st * C::STAGE_BYTES;
+          uint8_t* sv = sk + C::KV_BYTES;
+#pragma unroll
+          for (int bx = 0; bx < C::NBOX; ++bx) {
+            tma_load_3d(sk + bx * C::BOX_BYTES, &tmK, bx * 64, g, zb + pos, &full[st]);
+            tma_load_3d(sv + bx * C::BOX_BYTES, &tmV, bx * 64, g, zb + pos, &full[st]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      if (!ok) flag_error(p.err, GQA_ERR_TIMEOUT);
+      for (int st = 0; st < C::NST && st < it; ++st) {  // the last load of each stage lands
+        const int last = st + ((it - 1 - st) / C::NST) * C::NST;
+        if (!mbar_wait(&full[st], (last / C::NST) & 1)) flag_error(p.err, GQA_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == C::ISSUER) {  // ---- MMA issuer: lane 0 issues, the warp walks the groups
+    constexpr uint32_t kIdS = umma_idesc_f16(C::M, C::TP, false);
+    constexpr uint32_t kIdO = umma_idesc_f16(C::M, D, true);
+    const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
+    int it = 0, qn = 0;
+    for (int k = slot; ok; k += nslots) {
+      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      if (t0 < 0) break;
+      const RowGroup gr = rows_group(p, t0, R, lane);
+      const int c1 = min(c0 + p.chunk, gr.lmax);
+      if (c1 <= c0) continue;
+      const int ntile = (c1 - c0 + C::TP - 1) / C::TP;
+      ok = __all_sync(0xffffffffu, mbar_wait(q_full, qn & 1));
+      ++qn;
+      if (!ok) break;
+      if (lane == 0) {
+        // S(js) may go once tile js has landed and P.V(js - NPB) was issued (S buffer js % NPB
+        // is free then: its softmax wrote P(js - NPB)); P.V(jp) once P(jp) is written
+        int js = 0, jp = 0;
+        uint32_t spins = 0;
+        while (jp < ntile) {
+          bool issued = false;
+          if (js < ntile && js < jp + C::NPB) {
+            const int i = it + js, st = i % C::NST;
+            if (mbar_test(&full[st], (i / C::NST) & 1)) {
+              tc_fence_after();
+              const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < C::KS_S; ++kk) {
+                const uint32_t ko = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                const uint32_t qo = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+                umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
+                         umma_desc_sw128(q_addr + qo, 16, 1024),
+                         umma_desc_sw128(sk + ko, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&s_full[i % C::NPB]);
+              ++js;
+              issued = true;
+            }
+          }
+          if (jp < js) {
+            const int i = it + jp;
+            if (mbar_test(&p_full[i % C::NPB], (i / C::NPB) & 1)) {
+              tc_fence_after();
+              const uint32_t sv = smem_addr(stages + (i % C::NST) * C::STAGE_BYTES + C::KV_BYTES);
+              const uint32_t pa = p_addr + (i % C::NPB) * C::P_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < C::KS_O; ++kk)
+                umma_f16(tbase + C::O_COL, umma_desc_sw128(pa + kk * 32, 16, 1024),
+                         umma_desc_sw128(sv + kk * 2048, C::BOX_BYTES, 1024), kIdO,
+                         (jp == 0 && kk == 0) ? 0u : 1u);
+              umma_commit(&empty[i % C::NST]);
+              umma_commit(&pv_done[i % C::NPB]);
+              ++jp;
+              issued = true;
+            }
+          }
+          if (issued) {
+            spins = 0;
+          } else if (++spins > 16u * kSpinLimit) {  // nothing ready for far too long
+            ok = false;
+            break;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      it += ntile;
+    }
+    if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
+    // every MMA this thread issued has completed before TMEM is freed
+    if (lane == 0) {
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0)) flag_error(p.err, GQA_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else {  // ---- softmax warpgroup: two threads per pair (position halves of each tile)
+    const int h = lane >> 4;                 // tile positions [32 h, 32 h + 32)
+    const int i = warp * 16 + (lane & 15);   // pair = MMA row
+    const int jr = i / G;
+    const uint32_t t_q = tbase + (static_cast<uint32_t>(warp * 32) << 16);  // lane quadrant
+    float* xo = reinterpret_cast<float*>(sX);  // exchange: records [NP][D + 2], then flags
+    int* xw = reinterpret_cast<int*>(xo + C::NP * (D + 2));
+    // a completed phase is seen at once by a test; a pending one is waited for (bounded)
+    auto wait = [](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_test(bar, parity) || mbar_wait(bar, parity));
+    };
+    int it = 0, qn = 0;
+    for (int k = slot; ok; k += nslots) {
+      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      if (t0 < 0) break;
+      const RowGroup gr = rows_group(p, t0, R, lane);
+      const bool seq_ok = gr.s >= 0 && gr.s < p.n_seq;
+      const int c1 = min(c0 + p.chunk, gr.lmax);
+      if (c == 0 && warp == 0) {  // per-row bookkeeping: flags, chunk counts, empty rows
+        for (int jb = 0; jb < gr.nr; jb += 32) {
+          int err = 0;
+          const int L = jb + lane < gr.nr ? rows_len(p, t0 + jb + lane, seq_ok, &err) : 0;
+          if (jb + lane < gr.nr) {
+            if (err && g == 0) flag_error(p.err, err);
+            if (g == 0 && p.merge) p.n_valid[t0 + jb + lane] = (L + p.chunk - 1) / p.chunk;
+          }
+          for (int jj = 0; jj < 32 && jb + jj < gr.nr; ++jj) {
+            if (__shfl_sync(0xffffffffu, L, jj) != 0) continue;  // empty row: zeros
+            for (int e = lane; e < G * D; e += 32)
+              p.out[((size_t)(t0 + jb + jj) * p.n_heads + g * G + e / D) * D + e % D] = 0.f;
+          }
+        }
+      }
+      if (c1 <= c0) continue;  // the same decision as the producer's and the issuer's
+      const int ntile = (c1 - c0 + C::TP - 1) / C::TP;
+      const bool rv = jr < gr.nr;  // this pair is a real row
+      const int t = t0 + (rv ? jr : 0);
+      int dummy = 0;
+      const int Lp = rv ? rows_len(p, t, seq_ok, &dummy) : 0;
+      // chunk positions [0, lim0) are the pair's, counted from this thread's half of a tile
+      const int lim0 = min(Lp, c0 + p.chunk) - c0 - C::CPT * h;
+
+      // ---- Q: the staged fp32 q [pair][D] to f16 with scale * log2(e), 128-byte swizzled:
+      //      thread r takes float4 pieces r, r + 128, ... (all loads first).  Pad pairs get
+      //      zeros (their staging is not loaded).  No P is written before S(0), which waits for
+      //      every thread's q_full arrival.
+      ok = wait(q_land, qn & 1);
+      if (!ok) break;
+      {
+        constexpr int NQ = C::NP * D / 4 / (32 * C::NSW);  // float4 pieces per thread
+        const float4* qs = reinterpret_cast<const float4*>(sX);
+        float4 v[NQ];
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+          const int f = threadIdx.x + u * 32 * C::NSW, qr = f / (D / 4);
+          v[u] = qr / G < gr.nr ? qs[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float sc = p.scale_log2;
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+          const int f = threadIdx.x + u * 32 * C::NSW, qr = f / (D / 4), c4 = f % (D / 4);
+          const int ch = c4 >> 1;  // 16-byte chunk of the f16 row
+          uint2 hv;
+          hv.x = h2_bits(__floats2half2_rn(v[u].x * sc, v[u].y * sc));
+          hv.y = h2_bits(__floats2half2_rn(v[u].z * sc, v[u].w * sc));
+          *reinterpret_cast<uint2*>(sQ + (ch >> 3) * C::Q_BOX + qr * 128 +
+                                    (((ch & 7) ^ (qr & 7)) << 4) + (c4 & 1) * 8) = hv;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(q_full);
+      ++qn;
+
+      float m_run = -INFINITY, l_run = 0.f;  // m_run: the pair's (both halves'); l_run: this half's
+      for (int j = 0; j < ntile; ++j) {
+        const int it_j = it + j, b = it_j % C::NPB;
+        // S(it_j) complete; so is P.V(it_j - NPB), issued before it: P buffer b is free
+        ok = wait(&s_full[b], (it_j / C::NPB) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld16x2<C::CPT>(t_q + C::S_COL + b * C::TP, sr);
+        tmem_ld_wait();
+        const int lim = lim0 - j * C::TP;  // columns [0, lim) of this thread's 32
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          mq[e & 3] = fmaxf(mq[e & 3], e < lim ? __uint_as_float(sr[e]) : -INFINITY);
+        float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the pair's other half
+        const bool grow = mt > m_run + C::RESCALE_LOG2;  // false while mt = -inf
+        const bool resc = grow && m_run != -INFINITY;     // O holds weight: rescale it
+        if (__any_sync(0xffffffffu, resc)) {
+          // O must be final for tile it_j - 1 (this warp's lanes rescale their rows together)
+          ok = wait(&pv_done[(it_j - 1) % C::NPB], ((it_j - 1) / C::NPB) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const float corr = resc ? ex2_approx(m_run - mt) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 64; ++cc) {  // this half's D / 2 columns, 32 at a time
+            uint32_t o[32];
+            tmem_ld16x2<D / 2>(t_q + C::O_COL + cc * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st16x2<D / 2>(t_q + C::O_COL + cc * 32, o);
+          }
+          tmem_st_wait();
+          if (resc) l_run *= corr;
+        }
+        if (grow) m_run = mt;
+        const float mu = m_run == -INFINITY ? 0.f : m_run;  // lim <= 0 there: all weights 0
+        float lq[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t ph[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float w0 = e < lim ? ex2_approx(__uint_as_float(sr[e]) - mu) : 0.f;
+          const float w1 = e + 1 < lim ? ex2_approx(__uint_as_float(sr[e + 1]) - mu) : 0.f;
+          lq[(e >> 1) & 3] += w0 + w1;
+          ph[e >> 1] = h2_bits(__floats2half2_rn(w0, w1));
+        }
+        l_run += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+        // P row i, this half's 4 chunks of 8 positions
+        uint8_t* prow = sP + b * C::P_BYTES + i * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(prow + (((4 * h + q) ^ (i & 7)) << 4)) =
+              make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        // V rows past the group's longest row may hold cache garbage: zero them (P is 0 there)
+        const int nv = gr.lmax - (c0 + j * C::TP);
+        if (nv < C::TP) {
+          const int st = it_j % C::NST;
+          ok = wait(&full[st], (it_j / C::NST) & 1);
+          if (!ok) break;
+          uint8_t* sv = stages + st * C::STAGE_BYTES + C::KV_BYTES;
+          const int n16 = (C::TP - nv) * 8;  // 16-byte pieces per box
+          for (int e = threadIdx.x; e < C::NBOX * n16; e += 32 * C::NSW) {
+            const int bx = e / n16, vr = nv + (e % n16) / 8, ch = e % 8;
+            *reinterpret_cast<uint4*>(sv + bx * C::BOX_BYTES + vr * 128 + ch * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[b]);
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O final after the last tile's P.V; each thread moves its half of the
+      //      pair's O row into the exchange area, then the warpgroup writes the records (or
+      //      outputs) row by row, coalesced
+      const int last = it + ntile - 1;
+      ok = wait(&pv_done[last % C::NPB], (last / C::NPB) & 1);
+      it += ntile;
+      if (!ok) break;
+      tc_fence_after();
+      const float l = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+      const float f = p.merge ? 1.f : (l > 0.f ? 1.f / l : 0.f);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t o[32];
+        tmem_ld16x2<D / 2>(t_q + C::O_COL + cc * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          xo[i * (D + 2) + h * (D / 2) + cc * 32 + e] = __uint_as_float(o[e]) * f;
+      }
+      if (h == 0) {
+        xo[i * (D + 2) + D] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;  // natural log
+        xo[i * (D + 2) + D + 1] = l;
+        xw[i] = rv && c0 < Lp;  // the pair has positions in this chunk
+      }
+      named_bar_sync(1, 32 * C::NSW);
+      // the records (merge) or output rows, coalesced: a row's G heads are contiguous in both
+      // (G (D + 2) floats of records, G D floats of output), copied as float2
+      if (p.merge) {
+        const int per_row = G * (D + 2) / 2;  // float2 pieces of a row's records
+        for (int row = warp; row < gr.nr; row += C::NSW) {
+          if (!xw[row * G]) continue;
+          const float2* src = reinterpret_cast<const float2*>(xo) + row * per_row;
+          float2* dst = reinterpret_cast<float2*>(
+              p.part + (((size_t)(t0 + row) * p.n_split + c) * p.n_heads + g * G) * (D + 2));
+#pragma unroll 4
+          for (int e = lane; e < per_row; e += 32) dst[e] = src[e];
+        }
+      } else {
+        for (int q = warp; q < gr.nr * G; q += C::NSW) {
+          if (!xw[q]) continue;
+          const float2* src = reinterpret_cast<const float2*>(xo + q * (D + 2));
+          float2* dst = reinterpret_cast<float2*>(
+              p.out + ((size_t)(t0 + q / G) * p.n_heads + g * G + q % G) * D);
+#pragma unroll
+          for (int e = lane; e < D / 2; e += 32) dst[e] = src[e];
+        }
+      }
+      tc_fence_before();  // these TMEM reads precede the next group's MMAs (after q_full)
+      named_bar_sync(1, 32 * C::NSW);  // the exchange area is read before the next q lands
+      fence_async_smem();               // (generic reads before the next bulk copy's writes)
+      mbar_arrive(x_free);
+    }
+    if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::ISSUER) {
+    tc_fence_after();
+    tmem_free(tbase, C::TMEM_COLS);
+  }
+  // this CTA's partials are written: the merge kernel launched after this one may be scheduled
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+}  // namespace gqa

@@ -56,10 +56,13 @@ def _env(**kw):
 @contextmanager
 def f16_kernel(name):
     """Runs the block with the f16 path on one kernel: "chunked" (tensor cores, chunked grid:
-    the default), "streamk" (tensor cores, stream-K split) or "fma" (CUDA cores, chunked)."""
-    env = {"streamk": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT="streamk"),
-           "chunked": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT=None),
-           "fma": dict(GQA_F16_KERNEL="fma", GQA_F16_SPLIT=None)}[name]
+    the default; grouped rows on the tcgen05 kernel), "rows_mma" (the same with grouped rows on
+    the mma.sync kernel), "streamk" (tensor cores, stream-K split) or "fma" (CUDA cores,
+    chunked)."""
+    env = {"streamk": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT="streamk", GQA_F16_ROWS=None),
+           "chunked": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT=None, GQA_F16_ROWS=None),
+           "rows_mma": dict(GQA_F16_KERNEL=None, GQA_F16_SPLIT=None, GQA_F16_ROWS="mma"),
+           "fma": dict(GQA_F16_KERNEL="fma", GQA_F16_SPLIT=None, GQA_F16_ROWS=None)}[name]
     with _env(**env):
         yield
 

@@ -289,34 +289,43 @@ def test_workspace_reuse_leaves_counters_zero():
 
 # ----------------------------------------------------------------------------- row grouping
 
+ROWS_KERNELS = {"umma": "chunked", "mma": "rows_mma"}  # grouped rows: tcgen05 or mma.sync
+ROWS_PER_GROUP = {"umma": 64, "mma": 32}  # (row, head) pairs per group
+
+
+@pytest.mark.parametrize("rows", ["umma", "mma"])
 @pytest.mark.parametrize("chunk", [None, 64, 256])
 @pytest.mark.parametrize("D,G", [(D, G) for D in (64, 128) for G in (1, 2, 4, 8)])
-def test_rows_grouped_by_sequence(D, G, chunk):
+def test_rows_grouped_by_sequence(D, G, chunk, rows):
     """Rows sharing a sequence are served from one staged K/V tile per group: runs longer than a
-    group (G=8: 8 rows), causal and ragged lengths inside a group, an empty row, a row of one
-    position, and sequences interleaved."""
+    group (G=8 on the mma.sync kernel: 4 rows), causal and ragged lengths inside a group, an
+    empty row, a row of one position, and sequences interleaved."""
     seq_of = [0] * 11 + [1, 1, 2] + [0] * 3 + [2]
     L = [400 + 7 * r for r in range(11)] + [1, 399, 0, 300, 5, 401, 250]
     case = W.make_f16_case(500 + D + G, len(seq_of), 2 * G, 2, D, L, cache_cap=480,
                            seq_of=seq_of, n_seq=3, scale=1 / math.sqrt(D))
     gd = _gd()
-    assert gd.plan(len(seq_of), 2 * G, 2, D, 480, n_seq=3).row_group == 32 // G
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    with forced_chunk(chunk):
+    with forced_chunk(chunk), f16_kernel(ROWS_KERNELS[rows]):
+        assert gd.plan(len(seq_of), 2 * G, 2, D, 480, n_seq=3).row_group == ROWS_PER_GROUP[rows] // G
         got = run_case(case, err=err).cpu().numpy()
     assert int(err.item()) == 0
-    assert_close(got, oracle_ref(case), TOL_F16, f"rows D{D} G{G} chunk{chunk}")
+    assert_close(got, oracle_ref(case), TOL_F16, f"rows {rows} D{D} G{G} chunk{chunk}")
     assert (got[13] == 0).all()
 
 
 def test_rows_grouped_matches_per_row_kernel():
-    """The prefill chunk (16 causal rows over one cache) with and without row grouping."""
+    """The prefill chunk (16 causal rows over one cache) with row grouping on either row kernel
+    and without it."""
     case = W.prefill_chunk()
     got = run_case(case).cpu().numpy()
+    with f16_kernel("rows_mma"):
+        got_mma = run_case(case).cpu().numpy()
     with _rows_off():
         per_row = run_case(case).cpu().numpy()
     ref = oracle_ref(case)
-    assert_close(got, ref, TOL_F16, "grouped")
+    assert_close(got, ref, TOL_F16, "grouped (tcgen05)")
+    assert_close(got_mma, ref, TOL_F16, "grouped (mma.sync)")
     assert_close(per_row, ref, TOL_F16, "per row")
 
 
@@ -325,16 +334,18 @@ def _rows_off():
     return _env(GQA_F16_ROWS="off")
 
 
+@pytest.mark.parametrize("rows", ["umma", "mma"])
 @pytest.mark.parametrize("G", [1, 2, 4])
-def test_rows_grouped_long_runs(G):
-    """Runs longer than a group (32 / G rows: 32 for G = 1), split at multiples of the group
-    size, with a second sequence starting mid-group."""
-    seq_of = [0] * 70 + [1] * 5
-    L = [100 + r for r in range(70)] + [60, 0, 61, 62, 1]
-    case = W.make_f16_case(600 + G, len(seq_of), 2 * G, 2, 64, L, cache_cap=200, seq_of=seq_of,
+def test_rows_grouped_long_runs(G, rows):
+    """Runs longer than a group (pairs per group / G rows: 64 or 32 for G = 1), split at
+    multiples of the group size, with a second sequence starting mid-group."""
+    seq_of = [0] * 150 + [1] * 5
+    L = [100 + r for r in range(150)] + [60, 0, 61, 62, 1]
+    case = W.make_f16_case(600 + G, len(seq_of), 2 * G, 2, 64, L, cache_cap=260, seq_of=seq_of,
                            n_seq=2, scale=0.125)
-    got = run_case(case).cpu().numpy()
-    assert_close(got, oracle_ref(case), TOL_F16, f"long runs G{G}")
+    with f16_kernel(ROWS_KERNELS[rows]):
+        got = run_case(case).cpu().numpy()
+    assert_close(got, oracle_ref(case), TOL_F16, f"long runs {rows} G{G}")
 
 
 @pytest.mark.parametrize("pair_layout", [False, True])

@@ -39,7 +39,7 @@ def test_random_f16(i):
     case = W.make_f16_case(7100 + i, T, G * Hk, Hk, D, L, cache_cap=cap, seq_of=seq_of,
                            n_seq=n_seq, scale=1 / math.sqrt(D))
     ref = oracle_ref(case)
-    for kernel in ("chunked", "fma"):
+    for kernel in ("chunked", "rows_mma", "fma"):
         with f16_kernel(kernel), forced_chunk(chunk):
             got = run_case(case).cpu().numpy()
         assert_close(got, ref, TOL_F16, f"f16 #{i} D{D} G{G} Hk{Hk} T{T} {kernel} chunk{chunk}")

@@ -85,16 +85,26 @@ def test_plan_selected_width_caps_chunks(gd):
     assert p.grid_y == 4 * 3 and p.chunk == 128
 
 
-def test_plan_groups_rows_sharing_a_sequence(gd):
-    # 16 causal rows over one sequence (n_seq 1): two groups of 8 rows (G=4: 2 sets of 16
-    # (row, head) pairs); chunks sized for 2 groups x 8 KV heads on two CTAs per SM:
-    # 16 * 8192 / 304 -> 432 -> 448 positions
+def test_plan_groups_rows_sharing_a_sequence(gd, monkeypatch):
+    # 16 causal rows over one sequence (n_seq 1), G=4: one group of up to 16 rows (64 (row,
+    # head) pairs, each twice in the tcgen05 MMA's 128 rows); chunks of 64-position tiles sized
+    # for 1 group x 8 KV heads on one CTA per SM: 8 * 8192 / 152 -> 432 -> 448 positions
     p = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1)
-    assert p.row_group == 8 and p.chunk == 448 and p.n_split == 19
-    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 2)   # two group slots
+    assert p.row_group == 16 and p.chunk == 448 and p.n_split == 19 and p.tile == 64
+    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 1)   # one group slot
     # 64 rows of 32 sequences (pairs): 32 slots
     q = gd.plan(64, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=32)
-    assert q.row_group == 8 and q.grid_z == 32
+    assert q.row_group == 16 and q.grid_z == 32
+    # D=64 keeps the 64-position tile on the tcgen05 row kernel
+    assert gd.plan(16, 32, 8, 64, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1).tile == 64
+    # the mma.sync row kernel: two groups of 8 rows (2 sets of 16 pairs) on two CTAs per SM:
+    # 16 * 8192 / 304 -> 432 -> 448 positions
+    monkeypatch.setenv("GQA_F16_ROWS", "mma")
+    m = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=1)
+    assert m.row_group == 8 and m.chunk == 448 and m.n_split == 19
+    assert (m.grid_x, m.grid_y, m.grid_z) == (19, 8, 2)   # two group slots
+    assert gd.plan(64, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152, n_seq=32).row_group == 8
+    monkeypatch.delenv("GQA_F16_ROWS")
     # every row its own sequence, D=256, int8, or group size 3: no grouping
     assert gd.plan(16, 32, 8, 128, 8192, num_sms=152).row_group == 1
     assert gd.plan(16, 32, 8, 256, 8192, num_sms=152, n_seq=1).row_group == 1
