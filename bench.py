@@ -195,9 +195,23 @@ def _device_inputs(case, torch):
     return t
 
 
+def _rows_fused_merge(plan):
+    """Grouped rows on the tcgen05 kernel merge their own partials when the grid fits one CTA
+    per SM (the library's rule)."""
+    if not (plan.merge and not plan.streamk and plan.row_group > 1):
+        return False
+    if os.environ.get("GQA_F16_ROWS") == "mma":
+        return False
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return plan.grid_x * plan.grid_y * plan.grid_z <= sms
+
+
 def _merge_launch(plan):
     """1 when the step ends with a separate merge kernel (rows grouped by sequence)."""
-    return 1 if plan.merge and not plan.streamk and plan.row_group > 1 else 0
+    if plan.merge and not plan.streamk and plan.row_group > 1 and not _rows_fused_merge(plan):
+        return 1
+    return 0
 
 
 def _kernel_name(case, plan):
@@ -207,7 +221,13 @@ def _kernel_name(case, plan):
     if plan.streamk:
         return "streamk_mma_kernel (stream-K split, merge fused)"
     if plan.row_group > 1:
-        return "partial_mma_rows_kernel (rows grouped by sequence) + merge_kernel"
+        rows = ("partial_mma_rows_kernel" if os.environ.get("GQA_F16_ROWS") == "mma"
+                else "umma_rows_kernel")
+        if not plan.merge:
+            return rows + " (rows grouped by sequence)"
+        if _rows_fused_merge(plan):
+            return rows + " (rows grouped by sequence, merge fused)"
+        return rows + " (rows grouped by sequence) + merge_kernel"
     if "block_scores" in case.meta:
         return "topk_kernel + partial_kernel (split-KV, merge fused)"
     if plan.streamk:

@@ -265,7 +265,17 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
                              : 4LL * (head_dim / 16 + head_dim / 32 + 1) + 4LL * (head_dim / 16 + 1);
   if (nmax * row_bytes <= (tq ? kTqMinSplitBytes : kMinSplitBytes)) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");
-  if (forced > 0) chunk = forced;
+  if (forced > 0) {
+    chunk = forced;
+  } else if (umma_rows) {
+    // at most one CTA per SM in all, so that the chunk CTAs can merge their own partials (a
+    // cooperative launch); when even one chunk per group and KV head is too many, the merge
+    // kernel follows instead
+    const long long per_split = (long long)n_kv_heads * hsplit *
+                                std::min<long long>(groups, n_tok);
+    const long long cap = num_sms / std::max(per_split, 1LL);
+    if (cap >= 1) chunk = std::max(chunk, (std::max(nmax, 1LL) + cap - 1) / cap);
+  }
   chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;
   const long long whole = (std::max(nmax, 1LL) + tile - 1) / tile * tile;
   if (chunk > whole) chunk = whole;
@@ -404,12 +414,24 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     var.mma = !(k && std::strcmp(k, "fma") == 0);
   }
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
+  // grouped rows on the tcgen05 kernel merge their own partials when the whole grid fits one
+  // CTA per SM (a cooperative launch); otherwise merge_kernel follows
+  if (plan.merge && !plan.streamk && plan.row_group > 1 && gqa::rows_on_umma()) {
+    st = GQA_OK;
+    const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
+    p.fused_merge = ctas <= current_sm_count(&st) ? 1 : 0;
+  }
   cudaError_t e =
       plan.streamk        ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
       : plan.row_group > 1 ? gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream)
                            : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge && p.fused_merge) {  // not all resident after all
+    (void)cudaGetLastError();
+    p.fused_merge = 0;
+    e = gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
-  if (plan.merge && !plan.streamk && plan.row_group > 1) {
+  if (plan.merge && !plan.streamk && plan.row_group > 1 && !p.fused_merge) {
     // grouped rows: their partials are merged by merge_kernel, one warp per (row, head)
     e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
                           nullptr, 0, /*after_partials=*/true);

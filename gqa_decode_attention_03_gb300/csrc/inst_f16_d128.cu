@@ -57,8 +57,19 @@ cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
     const void* fu = reinterpret_cast<const void*>(&umma_rows_kernel<128>);
     cudaError_t e = ensure_smem(fu, U::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    umma_rows_kernel<128><<<grid, U::THREADS, U::SMEM_BYTES, s>>>(tk, tv, p);
-    return cudaGetLastError();
+    // with the fused merge the chunk CTAs of a group wait for one another: a cooperative launch
+    // guarantees they are all resident
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(U::THREADS);
+    cfg.dynamicSmemBytes = U::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.fused_merge ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, umma_rows_kernel<128>, tk, tv, p);
   }
   using C = RowsCfg<128>;
   const void* fn = reinterpret_cast<const void*>(&partial_mma_rows_kernel<128>);

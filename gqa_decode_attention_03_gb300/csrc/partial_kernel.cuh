@@ -55,6 +55,8 @@ struct PartialParams {
   int n_split;             // chunks per row in the grid (grid.x)
   float scale_log2;        // scale * log2(e)
   int merge;
+  int fused_merge;         // tcgen05 row kernel: the chunk CTAs of a group merge its partials
+                           // themselves (cooperative launch; counters [groups][n_kv_heads])
 };
 
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }

@@ -28,14 +28,13 @@
 // P.V MMA (P is zero there, but cache garbage could be NaN).  At the end of the chunk the O rows
 // go through shared memory so that the records (or outputs) are written row by row, coalesced.
 //
-// Warps: 0-3 softmax and epilogue, 4 TMA producer, 5 MMA issuer (one elected lane) and TMEM
-// owner.  The issuer polls its two inputs and issues whichever MMA is ready first: S(i) once
-// K/V tile i has landed (and S buffer i % 3 is free), P.V(i) once P(i) is written.  Barriers:
-// full/empty per stage (TMA <-> MMA), q_land (q staged), q_full (softmax wrote the group's Q),
-// s_full per S buffer (MMA -> softmax; S(i) is issued after P.V(i - 3), so it also frees P
-// buffer i % 3), p_full per P buffer (softmax -> MMA), pv_done per P buffer (MMA -> softmax: O
-// final for a rescale or the epilogue), x_free (softmax -> producer: the staging area is free for
-// the next group's q).  Every wait is bounded; a wait that runs out flags GQA_ERR_TIMEOUT and its
+// Warps: 0-3 softmax and epilogue, 4 TMA producer, 5 S issuer (one lane) and TMEM owner, 6 P.V
+// issuer (one lane).  S(i) goes once K/V tile i has landed and the softmax has read S(i - 3)
+// (three S buffers); P.V(i) once P(i) is written.  Barriers: full/empty per stage (TMA <-> MMA),
+// q_land (q staged), q_full (softmax wrote the group's Q), s_full per S buffer (S issuer ->
+// softmax), p_full per P buffer (softmax -> both issuers), pv_done per P buffer (P.V issuer ->
+// softmax: P buffer free again, O final for a rescale or the epilogue), x_free (softmax ->
+// producer: the staging area is free for the next group's q).  Every wait is bounded; a wait that runs out flags GQA_ERR_TIMEOUT and its
 // role stops, and before TMEM is freed the issuer waits for all of its MMAs to complete.
 //
 // MMA cost (measured on GB300, one thread issuing back to back): M64 N64 K16 ~56 cycles, M64
@@ -71,13 +70,13 @@ struct UmmaRowsCfg {
   static constexpr int TMEM_COLS = NPB * TP + D <= 256 ? 256 : 512;
   static constexpr int KS_S = D / 16;              // k steps of S = Q.K^T
   static constexpr int KS_O = TP / 16;             // k steps of O += P.V
-  static constexpr int NSW = 4, PRODUCER = 4, ISSUER = 5;
-  static constexpr int THREADS = 192;
-  static constexpr int NBAR = 2 * NST + 3 + 3 * NPB + 1;
+  static constexpr int NSW = 4, PRODUCER = 4, ISSUER = 5, PV_ISSUER = 6;
+  static constexpr int THREADS = 224;
+  static constexpr int NBAR = 2 * NST + 4 + 3 * NPB + 1;
   // staging of the group's fp32 q, then the epilogue's exchange: records [NP][D + 2] + flags
   static constexpr int X_BYTES = cmax(NP * D * 4, NP * (D + 2) * 4 + NP * 4);
   static constexpr int BAR_OFF = NST * STAGE_BYTES + Q_BYTES + NPB * P_BYTES;
-  static constexpr int X_OFF = align_up(BAR_OFF + NBAR * 8 + 4, 128);  // bulk copies, float4
+  static constexpr int X_OFF = align_up(BAR_OFF + NBAR * 8 + 8, 128);  // bulk copies, float4
   static constexpr int SMEM_BYTES = 1024 + X_OFF + X_BYTES;
   static constexpr float RESCALE_LOG2 = 8.f;
   static_assert(D == 64 || D == 128, "row grouping serves head_dim 64 and 128");
@@ -88,6 +87,104 @@ struct UmmaRowsCfg {
                 "swizzled tiles start on 1024-byte atoms");
   static_assert(BAR_OFF % 8 == 0 && X_OFF % 16 == 0, "barrier and staging alignment");
 };
+
+// The fused merge of one group (run by the 128 softmax threads of every chunk CTA of the group,
+// all resident under a cooperative launch).  Every CTA's records are stored and fenced before it
+// counts itself in; once all gridDim.x chunk CTAs are in, CTA c merges the group's pairs
+// c, c + gridDim.x, ... (warp w of it takes every fourth of those), reading the records past L1,
+// with merge_kernel's arithmetic; a second count-in lets the last CTA past the wait reset the
+// counter.
+template <int D>
+__device__ bool rows_fused_merge(const PartialParams& p, const RowGroup& gr, int k, int g, int c,
+                                 bool seq_ok, int* merge_ok) {
+  constexpr int DPL = D / 32;
+  constexpr int NSW = UmmaRowsCfg<D>::NSW;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = p.group;
+  const unsigned int nctas = gridDim.x;
+  unsigned int* cnt = p.counters + (size_t)k * p.n_kv_heads + g;
+  __threadfence();  // this thread's record stores, device-wide
+  named_bar_sync(1, 32 * NSW);
+  if (threadIdx.x == 0) {
+    atomicAdd(cnt, 1u);
+    int ok = 0;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= nctas) {
+        ok = 1;
+        break;
+      }
+    }
+    // every CTA counts in a second time once it has seen all in; the last of those resets the
+    // counter for the next call (its latency overlaps this CTA's merge)
+    if (ok && atomicAdd(cnt, 1u) == 2 * nctas - 1) atomicExch(cnt, 0u);
+    *merge_ok = ok;
+  }
+  named_bar_sync(1, 32 * NSW);
+  const bool ok = *merge_ok != 0;
+  if (ok) {
+    const size_t rec = (size_t)p.n_heads * (D + 2);
+    for (int q = c + warp * (int)nctas; q < gr.nr * G; q += NSW * (int)nctas) {
+      const int t = gr.t0 + q / G, h = g * G + q % G;
+      int dummy = 0;
+      const int L = rows_len(p, t, seq_ok, &dummy);
+      if (L == 0) continue;  // zeroed by the bookkeeping
+      const int nv = min((L + p.chunk - 1) / p.chunk, p.n_split);
+      const float* base = p.part + ((size_t)t * p.n_split * p.n_heads + h) * (D + 2);
+      float a[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) a[e] = 0.f;
+      float M = -INFINITY, Ls = 0.f;
+      // batches of up to MB chunks: every load of a batch (lane c's (m, l), each lane's D / 32
+      // dims of every chunk) is issued before any is used, so a batch costs one L2 round trip
+      constexpr int MB = 24;
+      for (int cb = 0; cb < nv; cb += MB) {
+        const int nb = min(MB, nv - cb);
+        float m = -INFINITY, l = 0.f;
+        if (lane < nb) {
+          m = __ldcg(base + (cb + lane) * rec + D);
+          l = __ldcg(base + (cb + lane) * rec + D + 1);
+        }
+        const float* ac = base + cb * rec + lane * DPL;
+        float2 v[MB][DPL / 2];
+#pragma unroll
+        for (int j = 0; j < MB; ++j)
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e)
+            v[j][e] = j < nb ? __ldcg(reinterpret_cast<const float2*>(ac + j * rec) + e)
+                             : make_float2(0.f, 0.f);
+        float mb = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        const float M_new = fmaxf(M, mb);
+        if (M_new == -INFINITY) continue;
+        const float corr = M == -INFINITY ? 0.f : __expf(M - M_new);
+        M = M_new;
+        Ls *= corr;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) a[e] *= corr;
+        const float w = m == -INFINITY ? 0.f : __expf(m - M);
+        Ls = fmaf(l, w, Ls);
+#pragma unroll
+        for (int j = 0; j < MB; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, j);  // 0 past nb (lanes >= nb: w = 0)
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e) {
+            a[2 * e] = fmaf(wj, v[j][e].x, a[2 * e]);
+            a[2 * e + 1] = fmaf(wj, v[j][e].y, a[2 * e + 1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      float* orow = p.out + ((size_t)t * p.n_heads + h) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; e += 2) *reinterpret_cast<float2*>(orow + e) = make_float2(a[e] * inv, a[e + 1] * inv);
+    }
+  }
+  return ok;
+}
 
 template <int D>
 __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
@@ -111,10 +208,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
   uint64_t* s_full = q_full + 1;
   uint64_t* p_full = s_full + C::NPB;
   uint64_t* pv_done = p_full + C::NPB;
-  uint64_t* drain = pv_done + C::NPB;
-  uint64_t* q_land = drain + 1;
+  uint64_t* drain = pv_done + C::NPB;  // [2]: one per issuing thread
+  uint64_t* q_land = drain + 2;
   uint64_t* x_free = q_land + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(x_free + 1);
+  int* merge_ok = reinterpret_cast<int*>(tmem_holder + 1);
   uint8_t* sX = stages + C::X_OFF;  // 128-byte aligned
 
   if (threadIdx.x == 0) {
@@ -128,7 +226,8 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       mbar_init(&p_full[i], 32 * C::NSW);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(q_land, 1);
     mbar_init(x_free, 32 * C::NSW);
     mbar_init_fence();
@@ -197,7 +296,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         if (!mbar_wait(&full[st], (last / C::NST) & 1)) flag_error(p.err, GQA_ERR_TIMEOUT);
       }
     }
-  } else if (warp == C::ISSUER) {  // ---- MMA issuer: lane 0 issues, the warp walks the groups
+  } else if (warp == C::ISSUER || warp == C::PV_ISSUER) {
+    // ---- MMA issuers, lane 0 of each: warp ISSUER issues S = Q . K^T, warp PV_ISSUER
+    //      O += P . V (two issuing threads keep both MMA streams going; MMAs of one shape issued
+    //      back to back also run faster than alternating ones)
+    const bool is_s = warp == C::ISSUER;
     constexpr uint32_t kIdS = umma_idesc_f16(C::M, C::TP, false);
     constexpr uint32_t kIdO = umma_idesc_f16(C::M, D, true);
     const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
@@ -213,52 +316,41 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       ++qn;
       if (!ok) break;
       if (lane == 0) {
-        // S(js) may go once tile js has landed and P.V(js - NPB) was issued (S buffer js % NPB
-        // is free then: its softmax wrote P(js - NPB)); P.V(jp) once P(jp) is written
-        int js = 0, jp = 0;
-        uint32_t spins = 0;
-        while (jp < ntile) {
-          bool issued = false;
-          if (js < ntile && js < jp + C::NPB) {
-            const int i = it + js, st = i % C::NST;
-            if (mbar_test(&full[st], (i / C::NST) & 1)) {
-              tc_fence_after();
-              const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
+        for (int j = 0; j < ntile && ok; ++j) {
+          const int i = it + j;
+          if (is_s) {
+            // S(i) once tile i has landed and the softmax has read S(i - NPB) (its P is out)
+            const int st = i % C::NST;
+            ok = mbar_wait(&full[st], (i / C::NST) & 1) &&
+                 (j < C::NPB ||
+                  mbar_wait(&p_full[(i - C::NPB) % C::NPB], ((i - C::NPB) / C::NPB) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sk = smem_addr(stages + st * C::STAGE_BYTES);
 #pragma unroll
-              for (int kk = 0; kk < C::KS_S; ++kk) {
-                const uint32_t ko = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                const uint32_t qo = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-                umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
-                         umma_desc_sw128(q_addr + qo, 16, 1024),
-                         umma_desc_sw128(sk + ko, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-              }
-              umma_commit(&s_full[i % C::NPB]);
-              ++js;
-              issued = true;
+            for (int kk = 0; kk < C::KS_S; ++kk) {
+              const uint32_t ko = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+              const uint32_t qo = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+              umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
+                       umma_desc_sw128(q_addr + qo, 16, 1024),
+                       umma_desc_sw128(sk + ko, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
             }
-          }
-          if (jp < js) {
-            const int i = it + jp;
-            if (mbar_test(&p_full[i % C::NPB], (i / C::NPB) & 1)) {
-              tc_fence_after();
-              const uint32_t sv = smem_addr(stages + (i % C::NST) * C::STAGE_BYTES + C::KV_BYTES);
-              const uint32_t pa = p_addr + (i % C::NPB) * C::P_BYTES;
+            umma_commit(&s_full[i % C::NPB]);
+          } else {
+            // P.V(i) once P(i) is written (after S(i) completed); its completion frees the
+            // stage (K was read by S(i) before) and P buffer i % NPB
+            ok = mbar_wait(&p_full[i % C::NPB], (i / C::NPB) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sv = smem_addr(stages + (i % C::NST) * C::STAGE_BYTES + C::KV_BYTES);
+            const uint32_t pa = p_addr + (i % C::NPB) * C::P_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < C::KS_O; ++kk)
-                umma_f16(tbase + C::O_COL, umma_desc_sw128(pa + kk * 32, 16, 1024),
-                         umma_desc_sw128(sv + kk * 2048, C::BOX_BYTES, 1024), kIdO,
-                         (jp == 0 && kk == 0) ? 0u : 1u);
-              umma_commit(&empty[i % C::NST]);
-              umma_commit(&pv_done[i % C::NPB]);
-              ++jp;
-              issued = true;
-            }
-          }
-          if (issued) {
-            spins = 0;
-          } else if (++spins > 16u * kSpinLimit) {  // nothing ready for far too long
-            ok = false;
-            break;
+            for (int kk = 0; kk < C::KS_O; ++kk)
+              umma_f16(tbase + C::O_COL, umma_desc_sw128(pa + kk * 32, 16, 1024),
+                       umma_desc_sw128(sv + kk * 2048, C::BOX_BYTES, 1024), kIdO,
+                       (j == 0 && kk == 0) ? 0u : 1u);
+            umma_commit(&empty[i % C::NST]);
+            umma_commit(&pv_done[i % C::NPB]);
           }
         }
       }
@@ -268,8 +360,8 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
     // every MMA this thread issued has completed before TMEM is freed
     if (lane == 0) {
-      umma_commit(drain);
-      if (!mbar_wait(drain, 0)) flag_error(p.err, GQA_ERR_TIMEOUT);
+      umma_commit(&drain[is_s ? 0 : 1]);
+      if (!mbar_wait(&drain[is_s ? 0 : 1], 0)) flag_error(p.err, GQA_ERR_TIMEOUT);
     }
     __syncwarp();
   } else {  // ---- softmax warpgroup: two threads per pair (position halves of each tile)
@@ -305,7 +397,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
           }
         }
       }
-      if (c1 <= c0) continue;  // the same decision as the producer's and the issuer's
+      if (c1 <= c0) {  // the same decision as the producer's and the issuer's
+        if (p.merge && p.fused_merge) ok = rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
+        if (!ok) break;
+        continue;
+      }
       const int ntile = (c1 - c0 + C::TP - 1) / C::TP;
       const bool rv = jr < gr.nr;  // this pair is a real row
       const int t = t0 + (rv ? jr : 0);
@@ -349,7 +445,6 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;  // m_run: the pair's (both halves'); l_run: this half's
       for (int j = 0; j < ntile; ++j) {
         const int it_j = it + j, b = it_j % C::NPB;
-        // S(it_j) complete; so is P.V(it_j - NPB), issued before it: P buffer b is free
         ok = wait(&s_full[b], (it_j / C::NPB) & 1);
         if (!ok) break;
         tc_fence_after();
@@ -384,6 +479,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
           if (resc) l_run *= corr;
         }
         if (grow) m_run = mt;
+        // P buffer b is free once P.V(it_j - NPB) has completed (earlier groups' all have)
+        if (j >= C::NPB) {
+          ok = wait(&pv_done[b], ((it_j - C::NPB) / C::NPB) & 1);
+          if (!ok) break;
+        }
         const float mu = m_run == -INFINITY ? 0.f : m_run;  // lim <= 0 there: all weights 0
         float lq[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t ph[16];
@@ -472,6 +572,8 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       named_bar_sync(1, 32 * C::NSW);  // the exchange area is read before the next q lands
       fence_async_smem();               // (generic reads before the next bulk copy's writes)
       mbar_arrive(x_free);
+      if (p.merge && p.fused_merge) ok = rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
+      if (!ok) break;
     }
     if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
   }

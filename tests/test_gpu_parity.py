@@ -371,3 +371,27 @@ def test_merge_with_sigmoid_gate(D, pair_layout):
     ref = oracle.gated_merge(part[..., :D].astype(np.float64), part[..., D].astype(np.float64),
                              part[..., D + 1].astype(np.float64), n_valid, g)
     assert_close(got.cpu().numpy(), ref, 1e-5, "gated merge")
+
+
+@pytest.mark.parametrize("Hk,chunk,fused", [(2, None, None), (2, 256, False), (1, 256, True)])
+def test_rows_grouped_many_groups_merge_paths(Hk, chunk, fused):
+    """Forty sequences of three rows each.  The planner keeps the tcgen05 row kernel's grid within
+    one CTA per SM; with 256-position chunks forced, 3 x 2 x 40 CTAs do not fit, so merge_kernel
+    follows the row kernel, while 3 x 1 x 40 do, and the chunk CTAs of each group merge their own
+    partials.  All against the oracle."""
+    rng = np.random.default_rng(650 + Hk)
+    seq_of = np.repeat(np.arange(40), 3)
+    L = rng.integers(1, 700, seq_of.size)
+    case = W.make_f16_case(651 + Hk, seq_of.size, 2 * Hk, Hk, 64, L, cache_cap=700,
+                           seq_of=seq_of, n_seq=40, scale=0.125)
+    gd = _gd()
+    with forced_chunk(chunk):
+        pl = gd.plan(case.n_tok, 2 * Hk, Hk, 64, 700, n_seq=40)
+        got = run_case(case).cpu().numpy()
+    ctas = pl.grid_x * pl.grid_y * pl.grid_z
+    assert pl.row_group == 32
+    if fused is None:
+        assert ctas <= 152
+    else:
+        assert pl.merge == 1 and (ctas <= 152) == fused
+    assert_close(got, oracle_ref(case), TOL_F16, f"many groups Hk{Hk} chunk{chunk}")
