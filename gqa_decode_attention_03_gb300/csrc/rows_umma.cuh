@@ -232,17 +232,26 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     mbar_init(x_free, 32 * C::NSW);
     mbar_init_fence();
   }
-  if (threadIdx.x == 32 && p.seq_of)  // the row tables' first lines, for the group search
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p.seq_of) : "memory");
-  if (threadIdx.x == 64) asm volatile("prefetch.global.L1 [%0];" ::"l"(p.kv_len) : "memory");
+  // Every warp walks the same groups (k = slot, slot + nslots, ...) in the same order.  The first
+  // group is looked up while thread 0 sets up the barriers and the issuer warp allocates TMEM.
+  int scan_t = 0, scan_cnt = 0;
+  const int t0_first = rows_find_leader(p, R, slot, scan_t, scan_cnt, lane);
+  RowGroup gr_first{};
+  if (t0_first >= 0) gr_first = rows_group(p, t0_first, R, lane);
+  auto group = [&](int k, RowGroup& gr) {  // the k-th group's leader (-1 past the last)
+    if (k == slot) {
+      gr = gr_first;
+      return t0_first;
+    }
+    const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+    if (t0 >= 0) gr = rows_group(p, t0, R, lane);
+    return t0;
+  };
   if (warp == C::ISSUER) tmem_alloc(tmem_holder, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
-
-  // Every warp walks the same groups (k = slot, slot + nslots, ...) in the same order.
-  int scan_t = 0, scan_cnt = 0;
   bool ok = true;
 
   if (warp == C::PRODUCER) {  // ---- TMA producer: lane 0 issues, the warp walks the groups
@@ -252,9 +261,9 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     }
     int it = 0, gn = 0;
     for (int k = slot; ok; k += nslots) {
-      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      RowGroup gr;
+      const int t0 = group(k, gr);
       if (t0 < 0) break;
-      const RowGroup gr = rows_group(p, t0, R, lane);
       const int c1 = min(c0 + p.chunk, gr.lmax);
       if (c1 <= c0) continue;
       // the group's fp32 q first (one bulk copy per row: its G heads are contiguous), into the
@@ -306,9 +315,9 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
     int it = 0, qn = 0;
     for (int k = slot; ok; k += nslots) {
-      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      RowGroup gr;
+      const int t0 = group(k, gr);
       if (t0 < 0) break;
-      const RowGroup gr = rows_group(p, t0, R, lane);
       const int c1 = min(c0 + p.chunk, gr.lmax);
       if (c1 <= c0) continue;
       const int ntile = (c1 - c0 + C::TP - 1) / C::TP;
@@ -377,9 +386,9 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     };
     int it = 0, qn = 0;
     for (int k = slot; ok; k += nslots) {
-      const int t0 = rows_find_leader(p, R, k, scan_t, scan_cnt, lane);
+      RowGroup gr;
+      const int t0 = group(k, gr);
       if (t0 < 0) break;
-      const RowGroup gr = rows_group(p, t0, R, lane);
       const bool seq_ok = gr.s >= 0 && gr.s < p.n_seq;
       const int c1 = min(c0 + p.chunk, gr.lmax);
       if (c == 0 && warp == 0) {  // per-row bookkeeping: flags, chunk counts, empty rows
