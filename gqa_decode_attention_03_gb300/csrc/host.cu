@@ -315,10 +315,13 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
                          float* out, const int32_t* kv_len, const int32_t* seq_of, int n_tok,
                          int n_seq, int n_heads, int n_kv_heads, int head_dim, int64_t cache_cap,
                          int max_kv_len, float scale, void* ws, size_t ws_bytes,
-                         int32_t* err_word, cudaStream_t stream, int scale_group = 64) {
+                         int32_t* err_word, cudaStream_t stream, int scale_group = 64,
+                         const float* gate = nullptr, int64_t gate_stride = 0) {
   gqa_status st = check_shape(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, kind);
   if (st != GQA_OK) return st;
   if (n_tok == 0) return GQA_OK;
+  if (gate && (gate_stride < head_dim || (reinterpret_cast<uintptr_t>(gate) & 3)))
+    return fail(GQA_EINVAL, "gate must be 4-byte aligned with gate_stride >= head_dim");
   if (!q || !kc || !vc || !out || !kv_len) return fail(GQA_EINVAL, "a required pointer is NULL");
   if (kind == GQA_KIND_Q8 && (!ksc || !vsc)) return fail(GQA_EINVAL, "scale pointer is NULL");
   if (!aligned16(q) || !aligned16(out) || !aligned16(kc) || !aligned16(vc))
@@ -371,6 +374,8 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.n_split = plan.n_split;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.merge = plan.merge;
+  p.gate = gate;
+  p.gate_stride = gate ? gate_stride : 0;
   if (plan.streamk) {  // ws = [arrival counters][piece records]
     const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
     p.counters = static_cast<unsigned int*>(ws);
@@ -421,6 +426,10 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
     p.fused_merge = ctas <= current_sm_count(&st) ? 1 : 0;
   }
+  // polls of the fused merge's wait before it gives up; GQA_MERGE_SPIN (tests) sets fewer,
+  // 0 making every such wait run out at once
+  const char* spin = std::getenv("GQA_MERGE_SPIN");
+  p.merge_spin = spin ? (unsigned)std::strtoul(spin, nullptr, 10) : gqa::kSpinLimit;
   cudaError_t e =
       plan.streamk        ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
       : plan.row_group > 1 ? gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream)
@@ -434,7 +443,7 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   if (plan.merge && !plan.streamk && plan.row_group > 1 && !p.fused_merge) {
     // grouped rows: their partials are merged by merge_kernel, one warp per (row, head)
     e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
-                          nullptr, 0, /*after_partials=*/true);
+                          p.gate, p.gate_stride, /*after_partials=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   }
   return GQA_OK;  // otherwise split rows were merged inside the kernel by their last CTA
@@ -476,6 +485,32 @@ gqa_status attn_decode_q8_sel_sg(const float* q, const int8_t* kq, const int8_t*
   return decode_common(GQA_KIND_Q8, q, kq, vq, ksc, vsc, ids, budget, out, kv_len, seq_of, n_tok,
                        n_seq, n_heads, n_kv_heads, head_dim, cache_cap, max_kv_len, scale, ws,
                        ws_bytes, err_word, stream, scale_group);
+}
+
+gqa_status attn_decode_f16_gated(const float* q, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, float* out, const int32_t* kv_len,
+                                 const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                                 int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                                 float scale, const float* gate, int64_t gate_stride, void* ws,
+                                 size_t ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  if (!gate) return fail(GQA_EINVAL, "attn_decode_f16_gated: gate is NULL");
+  return decode_common(GQA_KIND_F16, q, k_cache, v_cache, nullptr, nullptr, nullptr, -1, out,
+                       kv_len, seq_of, n_tok, n_seq, n_heads, n_kv_heads, head_dim, cache_cap,
+                       max_kv_len, scale, ws, ws_bytes, err_word, stream, 64, gate, gate_stride);
+}
+
+gqa_status attn_decode_q8_sel_gated(const float* q, const int8_t* kq, const int8_t* vq,
+                                    const uint16_t* ksc, const uint16_t* vsc, int scale_group,
+                                    const int32_t* ids, int budget, float* out,
+                                    const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                    int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                    int64_t cache_cap, int max_kv_len, float scale,
+                                    const float* gate, int64_t gate_stride, void* ws,
+                                    size_t ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  if (!gate) return fail(GQA_EINVAL, "attn_decode_q8_sel_gated: gate is NULL");
+  return decode_common(GQA_KIND_Q8, q, kq, vq, ksc, vsc, ids, budget, out, kv_len, seq_of, n_tok,
+                       n_seq, n_heads, n_kv_heads, head_dim, cache_cap, max_kv_len, scale, ws,
+                       ws_bytes, err_word, stream, scale_group, gate, gate_stride);
 }
 
 gqa_status attn_merge_gated(const float* part, const int32_t* n_valid, int n_split, int n_tok,

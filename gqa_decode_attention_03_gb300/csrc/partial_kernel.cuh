@@ -57,7 +57,20 @@ struct PartialParams {
   int merge;
   int fused_merge;         // tcgen05 row kernel: the chunk CTAs of a group merge its partials
                            // themselves (cooperative launch; counters [groups][n_kv_heads])
+  unsigned int merge_spin; // polls of the fused merge's wait for the group's other chunk CTAs
+                           // before it gives up (kSpinLimit unless a test asks for fewer)
+  const float* gate;       // sigmoid output gate or null: element (t, h, d) at
+  long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
 };
+
+// The sigmoid output gate that both pages apply to the merged row (qsa2.metal, qsa_merge2;
+// FORWARD_MSL, attn_combine): y / (1 + exp(-gate)) for output element (t, h, d); y itself when
+// the call has no gate.  Applied wherever a kernel writes an output row, after any epilogue.
+__device__ __forceinline__ float gated(const PartialParams& p, int t, int h, int d, float y) {
+  if (!p.gate) return y;
+  const float g = __ldg(p.gate + ((size_t)t * p.n_heads + h) * p.gate_stride + d);
+  return y * (1.f / (1.f + __expf(-g)));
+}
 
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -269,6 +282,8 @@ __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int
 #pragma unroll
     for (int k = 0; k < DPL; ++k) a[k] *= inv;
     epi(a, head, lane);  // e.g. the inverse rotation of a rotated-space accumulator
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a[k] = gated(p, t, head, lane * DPL + k, a[k]);
     if constexpr (DPL == 1) {
       o[0] = a[0];
     } else {
@@ -648,7 +663,7 @@ __global__ void __launch_bounds__(Cfg<K, D, GW, NPS>::MAX_THREADS, Cfg<K, D, GW,
         pr[D + 1] = Ls;
       }
     } else {
-      p.out[((size_t)t * p.n_heads + head) * D + d] = Ls > 0.f ? A / Ls : 0.f;
+      p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
     }
   }
   if (p.merge)

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
         pr[D + 1] = Ls;
       }
     } else {
-      p.out[((size_t)t * p.n_heads + head) * D + d] = Ls > 0.f ? A / Ls : 0.f;
+      p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
     }
   }
   if (p.merge)

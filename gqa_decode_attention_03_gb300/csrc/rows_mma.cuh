@@ -443,9 +443,12 @@ __global__ void __launch_bounds__(RowsCfg<D>::MAX_THREADS, 2)
           const float inv = l > 0.f ? 1.f / l : 0.f;
           float* orow = p.out + ((size_t)tr[u] * p.n_heads + hd[u]) * D;
 #pragma unroll
-          for (int n = 0; n < C::NT; ++n)
-            *reinterpret_cast<float2*>(orow + n * 8 + 2 * tig) =
-                make_float2(o[n][2 * u] * inv, o[n][2 * u + 1] * inv);
+          for (int n = 0; n < C::NT; ++n) {
+            const int d = n * 8 + 2 * tig;
+            *reinterpret_cast<float2*>(orow + d) =
+                make_float2(gated(p, tr[u], hd[u], d, o[n][2 * u] * inv),
+                            gated(p, tr[u], hd[u], d + 1, o[n][2 * u + 1] * inv));
+          }
         } else {
           float* prt = p.part + (((size_t)tr[u] * p.n_split + c) * p.n_heads + hd[u]) * (D + 2);
 #pragma unroll

@@ -34,8 +34,10 @@
 // q_land (q staged), q_full (softmax wrote the group's Q), s_full per S buffer (S issuer ->
 // softmax), p_full per P buffer (softmax -> both issuers), pv_done per P buffer (P.V issuer ->
 // softmax: P buffer free again, O final for a rescale or the epilogue), x_free (softmax ->
-// producer: the staging area is free for the next group's q).  Every wait is bounded; a wait that runs out flags GQA_ERR_TIMEOUT and its
-// role stops, and before TMEM is freed the issuer waits for all of its MMAs to complete.
+// producer: the staging area is free for the next group's q).  Every wait is bounded.  A wait
+// that runs out flags GQA_ERR_TIMEOUT; the producer and the issuers then stop, while the softmax
+// warps stop waiting but walk on to the end (their named barriers and the merge counters stay in
+// step).  Before TMEM is freed each issuer waits for all of its MMAs to complete.
 //
 // MMA cost (measured on GB300, one thread issuing back to back): M64 N64 K16 ~56 cycles, M64
 // N128 K16 ~70, M128 N256 K16 ~133 (the dense peak).  M = 64 half-fills the tensor core, which a
@@ -43,7 +45,10 @@
 // MMAs.
 //
 // Groups, slots, the per-row bookkeeping (n_valid, empty rows) and the partial format are those
-// of the mma.sync row kernel (rows_mma.cuh); split rows are merged afterwards by merge_kernel.
+// of the mma.sync row kernel (rows_mma.cuh).  Split rows are merged inside this kernel when the
+// whole grid fits one CTA per SM: the host then launches it cooperatively, so that a group's
+// chunk CTAs are resident together and can wait for one another (rows_fused_merge below).  A
+// larger grid is followed by merge_kernel instead, as a programmatic dependent launch.
 #pragma once
 
 #include "rows_mma.cuh"
@@ -92,10 +97,16 @@ struct UmmaRowsCfg {
 // all resident under a cooperative launch).  Every CTA's records are stored and fenced before it
 // counts itself in; once all gridDim.x chunk CTAs are in, CTA c merges the group's pairs
 // c, c + gridDim.x, ... (warp w of it takes every fourth of those), reading the records past L1,
-// with merge_kernel's arithmetic; a second count-in lets the last CTA past the wait reset the
-// counter.
+// with merge_kernel's arithmetic.
+//
+// The counter protocol survives a wait that runs out.  Every chunk CTA counts in exactly twice
+// per group, whatever happens: once after its records are stored, and once more after its wait
+// (seen all in, or given up after p.merge_spin polls).  The counter therefore reaches 2 nctas
+// in every call, and the CTA whose second count-in takes it there resets it to zero: no later
+// call on the same workspace can find it part-way.  A CTA whose wait ran out flags
+// GQA_ERR_TIMEOUT and skips its share of the merge; that call's output is not to be used.
 template <int D>
-__device__ bool rows_fused_merge(const PartialParams& p, const RowGroup& gr, int k, int g, int c,
+__device__ void rows_fused_merge(const PartialParams& p, const RowGroup& gr, int k, int g, int c,
                                  bool seq_ok, int* merge_ok) {
   constexpr int DPL = D / 32;
   constexpr int NSW = UmmaRowsCfg<D>::NSW;
@@ -107,7 +118,7 @@ __device__ bool rows_fused_merge(const PartialParams& p, const RowGroup& gr, int
   if (threadIdx.x == 0) {
     atomicAdd(cnt, 1u);
     int ok = 0;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < p.merge_spin; ++i) {
       unsigned int v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
       if (v >= nctas) {
@@ -115,9 +126,10 @@ __device__ bool rows_fused_merge(const PartialParams& p, const RowGroup& gr, int
         break;
       }
     }
-    // every CTA counts in a second time once it has seen all in; the last of those resets the
-    // counter for the next call (its latency overlaps this CTA's merge)
-    if (ok && atomicAdd(cnt, 1u) == 2 * nctas - 1) atomicExch(cnt, 0u);
+    // the second count-in, taken by every CTA whether or not its wait succeeded; the last one
+    // resets the counter for the next call (its latency overlaps this CTA's merge)
+    if (atomicAdd(cnt, 1u) == 2 * nctas - 1) atomicExch(cnt, 0u);
+    if (!ok) flag_error(p.err, GQA_ERR_TIMEOUT);
     *merge_ok = ok;
   }
   named_bar_sync(1, 32 * NSW);
@@ -180,10 +192,14 @@ __device__ bool rows_fused_merge(const PartialParams& p, const RowGroup& gr, int
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       float* orow = p.out + ((size_t)t * p.n_heads + h) * D + lane * DPL;
 #pragma unroll
-      for (int e = 0; e < DPL; e += 2) *reinterpret_cast<float2*>(orow + e) = make_float2(a[e] * inv, a[e + 1] * inv);
+      for (int e = 0; e < DPL; e += 2)
+        *reinterpret_cast<float2*>(orow + e) =
+            make_float2(gated(p, t, h, lane * DPL + e, a[e] * inv),
+                        gated(p, t, h, lane * DPL + e + 1, a[e + 1] * inv));
     }
   }
-  return ok;
+  // (merge_ok is written again only after the next named barrier, which every thread reaches
+  // after its read above)
 }
 
 template <int D>
@@ -380,12 +396,17 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     const uint32_t t_q = tbase + (static_cast<uint32_t>(warp * 32) << 16);  // lane quadrant
     float* xo = reinterpret_cast<float*>(sX);  // exchange: records [NP][D + 2], then flags
     int* xw = reinterpret_cast<int*>(xo + C::NP * (D + 2));
-    // a completed phase is seen at once by a test; a pending one is waited for (bounded)
-    auto wait = [](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_test(bar, parity) || mbar_wait(bar, parity));
+    // A completed phase is seen at once by a test; a pending one is waited for (bounded).
+    // After a wait has run out (ok false) no wait is tried again, but every softmax warp still
+    // walks every group and tile to the end -- computing garbage, flagged GQA_ERR_TIMEOUT --
+    // so that the four warps reach the same named barriers and every chunk CTA counts in on
+    // every group's merge counter.  ok is warp-uniform.
+    auto wait = [&ok](uint64_t* bar, uint32_t parity) {
+      if (ok) ok = __all_sync(0xffffffffu, mbar_test(bar, parity) || mbar_wait(bar, parity));
+      return ok;
     };
     int it = 0, qn = 0;
-    for (int k = slot; ok; k += nslots) {
+    for (int k = slot;; k += nslots) {
       RowGroup gr;
       const int t0 = group(k, gr);
       if (t0 < 0) break;
@@ -407,8 +428,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         }
       }
       if (c1 <= c0) {  // the same decision as the producer's and the issuer's
-        if (p.merge && p.fused_merge) ok = rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
-        if (!ok) break;
+        if (p.merge && p.fused_merge) rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
         continue;
       }
       const int ntile = (c1 - c0 + C::TP - 1) / C::TP;
@@ -423,8 +443,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       //      thread r takes float4 pieces r, r + 128, ... (all loads first).  Pad pairs get
       //      zeros (their staging is not loaded).  No P is written before S(0), which waits for
       //      every thread's q_full arrival.
-      ok = wait(q_land, qn & 1);
-      if (!ok) break;
+      wait(q_land, qn & 1);
       {
         constexpr int NQ = C::NP * D / 4 / (32 * C::NSW);  // float4 pieces per thread
         const float4* qs = reinterpret_cast<const float4*>(sX);
@@ -454,8 +473,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;  // m_run: the pair's (both halves'); l_run: this half's
       for (int j = 0; j < ntile; ++j) {
         const int it_j = it + j, b = it_j % C::NPB;
-        ok = wait(&s_full[b], (it_j / C::NPB) & 1);
-        if (!ok) break;
+        wait(&s_full[b], (it_j / C::NPB) & 1);
         tc_fence_after();
         uint32_t sr[32];
         tmem_ld16x2<C::CPT>(t_q + C::S_COL + b * C::TP, sr);
@@ -471,8 +489,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         const bool resc = grow && m_run != -INFINITY;     // O holds weight: rescale it
         if (__any_sync(0xffffffffu, resc)) {
           // O must be final for tile it_j - 1 (this warp's lanes rescale their rows together)
-          ok = wait(&pv_done[(it_j - 1) % C::NPB], ((it_j - 1) / C::NPB) & 1);
-          if (!ok) break;
+          wait(&pv_done[(it_j - 1) % C::NPB], ((it_j - 1) / C::NPB) & 1);
           tc_fence_after();
           const float corr = resc ? ex2_approx(m_run - mt) : 1.f;
 #pragma unroll 1
@@ -490,8 +507,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         if (grow) m_run = mt;
         // P buffer b is free once P.V(it_j - NPB) has completed (earlier groups' all have)
         if (j >= C::NPB) {
-          ok = wait(&pv_done[b], ((it_j - C::NPB) / C::NPB) & 1);
-          if (!ok) break;
+          wait(&pv_done[b], ((it_j - C::NPB) / C::NPB) & 1);
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;  // lim <= 0 there: all weights 0
         float lq[4] = {0.f, 0.f, 0.f, 0.f};
@@ -514,8 +530,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         const int nv = gr.lmax - (c0 + j * C::TP);
         if (nv < C::TP) {
           const int st = it_j % C::NST;
-          ok = wait(&full[st], (it_j / C::NST) & 1);
-          if (!ok) break;
+          wait(&full[st], (it_j / C::NST) & 1);
           uint8_t* sv = stages + st * C::STAGE_BYTES + C::KV_BYTES;
           const int n16 = (C::TP - nv) * 8;  // 16-byte pieces per box
           for (int e = threadIdx.x; e < C::NBOX * n16; e += 32 * C::NSW) {
@@ -528,15 +543,13 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&p_full[b]);
       }
-      if (!ok) break;
 
       // ---- epilogue: O final after the last tile's P.V; each thread moves its half of the
       //      pair's O row into the exchange area, then the warpgroup writes the records (or
       //      outputs) row by row, coalesced
       const int last = it + ntile - 1;
-      ok = wait(&pv_done[last % C::NPB], (last / C::NPB) & 1);
+      wait(&pv_done[last % C::NPB], (last / C::NPB) & 1);
       it += ntile;
-      if (!ok) break;
       tc_fence_after();
       const float l = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
       const float f = p.merge ? 1.f : (l > 0.f ? 1.f / l : 0.f);
@@ -571,18 +584,20 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         for (int q = warp; q < gr.nr * G; q += C::NSW) {
           if (!xw[q]) continue;
           const float2* src = reinterpret_cast<const float2*>(xo + q * (D + 2));
-          float2* dst = reinterpret_cast<float2*>(
-              p.out + ((size_t)(t0 + q / G) * p.n_heads + g * G + q % G) * D);
+          const int tq = t0 + q / G, hq = g * G + q % G;
+          float2* dst = reinterpret_cast<float2*>(p.out + ((size_t)tq * p.n_heads + hq) * D);
 #pragma unroll
-          for (int e = lane; e < D / 2; e += 32) dst[e] = src[e];
+          for (int e = lane; e < D / 2; e += 32) {
+            const float2 y = src[e];
+            dst[e] = make_float2(gated(p, tq, hq, 2 * e, y.x), gated(p, tq, hq, 2 * e + 1, y.y));
+          }
         }
       }
       tc_fence_before();  // these TMEM reads precede the next group's MMAs (after q_full)
       named_bar_sync(1, 32 * C::NSW);  // the exchange area is read before the next q lands
       fence_async_smem();               // (generic reads before the next bulk copy's writes)
       mbar_arrive(x_free);
-      if (p.merge && p.fused_merge) ok = rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
-      if (!ok) break;
+      if (p.merge && p.fused_merge) rows_fused_merge<D>(p, gr, k, g, c, seq_ok, merge_ok);
     }
     if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
   }

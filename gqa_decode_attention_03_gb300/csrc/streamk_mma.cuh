@@ -135,7 +135,9 @@ __device__ __forceinline__ void sk_merge_segment(const PartialParams& p, int t, 
     float* o = p.out + ((size_t)t * p.n_heads + g * G + h) * D + lane * DPL;
 #pragma unroll
     for (int k = 0; k < DPL; k += 2)
-      *reinterpret_cast<float2*>(o + k) = make_float2(a[k] * inv, a[k + 1] * inv);
+      *reinterpret_cast<float2*>(o + k) =
+          make_float2(gated(p, t, g * G + h, lane * DPL + k, a[k] * inv),
+                      gated(p, t, g * G + h, lane * DPL + k + 1, a[k + 1] * inv));
   }
 }
 
@@ -436,7 +438,8 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
         Ls = fmaf(r[D + 1], e, Ls);
       }
       if (whole) {
-        p.out[((size_t)t * p.n_heads + g * G + h) * D + d] = Ls > 0.f ? A / Ls : 0.f;
+        p.out[((size_t)t * p.n_heads + g * G + h) * D + d] =
+            gated(p, t, g * G + h, d, Ls > 0.f ? A / Ls : 0.f);
       } else {
         rec[(size_t)h * (D + 2) + d] = A;
         if (d == 0) {

@@ -1,22 +1,28 @@
-// topk.cu -- block top-k selection of the int8 path's selected-cell id list.
+// topk.cu -- the selected-cell id list of the int8 path: block top-k selection.
 //
-// qsa2.metal (regolith), qsa_topk2: a row's n_kv cells come in blocks of 4 (the last block holds
-// n_kv % 4 cells), every cell carries its block's score, and the row keeps the `budget` cells
-// with the largest scores, emitted in ascending order; equal scores go to the lower cell.  Rows
-// with n_kv <= budget keep every cell.  Scores are compared through an order-preserving fp32 ->
-// uint32 key.
+// What is selected (qsa2.metal, regolith, qsa_topk2): row t's n = kv_len[t] cells come in blocks
+// of 4 (block b holds cells 4b .. 4b + 3; the last block holds n % 4 cells when that is not 0)
+// and every cell carries its block's score.  The row keeps the `budget` cells with the largest
+// scores, equal scores going to the lower cell, and lists them in ascending order.  A row with
+// n <= budget keeps every cell.  Scores are ranked through the order-preserving map of fp32 bit
+// patterns to uint32 (the page's `okey`, which it leaves undefined).
 //
-// One CTA of 1024 threads per row.  The row's block keys are staged in shared memory once when
-// the longest row fits kTopkSmemBlocks blocks; otherwise every pass reads them from global
-// memory (L2 after the first).  The
-// threshold key is found digit by digit, 8 bits per pass
-// over 4 passes: a 256-bin shared histogram counts the cells (4 per block, fewer for the tail)
-// whose key agrees with the digits fixed so far; a block-wide scan of the bins from the top
-// finds the digit at which the running count reaches the number of cells still needed.  The
-// emit pass then gives each thread a contiguous range of blocks: blocks above the threshold
-// give all their cells, blocks at the threshold give cells in ascending order until the budget
-// is met (exclusive scans over the threads place every cell).  Integer work only: the result is
-// a deterministic function of the keys.
+// How it is found here -- one CTA of kSelThreads threads per row:
+//   1. The threshold.  Let ge(c) be the number of cells whose key is >= c.  The threshold T is
+//      the largest key value with ge(T) >= budget, i.e. the key of the budget-th cell in
+//      descending order.  It is found by a binary search on the 32-bit key value, one bit per
+//      step from the most significant: each step counts ge(candidate) over the row with one
+//      CTA-wide sum (a warp reduction, one barrier).  One more count gives ge(T + 1), the cells
+//      strictly above T; the remaining need = budget - ge(T + 1) cells come from blocks whose
+//      key equals T, lowest cells first.
+//   2. The list.  Blocks are visited in ascending order, kSelThreads of them per round (block
+//      r * kSelThreads + tid in round r).  A CTA-wide exclusive scan of the cells at key T gives
+//      each block the number of such cells before it, hence how many of its own it takes; a
+//      second scan of the taken cells gives each block its place in the output.  Both running
+//      totals carry over to the next round.
+// The row's block keys are staged in shared memory when its block count fits the room the
+// launch reserved; otherwise each step reads them from global memory (L2 after the first).
+// Integer work only: the list is a deterministic function of the keys.
 #include <cuda_runtime_api.h>
 
 #include "common.cuh"
@@ -24,133 +30,116 @@
 
 namespace gqa {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkSmemBlocks = 49152;  // 192 KB of staged keys: n_kv up to 196607 cells
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelStageBlocks = 53248;  // 208 KB of staged keys: rows of up to 212,991 cells
 
-__device__ __forceinline__ uint32_t order_key(float x) {
+// fp32 bit pattern -> uint32 whose unsigned order is the float order (-0 below +0; NaNs at the
+// ends): negative values have every bit flipped, the others get the sign bit set.
+__device__ __forceinline__ uint32_t monotone_key(float x) {
   const uint32_t u = __float_as_uint(x);
-  return (u >> 31) ? ~u : (u | 0x80000000u);
+  return (u & 0x80000000u) ? ~u : (u ^ 0x80000000u);
 }
 
-// Exclusive prefix sum of v over the CTA's threads (in thread order); *total gets the sum.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* wsum,
-                                                         uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  uint32_t x = v;
+// The CTA-wide sum of v, returned to every thread.  One barrier; `slot` (kSelWarps words) must
+// not be the slot of the previous CTA-wide call (callers alternate two).
+__device__ __forceinline__ uint32_t cta_sum(uint32_t v, uint32_t* slot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_add_sync(0xffffffffu, v);
+  if (lane == 0) slot[warp] = v;
+  __syncthreads();
+  return __reduce_add_sync(0xffffffffu, lane < kSelWarps ? slot[lane] : 0u);
+}
+
+// The exclusive prefix sum of v over the threads in thread order; *total gets the CTA's sum.
+// One barrier; slots as for cta_sum.
+__device__ __forceinline__ uint32_t cta_exclusive(uint32_t v, uint32_t* slot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = v;  // inclusive prefix within the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
   }
-  __syncthreads();  // wsum may still be read by the previous scan
-  if (lane == 31) wsum[warp] = x;
+  if (lane == 31) slot[warp] = inc;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t z = lane < nw ? wsum[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
-    }
-    if (lane < nw) wsum[lane] = z;  // inclusive warp totals
-  }
-  __syncthreads();
-  *total = wsum[nw - 1];
-  return (x - v) + (warp > 0 ? wsum[warp - 1] : 0u);
+  const uint32_t wt = lane < kSelWarps ? slot[lane] : 0u;
+  *total = __reduce_add_sync(0xffffffffu, wt);
+  const uint32_t before = __reduce_add_sync(0xffffffffu, lane < warp ? wt : 0u);
+  return before + inc - v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_kernel(const float* __restrict__ scores, long long stride,
-                const int32_t* __restrict__ kv_len, int budget, int max_kv_len,
-                int smem_blocks, int32_t* __restrict__ ids, int32_t* err) {
-  extern __shared__ uint32_t s_key[];  // smem_blocks keys: the row's block keys, when they fit
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t wsum[32];
-  __shared__ uint32_t s_digit, s_need;
+__global__ void __launch_bounds__(kSelThreads)
+    select_cells_kernel(const float* __restrict__ scores, long long stride,
+                        const int32_t* __restrict__ kv_len, int budget, int max_kv_len,
+                        int stage_cap, int32_t* __restrict__ ids, int32_t* err) {
+  extern __shared__ uint32_t staged[];
+  __shared__ uint32_t slots[2][kSelWarps];
   const int t = blockIdx.x, tid = threadIdx.x;
-  int n_kv = __ldg(kv_len + t);
-  if (n_kv < 0 || n_kv > max_kv_len) {
+  int n = __ldg(kv_len + t);
+  if (n < 0 || n > max_kv_len) {
     if (tid == 0) flag_error(err, GQA_ERR_KVLEN_RANGE);
-    n_kv = n_kv < 0 ? 0 : max_kv_len;
+    n = n < 0 ? 0 : max_kv_len;
   }
   int32_t* out = ids + (size_t)t * budget;
-  if (n_kv <= budget) {  // every cell, then -1 padding
-    for (int c = tid; c < budget; c += kTopkThreads) out[c] = c < n_kv ? c : -1;
+  if (n <= budget) {  // every cell, then -1
+    for (int i = tid; i < budget; i += kSelThreads) out[i] = i < n ? i : -1;
     return;
   }
+  const int nb = (n + 3) >> 2;  // blocks; the last one may hold fewer than 4 cells
   const float* row = scores + (size_t)t * stride;
-  const int nfull = n_kv >> 2, nb = nfull + 1, tail = n_kv & 3;
-  const bool staged = nb <= smem_blocks;
-  if (staged) {
-    for (int b = tid; b < nb; b += kTopkThreads) s_key[b] = order_key(__ldg(row + b));
+  const bool stage = nb <= stage_cap;
+  if (stage) {
+    for (int b = tid; b < nb; b += kSelThreads) staged[b] = monotone_key(__ldg(row + b));
     __syncthreads();
   }
-  auto key = [&](int b) { return staged ? s_key[b] : order_key(__ldg(row + b)); };
+  auto key = [&](int b) { return stage ? staged[b] : monotone_key(__ldg(row + b)); };
+  auto cells = [&](int b) { return static_cast<uint32_t>(min(4, n - 4 * b)); };
+  int sn = 0;  // alternates the reduction slots
+  auto count_ge = [&](uint32_t c) {
+    uint32_t m = 0;
+    for (int b = tid; b < nb; b += kSelThreads)
+      if (key(b) >= c) m += cells(b);
+    return cta_sum(m, slots[sn++ & 1]);
+  };
 
-  uint32_t prefix = 0, pmask = 0, need = (uint32_t)budget;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0u;
-    __syncthreads();
-    for (int b = tid; b < nb; b += kTopkThreads) {
-      const uint32_t k = key(b);
-      const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
-      if (w && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], w);
-    }
-    __syncthreads();
-    // thread i < 256 holds bin 255 - i: the scan gives the cells in strictly higher bins
-    const uint32_t cnt = tid < 256 ? hist[255 - tid] : 0u;
-    uint32_t total;
-    const uint32_t above = block_exclusive_scan(cnt, wsum, &total);
-    if (tid < 256 && above < need && above + cnt >= need) {
-      s_digit = 255u - tid;
-      s_need = need - above;
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    pmask |= 255u << shift;
-    need = s_need;
+  // ---- 1. the threshold key: the largest T with ge(T) >= budget (ge(0) = n > budget)
+  const uint32_t want = static_cast<uint32_t>(budget);
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t c = T | (1u << bit);
+    if (count_ge(c) >= want) T = c;
   }
-  const uint32_t T = prefix;  // the threshold key; `need` cells at T are still wanted
+  const uint32_t above = T == 0xffffffffu ? 0u : count_ge(T + 1u);
+  const uint32_t need = want - above;  // cells taken from blocks at the threshold, >= 1
 
-  // emit: thread tid owns blocks [b0, b1), ascending with tid
-  const int per = (nb + kTopkThreads - 1) / kTopkThreads;
-  const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
-  uint32_t gt = 0, eq = 0;
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t k = key(b);
-    const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
-    if (k > T) gt += w;
-    else if (k == T) eq += w;
-  }
-  uint32_t total;
-  const uint32_t eq_before = block_exclusive_scan(eq, wsum, &total);
-  const uint32_t eq_take = eq_before >= need ? 0u : min(eq, need - eq_before);
-  uint32_t off = block_exclusive_scan(gt + eq_take, wsum, &total);
-  uint32_t left = eq_take;
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t k = key(b);
-    const uint32_t w = b < nfull ? 4u : (uint32_t)tail;
+  // ---- 2. the list, ascending: rounds of kSelThreads blocks, running totals carried over
+  uint32_t eq_seen = 0, placed = 0;
+  for (int r0 = 0; r0 < nb && placed < want; r0 += kSelThreads) {
+    const int b = r0 + tid;
+    const bool real = b < nb;
+    const uint32_t k = real ? key(b) : 0u;
+    const uint32_t w = real ? cells(b) : 0u;
+    uint32_t round_eq, round_taken;
+    const uint32_t eq_before = eq_seen + cta_exclusive(k == T ? w : 0u, slots[sn++ & 1], &round_eq);
     uint32_t take = 0;
-    if (k > T) {
-      take = w;
-    } else if (k == T) {
-      take = min(w, left);
-      left -= take;
-    }
-    for (uint32_t c = 0; c < take; ++c) out[off + c] = 4 * b + (int)c;
-    off += take;
+    if (real && k > T) take = w;
+    if (real && k == T && need > eq_before) take = min(w, need - eq_before);
+    const uint32_t at = placed + cta_exclusive(take, slots[sn++ & 1], &round_taken);
+    for (uint32_t i = 0; i < take; ++i) out[at + i] = 4 * b + static_cast<int>(i);
+    eq_seen += round_eq;
+    placed += round_taken;
   }
 }
 
 }  // namespace gqa
 
 namespace gqa {
-void set_last_error(const char* msg);          // host.cu: the text gqa_last_error() returns
+void set_last_error(const char* msg);               // host.cu: the text gqa_last_error() returns
 cudaError_t ensure_smem(const void* fn, int bytes);  // launch_util.cu: the opt-in, once
 }
 
-static gqa_status topk_fail(gqa_status s, const char* msg) {
+static gqa_status select_fail(gqa_status s, const char* msg) {
   gqa::set_last_error(msg);
   return s;
 }
@@ -160,25 +149,26 @@ extern "C" gqa_status attn_select_topk(const float* block_scores, int64_t score_
                                        int budget, int32_t* ids, int32_t* err_word,
                                        cudaStream_t stream) {
   if (n_tok < 0 || budget <= 0 || max_kv_len < 0)
-    return topk_fail(GQA_EINVAL, "attn_select_topk: needs n_tok >= 0, budget >= 1, max_kv_len >= 0");
+    return select_fail(GQA_EINVAL,
+                       "attn_select_topk: needs n_tok >= 0, budget >= 1, max_kv_len >= 0");
   if (n_tok == 0) return GQA_OK;
   if (!block_scores || !kv_len || !ids)
-    return topk_fail(GQA_EINVAL, "attn_select_topk: a required pointer is NULL");
+    return select_fail(GQA_EINVAL, "attn_select_topk: a required pointer is NULL");
   if (score_stride < (int64_t)max_kv_len / 4 + 1)
-    return topk_fail(GQA_EINVAL, "attn_select_topk: score_stride < max_kv_len / 4 + 1");
-  // the staged keys: room for the longest row's blocks if they fit, else none (a row stages
-  // only when its own block count fits the room launched)
+    return select_fail(GQA_EINVAL, "attn_select_topk: score_stride < max_kv_len / 4 + 1");
+  // room for the longest row's keys when they fit the staging limit, else none: a row is staged
+  // only when its own block count fits the room launched
   const int nb_max = max_kv_len / 4 + 1;
-  const int smem_blocks = nb_max <= gqa::kTopkSmemBlocks ? nb_max : 0;
-  if (smem_blocks > 0) {  // the opt-in past 48 KB (static + dynamic), once, at the largest size
-    const cudaError_t e = gqa::ensure_smem(reinterpret_cast<const void*>(gqa::topk_kernel),
-                                           gqa::kTopkSmemBlocks * sizeof(uint32_t));
-    if (e != cudaSuccess) return topk_fail(GQA_ECUDA, cudaGetErrorString(e));
+  const int stage_cap = nb_max <= gqa::kSelStageBlocks ? nb_max : 0;
+  if (stage_cap > 0) {  // the opt-in past 48 KB, once, at the largest size
+    const cudaError_t e = gqa::ensure_smem(reinterpret_cast<const void*>(gqa::select_cells_kernel),
+                                           gqa::kSelStageBlocks * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return select_fail(GQA_ECUDA, cudaGetErrorString(e));
   }
-  gqa::topk_kernel<<<n_tok, gqa::kTopkThreads, (size_t)smem_blocks * sizeof(uint32_t), stream>>>(
-      block_scores, (long long)score_stride, kv_len, budget, max_kv_len, smem_blocks, ids,
-      err_word);
+  gqa::select_cells_kernel<<<n_tok, gqa::kSelThreads, (size_t)stage_cap * sizeof(uint32_t),
+                             stream>>>(block_scores, (long long)score_stride, kv_len, budget,
+                                       max_kv_len, stage_cap, ids, err_word);
   const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return topk_fail(GQA_ECUDA, cudaGetErrorString(e));
+  if (e != cudaSuccess) return select_fail(GQA_ECUDA, cudaGetErrorString(e));
   return GQA_OK;
 }

@@ -156,7 +156,7 @@ __device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, i
       rot(a, head, lane);
       float* o = p.out + ((size_t)t * p.n_heads + head) * D + lane * DPL;
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) o[k] = a[k];
+      for (int k = 0; k < DPL; ++k) o[k] = gated(p, t, head, lane * DPL + k, a[k]);
     }
   }
   if (p.merge)

@@ -214,15 +214,16 @@ static gqa_status tq_fail(gqa_status st, const char* msg) {
 
 static bool tq_aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
-                                     const uint32_t* k_polar, const uint32_t* k_jl,
-                                     const uint32_t* k_norms, const uint32_t* v_polar,
-                                     const uint32_t* v_norms, const float* centroids,
-                                     const float* signs, float qjl_scale, float scale, float* out,
-                                     const int32_t* kv_len, const int32_t* seq_of, int n_tok,
-                                     int n_seq, int n_heads, int n_kv_heads, int head_dim,
-                                     int64_t cache_cap, int max_kv_len, void* ws, size_t ws_bytes,
-                                     int32_t* err_word, cudaStream_t stream) {
+static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t* k_polar,
+                           const uint32_t* k_jl, const uint32_t* k_norms, const uint32_t* v_polar,
+                           const uint32_t* v_norms, const float* centroids, const float* signs,
+                           float qjl_scale, float scale, float* out, const int32_t* kv_len,
+                           const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                           int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                           void* ws, size_t ws_bytes, int32_t* err_word, cudaStream_t stream,
+                           const float* gate, int64_t gate_stride) {
+  if (gate && (gate_stride < head_dim || (reinterpret_cast<uintptr_t>(gate) & 3)))
+    return tq_fail(GQA_EINVAL, "attn_decode_tq: gate 4-byte aligned, gate_stride >= head_dim");
   if (head_dim != 32 && head_dim != 64 && head_dim != 128)
     return tq_fail(GQA_EINVAL, "attn_decode_tq: head_dim must be 32, 64 or 128");
   if (n_kv_heads <= 0 || n_heads % n_kv_heads)
@@ -269,6 +270,8 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
   p.n_split = plan.n_split;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.merge = plan.merge;
+  p.gate = gate;
+  p.gate_stride = gate ? gate_stride : 0;
   if (plan.merge) {
     const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);
@@ -302,4 +305,32 @@ extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
   return GQA_OK;
+}
+
+extern "C" gqa_status attn_decode_tq(const float* q_rot, const float* q_jl,
+                                     const uint32_t* k_polar, const uint32_t* k_jl,
+                                     const uint32_t* k_norms, const uint32_t* v_polar,
+                                     const uint32_t* v_norms, const float* centroids,
+                                     const float* signs, float qjl_scale, float scale, float* out,
+                                     const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                     int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                     int64_t cache_cap, int max_kv_len, void* ws, size_t ws_bytes,
+                                     int32_t* err_word, cudaStream_t stream) {
+  return tq_entry(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, signs,
+                  qjl_scale, scale, out, kv_len, seq_of, n_tok, n_seq, n_heads, n_kv_heads,
+                  head_dim, cache_cap, max_kv_len, ws, ws_bytes, err_word, stream, nullptr, 0);
+}
+
+extern "C" gqa_status attn_decode_tq_gated(
+    const float* q_rot, const float* q_jl, const uint32_t* k_polar, const uint32_t* k_jl,
+    const uint32_t* k_norms, const uint32_t* v_polar, const uint32_t* v_norms,
+    const float* centroids, const float* signs, float qjl_scale, float scale, float* out,
+    const int32_t* kv_len, const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+    int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len, const float* gate,
+    int64_t gate_stride, void* ws, size_t ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  if (!gate) return tq_fail(GQA_EINVAL, "attn_decode_tq_gated: gate is NULL");
+  return tq_entry(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, signs,
+                  qjl_scale, scale, out, kv_len, seq_of, n_tok, n_seq, n_heads, n_kv_heads,
+                  head_dim, cache_cap, max_kv_len, ws, ws_bytes, err_word, stream, gate,
+                  gate_stride);
 }

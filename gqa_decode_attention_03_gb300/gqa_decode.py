@@ -24,7 +24,8 @@ ERR_KVLEN_RANGE, ERR_ID_RANGE, ERR_SEQ_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 EXPORTS = ("attn_decode_plan", "attn_decode_workspace_bytes", "attn_decode_f16",
            "attn_decode_q8_sel", "attn_merge", "gqa_status_string", "gqa_last_error",
            "gqa_abi_version", "attn_decode_f16_noalloc", "attn_select_topk", "kv_append_q8", "attn_merge_gated",
-           "attn_decode_tq", "attn_decode_q8_sel_sg", "kv_append_q8_sg")
+           "attn_decode_tq", "attn_decode_q8_sel_sg", "kv_append_q8_sg", "attn_decode_f16_gated",
+           "attn_decode_q8_sel_gated", "attn_decode_tq_gated")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_decode.h
 
 
@@ -72,6 +73,15 @@ def _load():
     lib.attn_decode_tq.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(F), P, F, F, P, P, P, I,
                                    I, I, I, I, I64, I, P, SZ, P, P]
     lib.attn_decode_tq.restype = I
+    lib.attn_decode_f16_gated.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I64, I, F, P, I64, P,
+                                          SZ, P, P]
+    lib.attn_decode_f16_gated.restype = I
+    lib.attn_decode_q8_sel_gated.argtypes = [P, P, P, P, P, I, P, I, P, P, P, I, I, I, I, I, I64,
+                                             I, F, P, I64, P, SZ, P, P]
+    lib.attn_decode_q8_sel_gated.restype = I
+    lib.attn_decode_tq_gated.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(F), P, F, F, P, P, P,
+                                         I, I, I, I, I, I64, I, P, I64, P, SZ, P, P]
+    lib.attn_decode_tq_gated.restype = I
     lib.attn_merge.argtypes = [P, P, I, I, I, I, P, P]
     lib.attn_merge.restype = I
     lib.gqa_status_string.argtypes = [I]
@@ -113,6 +123,21 @@ def _need(x, dtype, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {x.dim()}")
 
 
+def _gate_args(gate, gate_stride, T, H, D):
+    """(gate, stride) checked for the gated entry points: fp32 on the device, element (t, h, d)
+    at flat index (t*H + h)*stride + d (stride default D; 2*D over [query | gate] pairs)."""
+    if gate.dtype != torch.float32 or not gate.is_cuda:
+        raise TypeError("gate must be a CUDA fp32 tensor")
+    if not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
+    gs = D if gate_stride is None else int(gate_stride)
+    if gs < D:
+        raise ValueError("gate_stride must be >= head_dim")
+    if gate.numel() < (T * H - 1) * gs + D:
+        raise ValueError("gate too small for its stride")
+    return gs
+
+
 def plan(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1, kind=KIND_F16, num_sms=0,
          n_seq=None):
     """The split plan the decode calls use (host only; num_sms 0 queries the device).
@@ -138,11 +163,12 @@ def alloc_workspace(n_tok, n_heads, n_kv_heads, head_dim, max_kv_len, budget=-1,
 
 
 def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv_len=None,
-                    out=None, ws=None, err=None, stream=None):
+                    out=None, ws=None, err=None, stream=None, gate=None, gate_stride=None):
     """Decode attention over an f16 cache; returns ``out [T][H][D]`` fp32.
 
     q [T][H][D] fp32; k_cache, v_cache [n_seq][cap][Hk][D] fp16; kv_len [T] int32 (device);
     seq_of [T] int32 or None; max_kv_len: host bound of kv_len (default: the cache capacity).
+    gate: optional fp32 sigmoid output gate (attn_decode_f16_gated), see ``_gate_args``.
     """
     _need(q, torch.float32, "q", 3)
     _need(k_cache, torch.float16, "k_cache", 4)
@@ -163,6 +189,14 @@ def attn_decode_f16(q, k_cache, v_cache, kv_len, scale=None, seq_of=None, max_kv
     _need(out, torch.float32, "out", 3)
     if ws is None:
         ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_F16, q.device, n_seq)
+    if gate is not None:
+        gs = _gate_args(gate, gate_stride, T, H, D)
+        _check(LIB.attn_decode_f16_gated(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                         _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
+                                         max_kv_len, scale, _ptr(gate), gs, _ptr(ws),
+                                         ws.numel() * ws.element_size(), _ptr(err),
+                                         _stream(stream)))
+        return out
     _check(LIB.attn_decode_f16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(kv_len),
                                _ptr(seq_of), T, n_seq, H, Hk, D, cap, max_kv_len, scale, _ptr(ws),
                                ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
@@ -195,7 +229,7 @@ def attn_decode_f16_noalloc(q, k_cache, v_cache, kv_len, scale=None, seq_of=None
 
 def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centroids, signs,
                    qjl_scale, kv_len, scale=None, seq_of=None, max_kv_len=None, out=None, ws=None,
-                   err=None, stream=None):
+                   err=None, stream=None, gate=None, gate_stride=None):
     """Decode attention over a TurboQuant-compressed cache; returns ``out [T][H][D]`` fp32.
 
     q_rot, q_jl [T][H][D] fp32 (the rotated and JL-projected query); packed words as int32 bit
@@ -227,6 +261,16 @@ def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centro
     _need(out, torch.float32, "out", 3)
     if ws is None:
         ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), -1, KIND_TQ, q_rot.device, n_seq)
+    if gate is not None:
+        gs = _gate_args(gate, gate_stride, T, H, D)
+        _check(LIB.attn_decode_tq_gated(_ptr(q_rot), _ptr(q_jl), _ptr(k_polar), _ptr(k_jl),
+                                        _ptr(k_norms), _ptr(v_polar), _ptr(v_norms), cents,
+                                        _ptr(signs), float(qjl_scale), scale, _ptr(out),
+                                        _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
+                                        max_kv_len, _ptr(gate), gs, _ptr(ws),
+                                        ws.numel() * ws.element_size(), _ptr(err),
+                                        _stream(stream)))
+        return out
     _check(LIB.attn_decode_tq(_ptr(q_rot), _ptr(q_jl), _ptr(k_polar), _ptr(k_jl), _ptr(k_norms),
                               _ptr(v_polar), _ptr(v_norms), cents, _ptr(signs), float(qjl_scale),
                               scale, _ptr(out), _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D,
@@ -236,7 +280,8 @@ def attn_decode_tq(q_rot, q_jl, k_polar, k_jl, k_norms, v_polar, v_norms, centro
 
 
 def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale=None,
-                       seq_of=None, max_kv_len=None, out=None, ws=None, err=None, stream=None):
+                       seq_of=None, max_kv_len=None, out=None, ws=None, err=None, stream=None,
+                       gate=None, gate_stride=None):
     """Decode attention over an int8 cache with per-64-dim f16 scales; optional selected ids.
 
     kq, vq [n_seq][cap][Hk][D] int8; ksc, vsc [n_seq][cap][Hk][D/G] fp16, one scale per G = 64
@@ -271,6 +316,15 @@ def attn_decode_q8_sel(q, kq, vq, ksc, vsc, kv_len, ids=None, budget=None, scale
     _need(out, torch.float32, "out", 3)
     if ws is None:
         ws = alloc_workspace(T, H, Hk, D, min(max_kv_len, cap), b, KIND_Q8, q.device, n_seq)
+    if gate is not None:
+        gs = _gate_args(gate, gate_stride, T, H, D)
+        _check(LIB.attn_decode_q8_sel_gated(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), sg,
+                                            _ptr(ids), 0 if ids is None else budget, _ptr(out),
+                                            _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,
+                                            max_kv_len, scale, _ptr(gate), gs, _ptr(ws),
+                                            ws.numel() * ws.element_size(), _ptr(err),
+                                            _stream(stream)))
+        return out
     _check(LIB.attn_decode_q8_sel_sg(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ksc), _ptr(vsc), sg,
                                      _ptr(ids), 0 if ids is None else budget, _ptr(out),
                                      _ptr(kv_len), _ptr(seq_of), T, n_seq, H, Hk, D, cap,

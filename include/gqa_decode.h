@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 8
+#define GQA_ABI_VERSION 9
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -317,6 +317,48 @@ gqa_status attn_decode_f16_noalloc(const float* q, const uint16_t* k_cache,
 gqa_status attn_merge_gated(const float* part, const int32_t* n_valid, int n_split, int n_tok,
                             int n_heads, int head_dim, const float* gate, int64_t gate_stride,
                             float* out, cudaStream_t stream);
+
+/*
+ * The decode calls with the sigmoid output gate applied to every output row.  Both model pages
+ * end their decode step with it, after the merge: qsa2.metal (regolith) qsa_merge2 and
+ * FORWARD_MSL (cherenkov docs) attn_combine multiply the merged row by sigmoid(gate), the gate
+ * being the second half of each head's [query | gate] pair.  Here:
+ *   out[t][h][d] = attention(t, h)[d] / (1 + exp(-gate[(t * n_heads + h) * gate_stride + d]))
+ * whether the row was split (the gate is applied by whichever kernel merges it) or not (by the
+ * kernel that writes it); empty rows stay 0.  For TurboQuant caches the gate applies to the
+ * row rotated back.
+ *   gate          device fp32, 4-byte aligned, not NULL
+ *   gate_stride   floats between consecutive (row, head) gate vectors, >= head_dim: head_dim
+ *                 for a plain [n_tok][n_heads][head_dim] gate; 2 * head_dim with
+ *                 gate = qfull + head_dim for the pages' per-head [query | gate] pairs
+ * Other arguments, layouts, workspaces and errors as the ungated call (attn_decode_f16,
+ * attn_decode_q8_sel_sg, attn_decode_tq); a bad gate or stride gives GQA_EINVAL.
+ */
+gqa_status attn_decode_f16_gated(const float* q, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, float* out, const int32_t* kv_len,
+                                 const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                                 int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                                 float scale, const float* gate, int64_t gate_stride, void* ws,
+                                 size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+gqa_status attn_decode_q8_sel_gated(const float* q, const int8_t* kq, const int8_t* vq,
+                                    const uint16_t* ksc, const uint16_t* vsc, int scale_group,
+                                    const int32_t* ids, int budget, float* out,
+                                    const int32_t* kv_len, const int32_t* seq_of, int n_tok,
+                                    int n_seq, int n_heads, int n_kv_heads, int head_dim,
+                                    int64_t cache_cap, int max_kv_len, float scale,
+                                    const float* gate, int64_t gate_stride, void* ws,
+                                    size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+gqa_status attn_decode_tq_gated(const float* q_rot, const float* q_jl, const uint32_t* k_polar,
+                                const uint32_t* k_jl, const uint32_t* k_norms,
+                                const uint32_t* v_polar, const uint32_t* v_norms,
+                                const float* centroids, const float* signs, float qjl_scale,
+                                float scale, float* out, const int32_t* kv_len,
+                                const int32_t* seq_of, int n_tok, int n_seq, int n_heads,
+                                int n_kv_heads, int head_dim, int64_t cache_cap, int max_kv_len,
+                                const float* gate, int64_t gate_stride, void* ws,
+                                size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
 
 /* Human-readable name of a status; static storage. */
 const char* gqa_status_string(gqa_status s);

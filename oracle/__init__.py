@@ -22,6 +22,7 @@ from .gqa_oracle import (  # noqa: F401
     gated_merge,
     lse_merge,
     order_key,
+    output_gate,
     quantize_q8,
     select_topk_cells,
     selected_positions,

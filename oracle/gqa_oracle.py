@@ -31,7 +31,8 @@ Passages followed (page title, then the part of it):
   * flash_attention_tq.metal (cera 0.4.0 sources): decode over a TurboQuant cache (PolarQuant
     centroid dot plus QJL sign correction, rotated-space accumulation, inverse Hadamard).
 
-Readings taken where the pages leave a step open are listed in DESIGN.md ("Readings").
+Where the pages leave a step open, the reading taken is stated in the docstring of the function
+that takes it.
 """
 
 from __future__ import annotations
@@ -302,12 +303,18 @@ def quantize_q8(x, group: int = SCALE_GROUP) -> tuple[np.ndarray, np.ndarray]:
     return q, d.astype(np.float16)
 
 
+def output_gate(out, gate) -> np.ndarray:
+    """The sigmoid output gate both model pages apply to an attention row after the merge
+    (qsa2.metal, qsa_merge2; FORWARD_MSL, attn_combine): out * 1 / (1 + exp(-gate)), element by
+    element; gate [T][H][D] is the second half of each head's [query | gate] pair there."""
+    g = np.asarray(gate, np.float64)
+    return np.asarray(out, np.float64) * (1.0 / (1.0 + np.exp(-g)))
+
+
 def gated_merge(acc, m, l, n_valid, gate) -> np.ndarray:
     """The merge followed by the sigmoid output gate (qsa2.metal, qsa_merge2; FORWARD_MSL,
-    attn_combine): out = lse_merge(...) * 1 / (1 + exp(-gate)), gate [T][H][D] (the second half
-    of each head's [query | gate] pair on those pages)."""
-    g = np.asarray(gate, np.float64)
-    return lse_merge(acc, m, l, n_valid) * (1.0 / (1.0 + np.exp(-g)))
+    attn_combine): output_gate(lse_merge(...), gate)."""
+    return output_gate(lse_merge(acc, m, l, n_valid), gate)
 
 
 # ----------------------------------------------------------------------------- TurboQuant KV

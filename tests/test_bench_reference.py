@@ -63,3 +63,10 @@ def test_reference_arm_prints_its_line(workload):
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"]
+
+
+def test_cpu_baseline_uses_every_host_core():
+    b = bench.cpu_baseline("tiny", budget_s=2.0)
+    assert b["kind"] == "oracle" and b["value"] > 0
+    assert b["cores"] == bench._cores() and b["host_cores"] == os.cpu_count()
+    assert b["single_core"]["cores"] == 1 and b["single_core"]["value"] > 0

@@ -60,11 +60,11 @@ def test_topk_feeds_the_selected_int8_path():
     assert_close(got, oracle_ref(case), TOL_Q8, "topk -> q8_sel")
 
 
-@pytest.mark.parametrize("max_kv", [49147, 60001, 196604, 196608, 200003])
+@pytest.mark.parametrize("max_kv", [49147, 200003, 212988, 212992, 260001])
 def test_topk_staged_and_unstaged_rows(max_kv):
-    """Rows whose block keys fit the shared-memory staging (max_kv_len / 4 + 1 <= 49152 blocks,
+    """Rows whose block keys fit the shared-memory staging (max_kv_len / 4 + 1 <= 53248 blocks,
     past the 48 KB that needs no opt-in) and rows past it, which read the keys from global
-    memory every pass."""
+    memory at every step of the threshold search."""
     kv_len = np.array([max_kv, max_kv - 3, 20000, 700, 0], np.int32)
     stride = max_kv // 4 + 1
     scores = W.make_block_scores(720 + max_kv % 97, len(kv_len), stride, 29)
@@ -73,3 +73,25 @@ def test_topk_staged_and_unstaged_rows(max_kv):
                                  err=err).cpu().numpy()
     assert int(err.item()) == 0
     assert np.array_equal(got, _oracle_ids(scores, kv_len, 2048))
+
+
+def test_topk_nan_scores_rank_at_the_ends():
+    """NaN scores rank through the same bit-pattern map: a positive NaN above +inf, a negative
+    one below -inf."""
+    s = np.array([[np.nan, 1.0, -np.nan, np.inf, 0.5, -np.inf, 2.0, 0.0]], np.float32)
+    s[0, 2] = -np.float32(np.nan)
+    kv_len = np.array([31, 31], np.int32)
+    s = np.concatenate([s, s[:, ::-1].copy()])
+    for budget in (1, 4, 5, 13, 30):
+        got = _gd().attn_select_topk(dev(s), dev(kv_len), budget, max_kv_len=31).cpu().numpy()
+        assert np.array_equal(got, _oracle_ids(s, kv_len, budget)), budget
+
+
+def test_topk_kv_len_out_of_range_is_clamped_and_flagged():
+    kv_len = np.array([-5, 900, 40], np.int32)
+    scores = W.make_block_scores(731, 3, 200 // 4 + 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _gd().attn_select_topk(dev(scores), dev(kv_len), 16, max_kv_len=200,
+                                 err=err).cpu().numpy()
+    assert int(err.item()) & _gd().ERR_KVLEN_RANGE
+    assert np.array_equal(got, _oracle_ids(scores, np.array([0, 200, 40]), 16))

@@ -37,7 +37,8 @@ def test_library_exports_every_declared_symbol(gd):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in the header but not exported"
     assert set(declared_functions()) <= set(gd.EXPORTS) | set(declared_functions())
-    assert gd.LIB.gqa_abi_version() == 8
+    assert gd.LIB.gqa_abi_version() == 9
+    assert set(gd.EXPORTS) == set(declared_functions())
 
 
 def test_status_strings(gd):

@@ -337,6 +337,25 @@ def test_gated_merge_closed_forms():
     assert np.allclose(oracle.gated_merge(acc, m, l, [2], g), 0.75 * base, rtol=1e-14)
 
 
+def test_output_gate_closed_forms():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2, 3, 64))
+    g = rng.standard_normal((2, 3, 64)) * 4
+    # sigmoid(g) + sigmoid(-g) = 1: the two gated rows add back to the row
+    assert np.allclose(oracle.output_gate(x, g) + oracle.output_gate(x, -g), x, rtol=1e-14,
+                       atol=1e-15)
+    assert np.array_equal(oracle.output_gate(x, np.zeros_like(g)), x / 2)  # sigmoid(0) = 1/2
+    assert np.allclose(oracle.output_gate(x, np.full_like(g, np.log(3.0))), 0.75 * x,
+                       rtol=1e-14)  # sigmoid(ln 3) = 3/4
+    assert np.allclose(oracle.output_gate(x, np.full_like(g, -np.log(3.0))), 0.25 * x,
+                       rtol=1e-13)
+    # element by element: one gate entry moves one output entry
+    g2 = np.zeros_like(g)
+    g2[1, 2, 7] = np.log(3.0)
+    d = oracle.output_gate(x, g2) - x / 2
+    assert np.count_nonzero(np.abs(d) > 1e-15) == 1 and abs(d[1, 2, 7] - 0.25 * x[1, 2, 7]) < 1e-14
+
+
 # ----------------------------------------------------------------------------- TurboQuant
 
 def _tq_oracle(c, rows=None):
