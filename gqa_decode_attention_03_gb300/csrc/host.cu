@@ -135,7 +135,11 @@ Variant pick_variant(int heads_per_cta) {
 // size that gets there -- so a wide group (12 heads) spreads over three times as many CTAs.
 // The tensor-core kernels serve the whole group in one CTA.
 int head_split_for(int kind, int group) {
-  if (kind == GQA_KIND_TQ) return 1;  // the TurboQuant kernel serves the whole group
+  if (kind == GQA_KIND_TQ) {  // the TurboQuant kernels serve up to 8 heads of a group per CTA
+    for (int hs = 1; hs <= group; ++hs)
+      if (group % hs == 0 && group / hs <= 8) return hs;
+    return group;
+  }
   const char* k = std::getenv("GQA_F16_KERNEL");
   const bool fma = kind == GQA_KIND_Q8 || (k && std::strcmp(k, "fma") == 0);
   if (!fma) return 1;
@@ -376,6 +380,8 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.merge = plan.merge;
   p.gate = gate;
   p.gate_stride = gate ? gate_stride : 0;
+  p.even_split = env_int("GQA_EVEN_SPLIT") > 0 ? 1 : 0;
+  p.longest_first = env_int("GQA_LONGEST_FIRST") > 0 && n_tok <= 64 ? 1 : 0;
   if (plan.streamk) {  // ws = [arrival counters][piece records]
     const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
     p.counters = static_cast<unsigned int*>(ws);
@@ -411,6 +417,16 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
 
   p.head_split = plan.streamk ? 1 : plan.grid_y / n_kv_heads;
   gqa::Variant var = gqa::pick_variant(p.group / p.head_split);
+  {
+    // int8 grids smaller than the GPU (a few rows of selected cells) are latency-bound: eight
+    // row slices per stage give each CTA twice the consumer warps (GB300, the 1024-of-8192
+    // selected-cell workload: 17.0 us per step against 18.9 with four)
+    st = GQA_OK;
+    const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
+    if (kind == GQA_KIND_Q8 && var.gw == 4 && var.nps == 4 && !plan.streamk &&
+        ctas < current_sm_count(&st))
+      var.nps = 8;
+  }
   const int nhg = (p.group / p.head_split + var.gw - 1) / var.gw;
   const int threads = 32 * (nhg * var.nps + 1);
   // f16 caches run on the tensor cores unless GQA_F16_KERNEL=fma asks for the CUDA-core kernel

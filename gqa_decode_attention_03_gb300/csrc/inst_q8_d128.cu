@@ -19,6 +19,7 @@ cudaError_t launch_partial_q8_d128(Variant v, const CUtensorMap& tk, const CUten
                                     const PartialParams& p, dim3 grid, int threads,
                                     cudaStream_t s) {
   constexpr Kind K = Kind::Q8;
+  if (v.nps == 8) return launch_one<K, 128, 4, 8>(tk, tv, p, grid, threads, s);
   if (v.nps == 4) {
     if (v.gw == 1) return launch_one<K, 128, 1, 4>(tk, tv, p, grid, threads, s);
     if (v.gw == 2) return launch_one<K, 128, 2, 4>(tk, tv, p, grid, threads, s);

@@ -61,6 +61,9 @@ struct PartialParams {
                            // before it gives up (kSpinLimit unless a test asks for fewer)
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at
   long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
+  int even_split;          // f16 tensor-core kernel: a row's ceil(L / chunk) chunks are made
+                           // equal (rounded up to whole stages) instead of chunk, ..., remainder
+  int longest_first;       // f16 tensor-core kernel: grid.z walks the rows longest first
 };
 
 // The sigmoid output gate that both pages apply to the merged row (qsa2.metal, qsa_merge2;
@@ -331,7 +334,9 @@ __device__ __forceinline__ void produce_tma(const CUtensorMap* tmK, const CUtens
 
 // int8: the 32 lanes gather the chunk's rows (through the id list when there is one) with
 // cp.async; a row whose id lies outside [0, L) is flagged, masked, and filled from cell 0 so
-// the staged bytes stay finite.
+// the staged bytes stay finite.  The ids of tile i + 1 are loaded before tile i's copies are
+// issued (a lane's rows of a tile at once), so their latency overlaps the copies instead of
+// preceding each row's.
 template <class C, int D>
 __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* stages,
                                                uint64_t* full, uint64_t* empty, int ntiles,
@@ -339,10 +344,22 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
                                                int lane) {
   const uint8_t* kq = static_cast<const uint8_t*>(p.kc);
   const uint8_t* vq = static_cast<const uint8_t*>(p.vc);
+  constexpr int RPL = C::TP / 32;  // rows of a tile per lane
+  static_assert(C::TP % 32 == 0, "whole rows per lane");
+  auto fetch = [&](int i, int (&cell)[RPL]) {  // the visited-list entries of tile i
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int j = c0 + i * C::TP + lane + 32 * k;
+      cell[k] = j < c1 ? (p.ids ? __ldg(p.ids + (size_t)t * p.budget + j) : j) : 0;
+    }
+  };
+  int cur[RPL], nxt[RPL];
+  fetch(0, cur);
   int issued = 0;
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % C::NST;
+    if (i + 1 < ntiles) fetch(i + 1, nxt);
     if (i >= C::NST) {
       const bool w = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::NST) - 1) & 1));
       if (!w) {
@@ -355,11 +372,13 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
     __half* skc = reinterpret_cast<__half*>(sk + C::KV_BYTES);
     __half* svc = skc + C::TP * C::NSC;
     int* rowok = reinterpret_cast<int*>(sk + C::KV_BYTES + C::SC_BYTES);
-    for (int r = lane; r < C::TP; r += 32) {
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int r = lane + 32 * k;
       const int j = c0 + i * C::TP + r;  // index into the visited list
       int okr = 0;
       if (j < c1) {
-        int cell = p.ids ? __ldg(p.ids + (size_t)t * p.budget + j) : j;
+        int cell = cur[k];
         okr = (cell >= 0 && cell < L);
         if (!okr) {
           flag_error(p.err, GQA_ERR_ID_RANGE);
@@ -395,6 +414,8 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
     mbar_arrive(&full[st]);            // releases rowok and the plain scale stores
     cp_async_arrive_noinc(&full[st]);  // fires once this lane's copies have landed
     issued = i + 1;
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) cur[k] = nxt[k];
   }
   if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
   for (int st = 0; st < C::NST && st < issued; ++st) {

@@ -10,16 +10,20 @@
 // How it is found here -- one CTA of kSelThreads threads per row:
 //   1. The threshold.  Let ge(c) be the number of cells whose key is >= c.  The threshold T is
 //      the largest key value with ge(T) >= budget, i.e. the key of the budget-th cell in
-//      descending order.  It is found by a binary search on the 32-bit key value, one bit per
-//      step from the most significant: each step counts ge(candidate) over the row with one
-//      CTA-wide sum (a warp reduction, one barrier).  One more count gives ge(T + 1), the cells
-//      strictly above T; the remaining need = budget - ge(T + 1) cells come from blocks whose
-//      key equals T, lowest cells first.
-//   2. The list.  Blocks are visited in ascending order, kSelThreads of them per round (block
-//      r * kSelThreads + tid in round r).  A CTA-wide exclusive scan of the cells at key T gives
-//      each block the number of such cells before it, hence how many of its own it takes; a
-//      second scan of the taken cells gives each block its place in the output.  Both running
-//      totals carry over to the next round.
+//      descending order.  It is built eight bits at a time from the most significant.  At the
+//      step for bits sh .. sh + 7, a block whose key agrees with T above them adds its cells to
+//      bin `digit` of its warp's 257-bin histogram (shared atomics), a block whose higher bits
+//      already exceed T's to bin 256; the others count for nothing.  The warps' bins are summed
+//      and a CTA scan turns them into suffix sums, ge(T + j 2^sh) for every candidate digit j;
+//      the digit is the one whose suffix still holds budget cells while the next one's does
+//      not.  After the last step the next suffix is ge(T + 1), the cells strictly above T; the
+//      remaining need = budget - ge(T + 1) cells come from blocks whose key equals T, lowest
+//      cells first.
+//   2. The list.  Blocks are visited in ascending order in rounds of 4 kSelThreads blocks,
+//      four consecutive blocks a thread.  Exclusive scans (within the thread, then over the
+//      CTA) of the cells at key T give each block the number of such cells before it, hence how
+//      many of its own it takes; a second pair of scans of the taken cells gives each block its
+//      place in the output.  Both running totals carry over to the next round.
 // The row's block keys are staged in shared memory when its block count fits the room the
 // launch reserved; otherwise each step reads them from global memory (L2 after the first).
 // Integer work only: the list is a deterministic function of the keys.
@@ -32,7 +36,8 @@ namespace gqa {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelStageBlocks = 53248;  // 208 KB of staged keys: rows of up to 212,991 cells
+constexpr int kSelStageBlocks = 46080;  // 180 KB of staged keys: rows of up to 184,319 cells
+constexpr int kSelBins = 257;           // digits 0..255 of a step, and "above every candidate"
 
 // fp32 bit pattern -> uint32 whose unsigned order is the float order (-0 below +0; NaNs at the
 // ends): negative values have every bit flipped, the others get the sign bit set.
@@ -41,18 +46,9 @@ __device__ __forceinline__ uint32_t monotone_key(float x) {
   return (u & 0x80000000u) ? ~u : (u ^ 0x80000000u);
 }
 
-// The CTA-wide sum of v, returned to every thread.  One barrier; `slot` (kSelWarps words) must
-// not be the slot of the previous CTA-wide call (callers alternate two).
-__device__ __forceinline__ uint32_t cta_sum(uint32_t v, uint32_t* slot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = __reduce_add_sync(0xffffffffu, v);
-  if (lane == 0) slot[warp] = v;
-  __syncthreads();
-  return __reduce_add_sync(0xffffffffu, lane < kSelWarps ? slot[lane] : 0u);
-}
-
 // The exclusive prefix sum of v over the threads in thread order; *total gets the CTA's sum.
-// One barrier; slots as for cta_sum.
+// One barrier; `slot` (kSelWarps words or more) must not be the slot of the previous
+// CTA-wide call (callers alternate two).
 __device__ __forceinline__ uint32_t cta_exclusive(uint32_t v, uint32_t* slot, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = v;  // inclusive prefix within the warp
@@ -69,13 +65,17 @@ __device__ __forceinline__ uint32_t cta_exclusive(uint32_t v, uint32_t* slot, ui
   return before + inc - v;
 }
 
+// The first warp's row of a histogram that has been read: room for the 257 suffix sums.
+__device__ __forceinline__ uint32_t* staged_scratch(uint32_t (*h)[kSelBins]) { return h[0]; }
+
 __global__ void __launch_bounds__(kSelThreads)
     select_cells_kernel(const float* __restrict__ scores, long long stride,
                         const int32_t* __restrict__ kv_len, int budget, int max_kv_len,
                         int stage_cap, int32_t* __restrict__ ids, int32_t* err) {
   extern __shared__ uint32_t staged[];
   __shared__ uint32_t slots[2][kSelWarps];
-  const int t = blockIdx.x, tid = threadIdx.x;
+  __shared__ uint32_t hist[2][kSelWarps][kSelBins];  // per-warp digit histograms, two steps
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int n = __ldg(kv_len + t);
   if (n < 0 || n > max_kv_len) {
     if (tid == 0) flag_error(err, GQA_ERR_KVLEN_RANGE);
@@ -89,44 +89,90 @@ __global__ void __launch_bounds__(kSelThreads)
   const int nb = (n + 3) >> 2;  // blocks; the last one may hold fewer than 4 cells
   const float* row = scores + (size_t)t * stride;
   const bool stage = nb <= stage_cap;
-  if (stage) {
+  for (int i = lane; i < kSelBins; i += 32) hist[0][warp][i] = hist[1][warp][i] = 0u;
+  if (stage)
     for (int b = tid; b < nb; b += kSelThreads) staged[b] = monotone_key(__ldg(row + b));
-    __syncthreads();
-  }
+  __syncthreads();
   auto key = [&](int b) { return stage ? staged[b] : monotone_key(__ldg(row + b)); };
   auto cells = [&](int b) { return static_cast<uint32_t>(min(4, n - 4 * b)); };
   int sn = 0;  // alternates the reduction slots
-  auto count_ge = [&](uint32_t c) {
-    uint32_t m = 0;
-    for (int b = tid; b < nb; b += kSelThreads)
-      if (key(b) >= c) m += cells(b);
-    return cta_sum(m, slots[sn++ & 1]);
-  };
 
-  // ---- 1. the threshold key: the largest T with ge(T) >= budget (ge(0) = n > budget)
+  // ---- 1. the threshold key, eight bits a step (ge(T) >= budget holds throughout: ge(0) = n)
+  __shared__ uint32_t pick[2];  // the step's digit and the cells above T + 2^sh
   const uint32_t want = static_cast<uint32_t>(budget);
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t c = T | (1u << bit);
-    if (count_ge(c) >= want) T = c;
+  uint32_t T = 0, above = 0;
+  for (int step = 0, sh = 24; sh >= 0; ++step, sh -= 8) {
+    // Bin of a block: its key's digit at sh (0 .. 255) when the key agrees with T above bit
+    // sh + 8, bin 256 when its higher bits already exceed T's (above every candidate), no bin
+    // when they fall short.  Cells go into the warp's own histogram by shared atomics.
+    uint32_t(*h)[kSelBins] = hist[step & 1];
+    const uint32_t hiT = sh == 24 ? 0u : T >> (sh + 8);
+    for (int b = tid; b < nb; b += kSelThreads) {
+      const uint32_t k = key(b);
+      const uint32_t hk = sh == 24 ? 0u : k >> (sh + 8);
+      if (hk >= hiT) atomicAdd(&h[warp][hk > hiT ? 256u : (k >> sh) & 255u], cells(b));
+    }
+    __syncthreads();
+    // thread i (< 257) gathers bin i over the warps; suf_i = cells in bins >= i, i.e.
+    // ge(T + i 2^sh) for the digits i = 1 .. 255, and the cells above every candidate for 256
+    uint32_t bin = 0;
+    if (tid < kSelBins)
+      for (int w = 0; w < kSelWarps; ++w) bin += h[w][tid];
+    uint32_t total;
+    const uint32_t suf = [&] {
+      const uint32_t before = cta_exclusive(bin, slots[sn++ & 1], &total);
+      return total - before;
+    }();
+    // the digit: the one i in 0 .. 255 with suf_i >= budget > suf_(i+1) (suf_0 >= budget, and
+    // suf does not grow with i); suf_256 sits in the slot of thread 256
+    uint32_t* sufs = staged_scratch(h);  // the histogram just read, reused for suf
+    __syncthreads();                     // every gather read of h is done
+    if (tid < kSelBins) sufs[tid] = suf;
+    __syncthreads();
+    if (tid < 256 && suf >= want && sufs[tid + 1] < want) {
+      pick[0] = tid;
+      pick[1] = sufs[tid + 1];
+    }
+    __syncthreads();
+    T |= pick[0] << sh;
+    above = pick[1];  // cells at or above T + 2^sh
+    // the other histogram was last read two barriers ago: clear it for the next step
+    for (int i = lane; i < kSelBins; i += 32) hist[(step + 1) & 1][warp][i] = 0u;
   }
-  const uint32_t above = T == 0xffffffffu ? 0u : count_ge(T + 1u);
   const uint32_t need = want - above;  // cells taken from blocks at the threshold, >= 1
 
-  // ---- 2. the list, ascending: rounds of kSelThreads blocks, running totals carried over
+  // ---- 2. the list, ascending: rounds of 4 kSelThreads blocks, 4 consecutive blocks a
+  //      thread, running totals carried over
+  constexpr int BPT = 4;
   uint32_t eq_seen = 0, placed = 0;
-  for (int r0 = 0; r0 < nb && placed < want; r0 += kSelThreads) {
-    const int b = r0 + tid;
-    const bool real = b < nb;
-    const uint32_t k = real ? key(b) : 0u;
-    const uint32_t w = real ? cells(b) : 0u;
+  for (int r0 = 0; r0 < nb && placed < want; r0 += BPT * kSelThreads) {
+    const int b0 = r0 + BPT * tid;
+    uint32_t k[BPT], w[BPT], eq_own = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      const bool real = b0 + i < nb;
+      k[i] = real ? key(b0 + i) : 0u;
+      w[i] = real ? cells(b0 + i) : 0u;
+      eq_own += k[i] == T ? w[i] : 0u;
+    }
     uint32_t round_eq, round_taken;
-    const uint32_t eq_before = eq_seen + cta_exclusive(k == T ? w : 0u, slots[sn++ & 1], &round_eq);
-    uint32_t take = 0;
-    if (real && k > T) take = w;
-    if (real && k == T && need > eq_before) take = min(w, need - eq_before);
-    const uint32_t at = placed + cta_exclusive(take, slots[sn++ & 1], &round_taken);
-    for (uint32_t i = 0; i < take; ++i) out[at + i] = 4 * b + static_cast<int>(i);
+    uint32_t eq_before = eq_seen + cta_exclusive(eq_own, slots[sn++ & 1], &round_eq);
+    uint32_t take[BPT], take_own = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      take[i] = k[i] > T ? w[i] : 0u;
+      if (k[i] == T) {
+        take[i] = need > eq_before ? min(w[i], need - eq_before) : 0u;
+        eq_before += w[i];
+      }
+      take_own += take[i];
+    }
+    uint32_t at = placed + cta_exclusive(take_own, slots[sn++ & 1], &round_taken);
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      for (uint32_t c = 0; c < take[i]; ++c) out[at + c] = 4 * (b0 + i) + static_cast<int>(c);
+      at += take[i];
+    }
     eq_seen += round_eq;
     placed += round_taken;
   }

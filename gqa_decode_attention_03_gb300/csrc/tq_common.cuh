@@ -10,9 +10,10 @@
 // 2k..2k+1; 32 sign bits per uint32; f16 norm pairs; every region head-major, each (sequence,
 // KV head) holding its cache_cap positions contiguously.
 //
-// Both kernels run one CTA of kTqWarps warps per (KV chunk, KV head, query row).  Each warp
-// keeps its own online-softmax state for every head of the group; at the end the warps' states
-// meet in shared memory (`mg`, [warp][head][D + 2]: rotated accumulator, running max in log2
+// Both kernels run one CTA of kTqWarps warps per (KV chunk, KV head x head split, query row):
+// a group of more than kTqMaxGroup query heads is served by head_split CTAs of at most
+// kTqMaxGroup heads each (each decoding the same K/V).  Each warp keeps its own online-softmax
+// state for every head of the CTA; at the end the warps' states meet in shared memory (`mg`, [warp][head][D + 2]: rotated accumulator, running max in log2
 // units, running sum) and tq_finish combines them, then either normalises, rotates back and
 // writes the row, or writes the chunk's rotated partial for the last CTA's merge.
 #pragma once
@@ -40,6 +41,20 @@ struct TqParams {
   float c0, c1, c2, c3;        // centroids
   float qjl_scale;
 };
+
+// The query heads one CTA serves: KV head g, heads head0 .. head0 + G - 1 of its group, and the
+// column of the (row, column) arrival counters its chunks share.
+struct TqCta {
+  int g, head0, G, col;
+};
+__device__ __forceinline__ TqCta tq_cta(const PartialParams& p) {
+  TqCta a;
+  a.g = blockIdx.y / p.head_split;
+  a.G = p.group / p.head_split;
+  a.head0 = a.g * p.group + (blockIdx.y % p.head_split) * a.G;
+  a.col = blockIdx.y;
+  return a;
+}
 
 __device__ __forceinline__ float half_lo(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
@@ -86,7 +101,7 @@ struct TqRotateBack {
 // Row t's length and sequence (out-of-range values flagged and clamped), the chunk's [c0, c1),
 // and the row's bookkeeping (n_valid; zeros for an empty context, as the page writes for
 // seq_len == 0).  False when this CTA has no positions.
-__device__ __forceinline__ bool tq_row_setup(const PartialParams& p, int t, int c, int g, int G,
+__device__ __forceinline__ bool tq_row_setup(const PartialParams& p, int t, int c, const TqCta& a,
                                              int D, int& L, int& s, int& c0, int& c1) {
   L = __ldg(p.kv_len + t);
   int errbits = 0;
@@ -102,14 +117,14 @@ __device__ __forceinline__ bool tq_row_setup(const PartialParams& p, int t, int 
   }
   c0 = c * p.chunk;
   c1 = min(c0 + p.chunk, L);
-  if (c == 0 && g == 0 && threadIdx.x == 0) {
+  if (c == 0 && a.col == 0 && threadIdx.x == 0) {
     if (errbits) flag_error(p.err, errbits);
     if (p.merge) p.n_valid[t] = (L + p.chunk - 1) / p.chunk;
   }
   if (c0 >= L) {
     if (c == 0)
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
+      for (int i = threadIdx.x; i < a.G * D; i += blockDim.x)
+        p.out[((size_t)t * p.n_heads + a.head0 + i / D) * D + i % D] = 0.f;
     return false;
   }
   return true;
@@ -119,8 +134,9 @@ __device__ __forceinline__ bool tq_row_setup(const PartialParams& p, int t, int 
 // the row (normalised and rotated back) or this chunk's rotated partial; with a split, the
 // last CTA of the (row, KV head) then merges the partials and rotates the merged rows.
 template <int D>
-__device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, int t, int g, int c,
-                                          int L, int G) {
+__device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, int t,
+                                          const TqCta& cta, int c, int L) {
+  const int G = cta.G;
   constexpr int DPL = D / 32;
   const PartialParams& p = tp.base;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,7 +156,7 @@ __device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, i
 #pragma unroll
       for (int k = 0; k < DPL; ++k) a[k] = fmaf(r[lane * DPL + k], e, a[k]);
     }
-    const int head = g * G + h;
+    const int head = cta.head0 + h;
     if (p.merge) {
       float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
 #pragma unroll
@@ -160,8 +176,8 @@ __device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, i
     }
   }
   if (p.merge)
-    merge_if_last<D>(p, t, g * G, G, (size_t)t * p.n_kv_heads + g, (L + p.chunk - 1) / p.chunk,
-                     kTqWarps, rot);
+    merge_if_last<D>(p, t, cta.head0, G, (size_t)t * gridDim.y + cta.col,
+                     (L + p.chunk - 1) / p.chunk, kTqWarps, rot);
 }
 
 // Launchers (tq_decode.cu: CUDA cores; tq_mma.cu: tensor cores, nb = ceil(G / 4) n-blocks).

@@ -33,16 +33,17 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
   __shared__ float qjsum[kTqMaxGroup];
   __shared__ uint32_t vbuf[kTqWarps][32][PW];
   __shared__ float mg[kTqWarps * kTqMaxGroup * (D + 2)];
-  const int c = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
-  const int G = p.group;
+  const int c = blockIdx.x, t = blockIdx.z;
+  const TqCta cta = tq_cta(p);
+  const int g = cta.g, G = cta.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int L, s, c0, c1;
-  if (!tq_row_setup(p, t, c, g, G, D, L, s, c0, c1)) return;
+  if (!tq_row_setup(p, t, c, cta, D, L, s, c0, c1)) return;
 
-  // the group's rotated and JL queries, and the per-head sum of q_jl
+  // the CTA's rotated and JL queries, and the per-head sum of q_jl
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const size_t qi = ((size_t)t * p.n_heads + g * G) * D + i;
+    const size_t qi = ((size_t)t * p.n_heads + cta.head0) * D + i;
     qr[i / D][i % D] = __ldg(tp.q_rot + qi);
     qj[i / D][i % D] = __ldg(tp.q_jl + qi);
   }
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(32 * kTqWarps) tq_decode_kernel(const TqParams
     }
   }
   __syncthreads();
-  tq_finish<D>(tp, mg, t, g, c, L, G);
+  tq_finish<D>(tp, mg, t, cta, c, L);
 }
 
 cudaError_t launch_tq_fma(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream) {
@@ -228,8 +229,8 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
     return tq_fail(GQA_EINVAL, "attn_decode_tq: head_dim must be 32, 64 or 128");
   if (n_kv_heads <= 0 || n_heads % n_kv_heads)
     return tq_fail(GQA_EINVAL, "attn_decode_tq: n_heads must be a positive multiple of n_kv_heads");
-  if (n_heads / n_kv_heads > gqa::kTqMaxGroup)
-    return tq_fail(GQA_EUNSUPPORTED, "attn_decode_tq: group size above 8");
+  if (n_heads / n_kv_heads > 16)
+    return tq_fail(GQA_EUNSUPPORTED, "attn_decode_tq: group size above 16");
   if (n_tok < 0 || n_tok > 65535) return tq_fail(GQA_EINVAL, "attn_decode_tq: n_tok outside [0, 65535]");
   if (n_tok == 0) return GQA_OK;
   if (!q_rot || !q_jl || !k_polar || !k_jl || !k_norms || !v_polar || !v_norms || !centroids ||
@@ -262,7 +263,7 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   p.n_heads = n_heads;
   p.n_kv_heads = n_kv_heads;
   p.group = n_heads / n_kv_heads;
-  p.head_split = 1;
+  p.head_split = plan.grid_y / n_kv_heads;  // CTAs per KV head, kTqMaxGroup heads each at most
   p.cache_cap = cache_cap;
   p.max_kv_len = max_len;
   p.budget = INT32_MAX;
@@ -298,10 +299,11 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   const int G = n_heads / n_kv_heads;
   // head_dim 32 runs on the CUDA cores: a 32-dim polar row is 8 bytes, below the tensor-core
   // kernel's 16-byte staging pieces
+  const int nb = G / p.head_split <= 4 ? 1 : 2;  // n-blocks of 4 heads per CTA
   if (head_dim == 32 || (kern && std::strcmp(kern, "fma") == 0))
     (void)gqa::launch_tq_fma(head_dim, grid, tp, stream);
   else
-    (void)gqa::launch_tq_mma(head_dim, G <= 4 ? 1 : 2, grid, tp, stream);
+    (void)gqa::launch_tq_mma(head_dim, nb, grid, tp, stream);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
   return GQA_OK;

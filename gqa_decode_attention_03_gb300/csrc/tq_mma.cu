@@ -31,46 +31,17 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime_api.h>
 
-#include "partial_mma.cuh"
-#include "tq_common.cuh"
+#include "tq_frag.cuh"
 
 namespace gqa {
 
 constexpr int kTqStages = 4;
 
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t lo4, uint32_t hi4, uint32_t sel) {
-  return __byte_perm(lo4, hi4, sel);
-}
-
-// Four 2-bit fields (bytes 0..3 of y, values 0..3) -> prmt selectors picking f16 numbers
-// (y.b0, y.b1) and (y.b2, y.b3) of an 8-byte table: each byte k becomes 0x22 k + 0x10 (nibbles
-// 2k, 2k + 1).  The high selector comes from a multiply-high on the FMA pipe, which leaves the
-// integer ALU pipe (the kernel's busiest) to the field extraction and the permutes.
-__device__ __forceinline__ void field_sel(uint32_t y, uint32_t& lo, uint32_t& hi) {
-  lo = y * 0x22u + 0x10101010u;
-  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(hi) : "r"(y), "r"(0x220000u), "r"(0x1010u));
-}
-
-// f16x2 of (a, b): the hi parts (part 0) or the lo parts a - hi, b - hi (part 1).
-__device__ __forceinline__ uint32_t f16_part(float a, float b, int part) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-  return h2_bits(part ? l : h);
-}
-
-// 2^(14 - e) for a = m 2^e, m in [0.5, 1): scales max |x| = a into [2^13, 2^14).
-__device__ __forceinline__ float pow2_scale(float a) {
-  if (!(a > 0.f) || !isfinite(a)) return 1.f;
-  int e;
-  frexpf(a, &e);
-  return ldexpf(1.f, 14 - e);
 }
 
 template <int D>
@@ -88,20 +59,22 @@ struct TqMmaLayout {
 // Three CTAs per SM at one n-block (up to 170 registers): 5 % faster on GB300 than four CTAs
 // at 128 registers, which spill
 template <int D, int NB>
-__global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2) tq_mma_kernel(const TqParams tp) {
+__global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
+    tq_mma_kernel(const TqParams tp) {
   using Lay = TqMmaLayout<D>;
   constexpr int PW = Lay::PW, JW = Lay::JW, KPS = Lay::KPS, S = kTqStages;
   const PartialParams& p = tp.base;
   __shared__ __align__(16) uint32_t sbuf[Lay::kBuf];  // stage ring, then the warps' states
   __shared__ __align__(16) float qr[kTqMaxGroup][D];
   __shared__ __align__(16) float qj[kTqMaxGroup][D];
-  const int c = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
-  const int G = p.group;
+  const int c = blockIdx.x, t = blockIdx.z;
+  const TqCta cta = tq_cta(p);
+  const int g = cta.g, G = cta.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int fr = lane >> 2, fq = lane & 3;
 
   int L, s, c0, c1;
-  if (!tq_row_setup(p, t, c, g, G, D, L, s, c0, c1)) return;
+  if (!tq_row_setup(p, t, c, cta, D, L, s, c0, c1)) return;
 
   // The first tiles' loads go out before the query setup, so their latency hides behind it.
   // per-thread constants of the decode: sign-bit multipliers (1 << (15 - bit)) of the QJL
@@ -168,7 +141,7 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2) tq_mma_kernel(
   }
 
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const size_t qi = ((size_t)t * p.n_heads + g * G) * D + i;
+    const size_t qi = ((size_t)t * p.n_heads + cta.head0) * D + i;
     qr[i / D][i % D] = __ldg(tp.q_rot + qi);
     qj[i / D][i % D] = __ldg(tp.q_jl + qi);
   }
@@ -372,7 +345,7 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2) tq_mma_kernel(
     }
   }
   __syncthreads();
-  tq_finish<D>(tp, mg, t, g, c, L, G);
+  tq_finish<D>(tp, mg, t, cta, c, L);
 }
 
 cudaError_t launch_tq_mma(int head_dim, int nb, dim3 grid, const TqParams& tp,

@@ -65,11 +65,11 @@ def test_random_q8(i):
 @pytest.mark.parametrize("kernel", ["mma", "fma"])
 def test_random_turboquant(i, kernel, monkeypatch):
     from gqa_decode_attention_03_gb300 import gqa_decode as gd
-    if kernel == "fma":
-        monkeypatch.setenv("GQA_TQ_KERNEL", "fma")
+    if kernel != "mma":
+        monkeypatch.setenv("GQA_TQ_KERNEL", kernel)
     r, T, n_seq, seq_of, cap, L, chunk = _draw(9000 + i)
     D = [32, 64, 128][int(r.integers(0, 3))]
-    G = [1, 2, 3, 4, 5, 8][int(r.integers(0, 6))]
+    G = [1, 2, 3, 4, 5, 8, 12, 16][int(r.integers(0, 8))]
     Hk = int(r.integers(1, 3))
     c = W.make_tq_case(9100 + i, T, G * Hk, Hk, D, L, cache_cap=cap, seq_of=seq_of, n_seq=n_seq)
     i32 = lambda a: dev(np.ascontiguousarray(a).view(np.int32))  # noqa: E731

@@ -60,9 +60,9 @@ def test_topk_feeds_the_selected_int8_path():
     assert_close(got, oracle_ref(case), TOL_Q8, "topk -> q8_sel")
 
 
-@pytest.mark.parametrize("max_kv", [49147, 200003, 212988, 212992, 260001])
+@pytest.mark.parametrize("max_kv", [49147, 184316, 184320, 200003, 260001])
 def test_topk_staged_and_unstaged_rows(max_kv):
-    """Rows whose block keys fit the shared-memory staging (max_kv_len / 4 + 1 <= 53248 blocks,
+    """Rows whose block keys fit the shared-memory staging (max_kv_len / 4 + 1 <= 46080 blocks,
     past the 48 KB that needs no opt-in) and rows past it, which read the keys from global
     memory at every step of the threshold search."""
     kv_len = np.array([max_kv, max_kv - 3, 20000, 700, 0], np.int32)

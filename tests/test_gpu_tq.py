@@ -1,7 +1,7 @@
 """GPU parity of attn_decode_tq (decode over a TurboQuant-compressed cache) against the fp64
 oracle's decode_tq on the same seeded inputs, for the tensor-core kernel and the CUDA-core one:
 one CTA per row, split rows merged by the last CTA, empty and ragged rows, rows sharing a
-sequence, group sizes 1 to 8 and both head_dims, workspace reuse, out-of-range lengths flagged.
+sequence, group sizes 1 to 16 and every head_dim, workspace reuse, out-of-range lengths flagged.
 
 Tolerance: both sides decode the same packed words, f16 norms and fp32 centroids exactly; they
 differ only by fp32 rounding of the dot products, the exp2 approximation and the order of the
@@ -23,10 +23,10 @@ TOL_TQ = 1e-4
 @pytest.fixture(params=["mma", "fma"], autouse=True)
 def tq_kernel(request, monkeypatch):
     """Every test runs on both kernels: tensor cores (the default) and CUDA cores."""
-    if request.param == "fma":
-        monkeypatch.setenv("GQA_TQ_KERNEL", "fma")
-    else:
+    if request.param == "mma":
         monkeypatch.delenv("GQA_TQ_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("GQA_TQ_KERNEL", request.param)
     return request.param
 
 
@@ -57,8 +57,11 @@ def check(got, ref, tol=TOL_TQ):
 
 
 @pytest.mark.parametrize("D", [32, 64, 128])
-@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (12, 4), (16, 4), (20, 4), (32, 4)])
+@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (12, 4), (16, 4), (20, 4), (32, 4), (36, 4),
+                                  (44, 4), (48, 4), (64, 4)])
 def test_tq_group_sizes(D, H, Hk):
+    """Group sizes 1 to 16: above 8 heads a group is served by several CTAs (9 heads: 3 x 3,
+    11: 11 x 1, 12: 2 x 6, 16: 2 x 8)."""
     c = W.make_tq_case(2100 + D + H, 2, H, Hk, D, [300, 77])
     check(run_tq(c), ref_tq(c))
 
@@ -137,8 +140,28 @@ def test_tq_head_dim_32_split_and_shared(chunk):
         check(run_tq(c), ref_tq(c))
 
 
+@pytest.mark.parametrize("chunk", [None, 128])
+def test_tq_twelve_heads_per_kv_head(chunk):
+    """The int8 page's group shape (12 query heads per KV head, qsa2.metal qsa_attn2) over a
+    TurboQuant cache: 48 heads over 4 KV heads, D = 128, split rows."""
+    c = W.make_tq_case(2207, 2, 48, 4, 128, [2500, 700], cache_cap=2500)
+    with forced_chunk(chunk):
+        check(run_tq(c), ref_tq(c))
+
+
+@pytest.mark.parametrize("chunk", [None, 256])
+def test_tq_odd_capacity_and_stage_tails(chunk):
+    """A cache capacity that is not a multiple of 4, lengths that end inside a 32-position
+    stage and inside a 16-position block, at D = 128 and 64."""
+    for D in (128, 64):
+        L = [1003, 17, 33, 999, 1]
+        c = W.make_tq_case(2208 + D, len(L), 8, 2, D, L, cache_cap=1003)
+        with forced_chunk(chunk):
+            check(run_tq(c), ref_tq(c))
+
+
 def test_tq_rejects_large_group():
     from gqa_decode_attention_03_gb300 import gqa_decode as gd
-    c = W.make_tq_case(2205, 1, 16, 1, 64, [64])
+    c = W.make_tq_case(2205, 1, 17, 1, 64, [64])
     with pytest.raises(gd.GqaError, match="GQA_EUNSUPPORTED"):
         run_tq(c)

@@ -194,6 +194,6 @@ def test_turboquant_argument_checks(gd):
                                      n_heads, n_kv_heads, head_dim, 64, 64, None, 0, None, None)
     assert call(head_dim=256) == gd.GQA_EINVAL
     assert call(n_heads=30) == gd.GQA_EINVAL
-    assert call(n_heads=80, n_kv_heads=8) == gd.GQA_EUNSUPPORTED   # group of 10
+    assert call(n_heads=136, n_kv_heads=8) == gd.GQA_EUNSUPPORTED  # group of 17
     assert call(ptr=0) == gd.GQA_EINVAL
     assert call(ptr=8) == gd.GQA_EINVAL                           # caches 16-byte aligned
