@@ -200,10 +200,10 @@ def _device_inputs(case, torch):
     return t
 
 
-def _rows_fused_merge(plan):
-    """Grouped rows on the tcgen05 kernel merge their own partials when the grid fits one CTA
-    per SM (the library's rule)."""
-    if not (plan.merge and not plan.streamk and plan.row_group > 1):
+def _rows_fused_merge(plan, kind="f16"):
+    """Grouped f16 rows on the tcgen05 kernel merge their own partials when the grid fits one
+    CTA per SM (the library's rule); TurboQuant row groups are always followed by merge_kernel."""
+    if not (plan.merge and not plan.streamk and plan.row_group > 1) or kind == "tq":
         return False
     if os.environ.get("GQA_F16_ROWS") == "mma":
         return False
@@ -212,15 +212,18 @@ def _rows_fused_merge(plan):
     return plan.grid_x * plan.grid_y * plan.grid_z <= sms
 
 
-def _merge_launch(plan):
+def _merge_launch(plan, kind="f16"):
     """1 when the step ends with a separate merge kernel (rows grouped by sequence)."""
-    if plan.merge and not plan.streamk and plan.row_group > 1 and not _rows_fused_merge(plan):
+    if (plan.merge and not plan.streamk and plan.row_group > 1
+            and not _rows_fused_merge(plan, kind)):
         return 1
     return 0
 
 
 def _kernel_name(case, plan):
     if case.kind == "tq":
+        if plan.row_group > 1:
+            return "tq_rows_kernel (rows grouped by sequence)" + (" + merge_kernel" if plan.merge else "")
         name = "tq_decode_kernel" if os.environ.get("GQA_TQ_KERNEL") == "fma" else "tq_mma_kernel"
         return name + (" (split-KV, merge fused)" if plan.merge else "")
     if plan.streamk:
@@ -470,7 +473,7 @@ def run_gpu(args):
                 "timing": "pipelined loop: copies on a second stream, two buffer sets"
                 if big else "one step at a time, copies inside its events",
                 "d2h_bytes_per_step": int(T * H * D * 4)},
-        "gpu_launches": int(K * (1 + (scores is not None) + _merge_launch(plan))),
+        "gpu_launches": int(K * (1 + (scores is not None) + _merge_launch(plan, case.kind))),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

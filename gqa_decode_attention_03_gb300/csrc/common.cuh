@@ -135,6 +135,38 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// The inverse rotation of a TurboQuant row (flash_attention_tq.metal's epilogue), on a row held
+// D/32 consecutive dims per lane: scale by 1/sqrt(D), the Walsh-Hadamard butterflies (within
+// the lane for strides below D/32, across lanes by shuffle above), then the sign flip.
+template <int D>
+__device__ __forceinline__ void rotate_back(float (&a)[D / 32], const float* signs, int lane) {
+  constexpr int DPL = D / 32;
+  const float s = rsqrtf(static_cast<float>(D));
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) a[k] *= s;
+#pragma unroll
+  for (int stride = 1; stride < DPL; stride <<= 1)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k)
+      if ((k & stride) == 0) {
+        const float x = a[k], y = a[k + stride];
+        a[k] = x + y;
+        a[k + stride] = x - y;
+      }
+#pragma unroll
+  for (int stride = DPL; stride < D; stride <<= 1) {
+    const int lmask = stride / DPL;
+    const bool high = (lane & lmask) != 0;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      const float other = __shfl_xor_sync(0xffffffffu, a[k], lmask);
+      a[k] = high ? other - a[k] : a[k] + other;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) a[k] *= __ldg(signs + lane * DPL + k);
+}
+
 __device__ __forceinline__ void flag_error(int32_t* err_word, int bits) {
   if (err_word) atomicOr(err_word, bits);
 }

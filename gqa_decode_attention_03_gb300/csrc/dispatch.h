@@ -80,7 +80,7 @@ inline cudaError_t launch_rows_f16(int head_dim, const CUtensorMap& tk, const CU
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,
                          int n_tok, int n_heads, float* out, cudaStream_t s,
                          const float* gate = nullptr, long long gate_stride = 0,
-                         bool after_partials = false);
+                         bool after_partials = false, const float* signs = nullptr);
 
 // Raises the function's dynamic shared-memory limit once per (function, device).
 cudaError_t ensure_smem(const void* fn, int bytes);

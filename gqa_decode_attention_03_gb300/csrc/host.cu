@@ -96,6 +96,8 @@ constexpr long long kMinSplitBytes = 128 << 10;
 constexpr int kTqCtasPerSm = 8;
 constexpr long long kTqMaxChunk = 2048;
 constexpr long long kTqMinSplitBytes = 32 << 10;
+// The TurboQuant row kernel: 8 warps and ~94 KB of shared memory, one CTA per SM.
+constexpr int kTqRowsCtasPerSm = 1;
 
 // Shapes that do not depend on the device.
 gqa_status check_shape(int n_tok, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
@@ -173,6 +175,17 @@ bool rows_on_umma() {
 // 128 MMA rows hold each (row, head) pair twice, once per position half), 32 / group size on the
 // mma.sync kernel.
 int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim) {
+  if (kind == GQA_KIND_TQ) {
+    // TurboQuant rows sharing a sequence: the tensor-core row kernel (tq_rows.cu) serves up to
+    // 64 (row, head) pairs per CTA from one decoded tile; head_dim 32 and the CUDA-core kernel
+    // stay one CTA per row
+    const char* k = std::getenv("GQA_TQ_KERNEL");
+    const char* r = std::getenv("GQA_TQ_ROWS");  // "off": one CTA per row (tests, comparison)
+    if (n_seq >= n_tok || head_dim == 32 || (k && std::strcmp(k, "fma") == 0) ||
+        (r && std::strcmp(r, "off") == 0))
+      return 1;
+    return 64 / (group / head_split_for(kind, group));
+  }
   if (kind != GQA_KIND_F16 || n_seq >= n_tok || use_streamk(kind, n_tok)) return 1;
   const char* k = std::getenv("GQA_F16_KERNEL");
   if (k && std::strcmp(k, "fma") == 0) return 1;
@@ -251,12 +264,18 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   const long long groups =
       rgroup > 1 ? std::max<long long>((n_tok + rgroup - 1) / rgroup, std::min(n_seq, n_tok)) : n_tok;
   plan->row_group = rgroup;
-  const bool umma_rows = rgroup > 1 && gqa::rows_on_umma();
-  if (umma_rows) tile = 64;  // the tcgen05 row kernel's tile, whatever head_dim
-  const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
   const bool tq = kind == GQA_KIND_TQ;
+  const bool umma_rows = rgroup > 1 && !tq && gqa::rows_on_umma();
+  if (umma_rows) tile = 64;  // the tcgen05 row kernel's tile, whatever head_dim
+  const bool tq_rows = rgroup > 1 && tq;
+  if (tq_rows) tile = 32;    // the TurboQuant row kernel's stage
+  const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
   const long long slots =
-      (long long)(tq ? kTqCtasPerSm : umma_rows ? kUmmaRowsCtasPerSm : kCtasPerSm) * num_sms;
+      (long long)(tq_rows ? kTqRowsCtasPerSm
+                  : tq    ? kTqCtasPerSm
+                  : umma_rows ? kUmmaRowsCtasPerSm
+                              : kCtasPerSm) *
+      num_sms;
   long long chunk = (units + slots - 1) / slots;
   chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
   // a split chunk spans at least two stages, so its pipeline has something to overlap

@@ -23,7 +23,7 @@ cudaError_t ensure_smem(const void* fn, int bytes) {
 
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,
                          int n_tok, int n_heads, float* out, cudaStream_t s, const float* gate,
-                         long long gate_stride, bool after_partials) {
+                         long long gate_stride, bool after_partials, const float* signs) {
   // one warp per (row, head), kMergeWarps per CTA
   const long long pairs = (long long)n_tok * n_heads;
   cudaLaunchConfig_t cfg{};
@@ -40,12 +40,12 @@ cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid
   cfg.numAttrs = after_partials ? 1 : 0;
   if (head_dim == 64)
     return cudaLaunchKernelEx(&cfg, merge_kernel<64>, part, n_valid, n_split, n_tok, n_heads,
-                              gate, gate_stride, out);
+                              gate, gate_stride, signs, out);
   if (head_dim == 128)
     return cudaLaunchKernelEx(&cfg, merge_kernel<128>, part, n_valid, n_split, n_tok, n_heads,
-                              gate, gate_stride, out);
+                              gate, gate_stride, signs, out);
   return cudaLaunchKernelEx(&cfg, merge_kernel<256>, part, n_valid, n_split, n_tok, n_heads, gate,
-                            gate_stride, out);
+                            gate_stride, signs, out);
 }
 
 }  // namespace gqa

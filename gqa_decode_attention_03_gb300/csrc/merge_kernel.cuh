@@ -5,7 +5,8 @@
 //   M = max_c m_c,  e_c = exp(m_c - M),  L = sum_c l_c e_c,  out[d] = sum_c acc_c[d] e_c / L
 // as in qsa2.metal's qsa_merge2 (regolith) and FORWARD_MSL's attn_combine (there in exp2 units).
 // With a gate, the merged row is multiplied by 1 / (1 + exp(-gate)) on the way out -- the
-// sigmoid output gate both pages apply after their merge.
+// sigmoid output gate both pages apply after their merge.  With `signs` (TurboQuant partials,
+// accumulated in the rotated basis) the merged row is rotated back first (rotate_back).
 // Lanes take the chunks 32 at a time: lane c reads (m_c, l_c), a warp max gives the batch's
 // maximum, and each lane then folds every chunk of the batch into its own D/32 output dims with
 // the chunk's weight broadcast by shuffle; the accumulator loads do not depend on the weights,
@@ -36,7 +37,7 @@ template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps)
     merge_kernel(const float* __restrict__ part, const int32_t* __restrict__ n_valid, int n_split,
                  int n_tok, int n_heads, const float* __restrict__ gate, long long gate_stride,
-                 float* __restrict__ out) {
+                 const float* __restrict__ signs, float* __restrict__ out) {
   constexpr int DPL = D / 32;  // output dims per lane
   // launched as a programmatic dependent of the partials' kernel: wait for that grid's
   // completion and memory (a no-op after an ordinary launch)
@@ -85,11 +86,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) a[k] *= inv;
+  if (signs) rotate_back<D>(a, signs, lane);  // warp-uniform
   float* orow = out + ((size_t)t * n_heads + h) * D + lane * DPL;
   const float* grow = gate ? gate + ((size_t)t * n_heads + h) * gate_stride + lane * DPL : nullptr;
 #pragma unroll
   for (int k = 0; k < DPL; ++k) {
-    float y = a[k] * inv;
+    float y = a[k];
     if (grow) y *= 1.f / (1.f + __expf(-__ldg(grow + k)));  // sigmoid output gate
     orow[k] = y;
   }

@@ -63,38 +63,13 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
-// Inverse rotation of a merged rotated row held D/32 consecutive dims per lane: scale by
-// 1/sqrt(D), the Walsh-Hadamard butterflies (within the lane for strides below D/32, across
-// lanes by shuffle above), then the sign flip.
+// Inverse rotation of a merged rotated row held D/32 consecutive dims per lane (common.cuh's
+// rotate_back), as the epilogue of merge_if_last.
 template <int D>
 struct TqRotateBack {
   const float* signs;
   __device__ __forceinline__ void operator()(float (&a)[D / 32], int /*head*/, int lane) const {
-    constexpr int DPL = D / 32;
-    const float s = rsqrtf(static_cast<float>(D));
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a[k] *= s;
-#pragma unroll
-    for (int stride = 1; stride < DPL; stride <<= 1)
-#pragma unroll
-      for (int k = 0; k < DPL; ++k)
-        if ((k & stride) == 0) {
-          const float x = a[k], y = a[k + stride];
-          a[k] = x + y;
-          a[k + stride] = x - y;
-        }
-#pragma unroll
-    for (int stride = DPL; stride < D; stride <<= 1) {
-      const int lmask = stride / DPL;
-      const bool high = (lane & lmask) != 0;
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) {
-        const float other = __shfl_xor_sync(0xffffffffu, a[k], lmask);
-        a[k] = high ? other - a[k] : a[k] + other;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a[k] *= __ldg(signs + lane * DPL + k);
+    rotate_back<D>(a, signs, lane);
   }
 };
 
@@ -184,5 +159,7 @@ __device__ __forceinline__ void tq_finish(const TqParams& tp, const float* mg, i
 cudaError_t launch_tq_fma(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream);
 cudaError_t launch_tq_mma(int head_dim, int nb, dim3 grid, const TqParams& tp,
                           cudaStream_t stream);
+// tq_rows.cu: rows sharing a sequence (grid.z = group slots), head_dim 64 or 128
+cudaError_t launch_tq_rows(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream);
 
 }  // namespace gqa

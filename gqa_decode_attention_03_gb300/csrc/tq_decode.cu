@@ -274,7 +274,7 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   p.gate = gate;
   p.gate_stride = gate ? gate_stride : 0;
   if (plan.merge) {
-    const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
+    const size_t cnt = ((size_t)n_tok * plan.grid_y * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);
     p.counters = static_cast<unsigned int*>(ws);
     p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt);
@@ -300,12 +300,19 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   // head_dim 32 runs on the CUDA cores: a 32-dim polar row is 8 bytes, below the tensor-core
   // kernel's 16-byte staging pieces
   const int nb = G / p.head_split <= 4 ? 1 : 2;  // n-blocks of 4 heads per CTA
-  if (head_dim == 32 || (kern && std::strcmp(kern, "fma") == 0))
+  if (plan.row_group > 1)  // rows sharing a sequence: one decoded tile for up to 64 pairs
+    (void)gqa::launch_tq_rows(head_dim, grid, tp, stream);
+  else if (head_dim == 32 || (kern && std::strcmp(kern, "fma") == 0))
     (void)gqa::launch_tq_fma(head_dim, grid, tp, stream);
   else
     (void)gqa::launch_tq_mma(head_dim, nb, grid, tp, stream);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
+  if (plan.row_group > 1 && plan.merge) {  // the row kernel's partials: merged, rotated back
+    e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
+                          gate, gate ? gate_stride : 0, /*after_partials=*/true, signs);
+    if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
+  }
   return GQA_OK;
 }
 

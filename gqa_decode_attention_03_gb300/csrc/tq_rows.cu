@@ -23,8 +23,10 @@
 //      A = the V planes (ldmatrix.trans), B = the weights in hi and lo parts.
 // Decoding stage k + 1 overlaps the contractions of stage k (two decoded buffers, one CTA
 // barrier per stage).  At the end of the chunk each warp holds its pairs' complete states: it
-// normalises, rotates back and writes them, or writes rotated partials that the last chunk CTA
-// of each row merges (merge_if_last with the inverse rotation as its epilogue).
+// normalises, rotates back and writes them, or writes rotated partials that merge_kernel,
+// launched next as a programmatic dependent, merges and rotates back -- one warp per (row,
+// head), all rows at once.  (A merge by each row's last chunk CTA left the rows' merges queued
+// behind one another in whichever CTA finished last.)
 #include <cuda_runtime_api.h>
 
 #include "rows_mma.cuh"
@@ -52,7 +54,8 @@ struct TqRowsCfg {
   static constexpr int RING_BYTES = S * SW * 4;
   static constexpr int DEC_OFF = align_up(RING_BYTES, 1024);
   static constexpr int MG_BYTES = NW * 8 * (D + 2) * 4;  // the warps' states, after the chunk
-  static constexpr int BAR_OFF = DEC_OFF + cmax(2 * DEC, MG_BYTES);
+  static constexpr int Q_BYTES = 2 * NP * D * 4;         // the group's queries, at its start
+  static constexpr int BAR_OFF = DEC_OFF + cmax(cmax(2 * DEC, MG_BYTES), Q_BYTES);
   static constexpr int SMEM = 1024 + BAR_OFF + S * 8;
   static_assert(oVp % 4 == 0 && oKj % 4 == 0 && oKn % 4 == 0 && SW % 4 == 0,
                 "packed parts on 16-byte boundaries");
@@ -137,13 +140,22 @@ __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const
     uint32_t qb[PW][NB][2], qjb[2 * JW][NB][2];
     float sp, sj;
     {
-      float amr = 0.f, amj = 0.f;  // the warp's pairs: max |q| for the power-of-two scales
-      for (int i = lane; i < 8 * D; i += 32) {
-        const int q = 8 * warp + i / D;
-        if (q >= np) break;
-        const size_t qi = ((size_t)(t0 + q / Gc) * p.n_heads + cta.head0 + q % Gc) * D + i % D;
-        amr = fmaxf(amr, fabsf(__ldg(tp.q_rot + qi)));
-        amj = fmaxf(amj, fabsf(__ldg(tp.q_jl + qi)));
+      // the group's queries, staged by coalesced loads into the (not yet used) decoded buffers:
+      // q_rot [pair][D] then q_jl [pair][D]
+      float* qs = reinterpret_cast<float*>(dec);
+      float* qjs = qs + C::NP * D;
+      for (int i = tid; i < np * (D / 4); i += 32 * C::NW) {
+        const int q = i / (D / 4), d4 = i % (D / 4);
+        const size_t qi = ((size_t)(t0 + q / Gc) * p.n_heads + cta.head0 + q % Gc) * D + 4 * d4;
+        reinterpret_cast<float4*>(qs)[i] = __ldg(reinterpret_cast<const float4*>(tp.q_rot + qi));
+        reinterpret_cast<float4*>(qjs)[i] = __ldg(reinterpret_cast<const float4*>(tp.q_jl + qi));
+      }
+      __syncthreads();
+      const int nq = min(8, max(np - 8 * warp, 0));  // the warp's real pairs
+      float amr = 0.f, amj = 0.f;  // their max |q|, for the power-of-two scales
+      for (int i = lane; i < nq * D; i += 32) {
+        amr = fmaxf(amr, fabsf(qs[8 * warp * D + i]));
+        amj = fmaxf(amj, fabsf(qjs[8 * warp * D + i]));
       }
       const float sr = pow2_scale(warp_max(amr)), sjq = pow2_scale(warp_max(amj));
       sp = p.scale_log2 / (sr * sc);
@@ -152,26 +164,26 @@ __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const
       for (int nb = 0; nb < NB; ++nb) {
         const int q = 8 * warp + 4 * nb + (fr >> 1);
         const bool hv = q < np;
-        const size_t q0 = ((size_t)(t0 + (hv ? q / Gc : 0)) * p.n_heads + cta.head0 + (hv ? q % Gc : 0)) * D;
-        const float* qrot = tp.q_rot + q0;
-        const float* qjl = tp.q_jl + q0;
+        const float* qrot = qs + (hv ? q : 0) * D;
+        const float* qjl = qjs + (hv ? q : 0) * D;
 #pragma unroll
         for (int kb = 0; kb < PW; ++kb) {
           const int d = 16 * kb;
-          qb[kb][nb][0] = hv ? f16_part(__ldg(qrot + d + polar_dim(2 * fq)) * sr,
-                                        __ldg(qrot + d + polar_dim(2 * fq + 1)) * sr, part) : 0u;
-          qb[kb][nb][1] = hv ? f16_part(__ldg(qrot + d + polar_dim(2 * fq + 8)) * sr,
-                                        __ldg(qrot + d + polar_dim(2 * fq + 9)) * sr, part) : 0u;
+          qb[kb][nb][0] = hv ? f16_part(qrot[d + polar_dim(2 * fq)] * sr,
+                                        qrot[d + polar_dim(2 * fq + 1)] * sr, part) : 0u;
+          qb[kb][nb][1] = hv ? f16_part(qrot[d + polar_dim(2 * fq + 8)] * sr,
+                                        qrot[d + polar_dim(2 * fq + 9)] * sr, part) : 0u;
         }
 #pragma unroll
         for (int ks = 0; ks < 2 * JW; ++ks) {
           const int d = 32 * (ks / 2), s0 = 16 * (ks % 2);
-          qjb[ks][nb][0] = hv ? f16_part(__ldg(qjl + d + sign_dim(s0 + 2 * fq)) * sjq,
-                                         __ldg(qjl + d + sign_dim(s0 + 2 * fq + 1)) * sjq, part) : 0u;
-          qjb[ks][nb][1] = hv ? f16_part(__ldg(qjl + d + sign_dim(s0 + 2 * fq + 8)) * sjq,
-                                         __ldg(qjl + d + sign_dim(s0 + 2 * fq + 9)) * sjq, part) : 0u;
+          qjb[ks][nb][0] = hv ? f16_part(qjl[d + sign_dim(s0 + 2 * fq)] * sjq,
+                                         qjl[d + sign_dim(s0 + 2 * fq + 1)] * sjq, part) : 0u;
+          qjb[ks][nb][1] = hv ? f16_part(qjl[d + sign_dim(s0 + 2 * fq + 8)] * sjq,
+                                         qjl[d + sign_dim(s0 + 2 * fq + 9)] * sjq, part) : 0u;
         }
       }
+      __syncthreads();  // the staging area is read before the first stage decodes into it
     }
     const bool active = 8 * warp < np;  // the warp has real pairs (warp-uniform)
 
@@ -442,20 +454,11 @@ __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const
         }
       }
     }
-    if (p.merge) {  // each row's last chunk CTA merges its partials and rotates the result
-      const TqRotateBack<D> rot{tp.signs};
-      for (int jr = 0; jr < gr.nr; ++jr) {
-        const int t = t0 + jr;
-        int dummy = 0;
-        const int L = rows_len(p, t, seq_ok, &dummy);
-        if (c0 >= L) continue;  // the same for every thread
-        merge_if_last<D>(p, t, cta.head0, Gc, (size_t)t * gridDim.y + cta.col,
-                         (L + p.chunk - 1) / p.chunk, C::NW, rot);
-      }
-    }
     __syncthreads();  // the state area is read before the next group decodes into it
   }
   if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
+  // this CTA's partials are written: the merge kernel launched after this one may be scheduled
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 template <int D>

@@ -93,6 +93,44 @@ def test_tq_named_prefill_chunk():
     check(run_tq(c), ref_tq(c))
 
 
+ROWS_CASES = [(D, G) for D in (64, 128) for G in (1, 2, 4, 8, 12, 16)]
+
+
+@pytest.mark.parametrize("chunk", [None, 64, 256])
+@pytest.mark.parametrize("D,G", ROWS_CASES)
+def test_tq_rows_grouped_by_sequence(D, G, chunk, tq_kernel):
+    """Rows sharing a sequence on the TurboQuant row kernel (the tensor-core path): runs longer
+    than a group (64 / G rows), causal and ragged lengths, an empty row, a one-position row,
+    sequences interleaved; against the oracle.  (The CUDA-core kernel serves each row alone.)"""
+    from gqa_decode_attention_03_gb300 import gqa_decode as gd
+    seq_of = [0] * 21 + [1, 1, 2] + [0] * 3 + [2]
+    L = [300 + 7 * r for r in range(21)] + [1, 299, 0, 200, 5, 301, 150]
+    c = W.make_tq_case(2300 + D + G, len(seq_of), 2 * G, 2, D, L, cache_cap=460,
+                       seq_of=seq_of, n_seq=3)
+    with forced_chunk(chunk):
+        pl = gd.plan(len(seq_of), 2 * G, 2, D, 460, -1, gd.KIND_TQ, n_seq=3)
+        if tq_kernel == "mma":
+            hs = 1 if G <= 8 else 2
+            assert pl.row_group == 64 // (G // hs) and pl.grid_y == 2 * hs
+        else:
+            assert pl.row_group == 1
+        got = run_tq(c)
+    check(got, ref_tq(c))
+    assert torch.count_nonzero(got[23]) == 0
+
+
+def test_tq_rows_match_one_cta_per_row(monkeypatch):
+    """The prefill chunk grouped and one CTA per row (GQA_TQ_ROWS=off): both against the
+    oracle."""
+    c = W.tq_prefill_chunk()
+    ref = ref_tq(c)
+    grouped = run_tq(c).clone()
+    monkeypatch.setenv("GQA_TQ_ROWS", "off")
+    per_row = run_tq(c)
+    check(grouped, ref)
+    check(per_row, ref)
+
+
 def test_tq_long_context_sampled_rows():
     # the full-size workload in the launch configuration the benchmark times; the oracle
     # recomputes three rows (the shortest, the longest, one between)
@@ -137,6 +175,16 @@ def test_tq_head_dim_32_split_and_shared(chunk):
     L = [901, 0, 130, 899]
     c = W.make_tq_case(2206, 4, 8, 2, 32, L, cache_cap=902, seq_of=[0, 1, 1, 0], n_seq=2)
     with forced_chunk(chunk):
+        check(run_tq(c), ref_tq(c))
+
+
+@pytest.mark.parametrize("G", [12, 16])
+def test_tq_head_split_many_rows(G):
+    """Groups served by two CTAs of heads, with enough split rows that the arrival counters
+    ([rows][KV heads x head split]) outgrow their first 256 bytes."""
+    L = [700 - 23 * r for r in range(24)]
+    c = W.make_tq_case(2209 + G, 24, 2 * G, 2, 64, L, cache_cap=700)
+    with forced_chunk(128):
         check(run_tq(c), ref_tq(c))
 
 

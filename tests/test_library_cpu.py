@@ -185,6 +185,23 @@ def test_plan_turboquant(gd):
     assert q.n_split == 2 and q.chunk == 256
 
 
+def test_plan_groups_turboquant_rows(gd, monkeypatch):
+    # 16 causal rows over one TurboQuant sequence, G=4: one group of 16 rows (64 pairs), chunks
+    # of 32-position stages for 8 KV heads on one CTA per SM: 8 * 8192 / 152 -> 432 -> 448
+    monkeypatch.delenv("GQA_TQ_KERNEL", raising=False)
+    monkeypatch.delenv("GQA_TQ_ROWS", raising=False)
+    p = gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_TQ, num_sms=152, n_seq=1)
+    assert p.row_group == 16 and p.tile == 32 and p.chunk == 448 and p.n_split == 19
+    assert (p.grid_x, p.grid_y, p.grid_z) == (19, 8, 1)
+    # 12 heads per KV head: two CTAs of 6 heads, 10 rows a group
+    q = gd.plan(16, 48, 4, 128, 8192, -1, gd.KIND_TQ, num_sms=152, n_seq=1)
+    assert q.row_group == 10 and q.grid_y == 8
+    # head_dim 32, the CUDA-core kernel, or grouping switched off: one CTA per row
+    assert gd.plan(16, 32, 8, 32, 8192, -1, gd.KIND_TQ, num_sms=152, n_seq=1).row_group == 1
+    monkeypatch.setenv("GQA_TQ_ROWS", "off")
+    assert gd.plan(16, 32, 8, 128, 8192, -1, gd.KIND_TQ, num_sms=152, n_seq=1).row_group == 1
+
+
 def test_turboquant_argument_checks(gd):
     # rejected on the host before any device call
     cents = (ctypes.c_float * 4)(0.0, 0.0, 0.0, 0.0)
