@@ -399,8 +399,13 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.merge = plan.merge;
   p.gate = gate;
   p.gate_stride = gate ? gate_stride : 0;
-  p.even_split = env_int("GQA_EVEN_SPLIT") > 0 ? 1 : 0;
-  p.longest_first = env_int("GQA_LONGEST_FIRST") > 0 && n_tok <= 64 ? 1 : 0;
+  // the per-row f16 tensor-core kernel goes out as a programmatic dependent of whatever precedes
+  // it on the stream: its launch and rasterisation overlap that kernel's tail (GB300, back-to-back
+  // steps: long context 143.2 -> 141.8 us, batched 296.8 -> 295.0); GQA_PDL=0 launches it plainly
+  {
+    const char* pd = std::getenv("GQA_PDL");
+    p.pdl = !(pd && std::strcmp(pd, "0") == 0);
+  }
   if (plan.streamk) {  // ws = [arrival counters][piece records]
     const size_t cnt = ((size_t)n_tok * n_kv_heads * sizeof(uint32_t) + 255) / 256 * 256;
     p.counters = static_cast<unsigned int*>(ws);

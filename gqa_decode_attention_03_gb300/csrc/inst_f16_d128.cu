@@ -28,8 +28,17 @@ static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, cons
   const void* fn = reinterpret_cast<const void*>(&partial_mma_kernel<D, NHG>);
   cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  partial_mma_kernel<D, NHG><<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::MAX_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, partial_mma_kernel<D, NHG>, tk, tv, p);
 }
 
 template <int NHG>

@@ -61,9 +61,7 @@ struct PartialParams {
                            // before it gives up (kSpinLimit unless a test asks for fewer)
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at
   long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
-  int even_split;          // f16 tensor-core kernel: a row's ceil(L / chunk) chunks are made
-                           // equal (rounded up to whole stages) instead of chunk, ..., remainder
-  int longest_first;       // f16 tensor-core kernel: grid.z walks the rows longest first
+  int pdl;                 // f16 tensor-core kernel launched as a programmatic dependent
 };
 
 // The sigmoid output gate that both pages apply to the merged row (qsa2.metal, qsa_merge2;

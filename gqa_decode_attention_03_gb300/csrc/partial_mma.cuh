@@ -89,30 +89,6 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
   lo = h2_bits(__floats2half2_rn(a - hf.x, b - hf.y));
 }
 
-// The row of rank r when the rows are ordered by visited length, longest first (ties: lower
-// row first).  Every CTA computes it from kv_len (clamped as the kernel clamps it); O(n_tok^2)
-// over a warp's lanes, so the host asks for it only for small row counts.
-__device__ __forceinline__ int row_by_length(const PartialParams& p, int r) {
-  const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
-  auto len = [&](int u) { return min(max(__ldg(p.kv_len + u), 0), lmax); };
-  const int lane = threadIdx.x & 31;
-  for (int u0 = 0; u0 < p.n_tok; u0 += 32) {
-    const int u = u0 + lane;
-    int rank = -1;
-    if (u < p.n_tok) {
-      const int lu = len(u);
-      rank = 0;
-      for (int v = 0; v < p.n_tok; ++v) {
-        const int lv = len(v);
-        rank += lv > lu || (lv == lu && v < u);
-      }
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, rank == r);
-    if (hit) return u0 + __ffs(hit) - 1;
-  }
-  return r;
-}
-
 template <int D, int NHG>
 __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::MIN_BLOCKS)
     partial_mma_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -120,7 +96,14 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
   using C = MmaCfg<D, NHG>;
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y;
-  const int t = p.longest_first ? row_by_length(p, blockIdx.z) : blockIdx.z;
+  const int t = blockIdx.z;
+  if (p.pdl) {
+    // launched as a programmatic dependent of the previous kernel on the stream: wait for its
+    // completion and memory before touching global memory, and let the next such launch be
+    // scheduled as soon as this grid's CTAs start retiring
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
   const int G = p.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -138,15 +121,9 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
     L = 0;
   }
   // the row's chunks: ceil(L / chunk) of them, of p.chunk positions each (the last one shorter)
-  // or, with even_split, of equal length rounded up to whole stages
-  int per = p.chunk;
-  int nchunks = (L + per - 1) / per;
-  if (p.even_split && nchunks > 1) {
-    per = ((L + nchunks - 1) / nchunks + C::TP - 1) / C::TP * C::TP;
-    nchunks = (L + per - 1) / per;
-  }
-  const int c0 = c * per;
-  const int c1 = min(c0 + per, L);
+  const int nchunks = (L + p.chunk - 1) / p.chunk;
+  const int c0 = c * p.chunk;
+  const int c1 = min(c0 + p.chunk, L);
   if (c == 0 && g == 0 && threadIdx.x == 0) {
     if (errbits) flag_error(p.err, errbits);
     if (p.merge) p.n_valid[t] = nchunks;
