@@ -8,9 +8,10 @@
 // sequence).  The group's 64 pairs are the M = 64 rows of the MMAs.
 //
 // Per 64-position tile, flash-attention style:
-//   S  = Q . K^T    M = 64 pairs, N = 64 positions, K = D: Q (f16, scale * log2 e folded in) and
-//                   the K tile K-major in shared memory; S in TMEM (row i in lane
-//                   32 (i / 16) + i % 16).
+//   S  = Q . K^T    M = 64 pairs, N = 64 positions, K = D: Q (scale * log2 e folded in) as an f16
+//                   hi part and an f16 lo remainder (about 22 bits of the fp32 q, two MMAs per
+//                   k-step accumulating into the same S) and the K tile K-major in shared memory;
+//                   S in TMEM (row i in lane 32 (i / 16) + i % 16).
 //   softmax         two threads per pair: thread (warp w, lane l) owns pair 16 w + l % 16 and
 //                   the tile's positions [32 h, 32 h + 32), h = l / 16 (one tcgen05.ld 16x32bx2).
 //                   It masks positions at or past its row's length; the two halves' maxima meet
@@ -68,7 +69,8 @@ struct UmmaRowsCfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K boxes, then V boxes
   static constexpr int NST = 4;
   static constexpr int Q_BOX = M * 128;            // Q: [box][64 pairs][128 bytes]
-  static constexpr int Q_BYTES = NBOX * Q_BOX;
+  static constexpr int Q_PLANE = NBOX * Q_BOX;     // one f16 part of Q
+  static constexpr int Q_BYTES = 2 * Q_PLANE;      // its hi part, then its lo part
   static constexpr int P_BYTES = M * TP * 2;       // P: [64 pairs][64 positions] f16
   static constexpr int NPB = 3;                    // S buffers (TMEM) and P buffers (smem)
   static constexpr int S_COL = 0, O_COL = NPB * TP;
@@ -356,9 +358,12 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
             for (int kk = 0; kk < C::KS_S; ++kk) {
               const uint32_t ko = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
               const uint32_t qo = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+              // q = hi + lo (f16 parts, about 22 bits), both against the f16 K tile
+              const uint64_t kdesc = umma_desc_sw128(sk + ko, 16, 1024);
               umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
-                       umma_desc_sw128(q_addr + qo, 16, 1024),
-                       umma_desc_sw128(sk + ko, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                       umma_desc_sw128(q_addr + qo, 16, 1024), kdesc, kIdS, kk > 0 ? 1u : 0u);
+              umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
+                       umma_desc_sw128(q_addr + C::Q_PLANE + qo, 16, 1024), kdesc, kIdS, 1u);
             }
             umma_commit(&s_full[i % C::NPB]);
           } else {
@@ -458,11 +463,13 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         for (int u = 0; u < NQ; ++u) {
           const int f = threadIdx.x + u * 32 * C::NSW, qr = f / (D / 4), c4 = f % (D / 4);
           const int ch = c4 >> 1;  // 16-byte chunk of the f16 row
-          uint2 hv;
-          hv.x = h2_bits(__floats2half2_rn(v[u].x * sc, v[u].y * sc));
-          hv.y = h2_bits(__floats2half2_rn(v[u].z * sc, v[u].w * sc));
-          *reinterpret_cast<uint2*>(sQ + (ch >> 3) * C::Q_BOX + qr * 128 +
-                                    (((ch & 7) ^ (qr & 7)) << 4) + (c4 & 1) * 8) = hv;
+          uint2 hv, lv;  // the f16 hi part and the f16 lo remainder of q * scale * log2(e)
+          split_hi_lo(v[u].x * sc, v[u].y * sc, hv.x, lv.x);
+          split_hi_lo(v[u].z * sc, v[u].w * sc, hv.y, lv.y);
+          uint8_t* dst = sQ + (ch >> 3) * C::Q_BOX + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4) +
+                         (c4 & 1) * 8;
+          *reinterpret_cast<uint2*>(dst) = hv;
+          *reinterpret_cast<uint2*>(dst + C::Q_PLANE) = lv;
         }
       }
       fence_async_smem();
