@@ -238,15 +238,14 @@ def _kernel_name(case, plan):
         if _rows_fused_merge(plan):
             return rows + " (rows grouped by sequence, merge fused)"
         return rows + " (rows grouped by sequence) + merge_kernel"
-    if "block_scores" in case.meta:
-        return "topk_kernel + partial_kernel (split-KV, merge fused)"
-    if plan.streamk:
-        return "streamk_mma_kernel (stream-K split, merge fused)"
     if case.kind == "f16" and os.environ.get("GQA_F16_KERNEL") != "fma":
         name = "partial_mma_kernel"
+    elif case.kind == "q8" and os.environ.get("GQA_Q8_KERNEL") != "fma":
+        name = "partial_mma_q8_kernel"
     else:
         name = "partial_kernel"
-    return name + (" (split-KV, merge fused)" if plan.merge else "")
+    name += " (split-KV, merge fused)" if plan.merge else ""
+    return ("select_cells_kernel + " + name) if "block_scores" in case.meta else name
 
 
 def _e2e_pipelined(torch, step, stream, x, out, q_h, qj_h, kv_h, out_h, steps):
@@ -419,7 +418,10 @@ def run_gpu(args):
     gbs = world * alg / (ms * 1e-3) / 1e9
     h2d = int(q_host.nbytes + case.kv_len.nbytes + (case.q_jl.nbytes if qj_h is not None else 0))
     data = ("synthetic: seeded N(0,1) q and f16 K/V, NaN past each sequence's length"
-            if case.kind != "tq" else
+            if case.kind == "f16" else
+            "synthetic: seeded N(0,1) q, uniform int8 K/V codes in [-127, 127] with uniform f16 "
+            "scales in [0.005, 0.02]; NaN scales past each length; sorted random cell ids"
+            if case.kind == "q8" else
             "synthetic: seeded N(0,1) rotated / JL queries, uniform random 2-bit indices and sign "
             "bits, f16 norms, Lloyd-Max 2-bit centroids; NaN norms past each length")
     # The roof of the step's dominant kernel.  Per-row decode reads each K/V byte once at a few

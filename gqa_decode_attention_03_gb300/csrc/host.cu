@@ -132,10 +132,18 @@ Variant pick_variant(int heads_per_cta) {
   return Variant{4, 2, 0};
 }
 
-// The CUDA-core kernel (int8 caches, or f16 with GQA_F16_KERNEL=fma) splits a KV head's query
-// heads over head_split CTAs of at most four heads each -- the smallest divisor of the group
-// size that gets there -- so a wide group (12 heads) spreads over three times as many CTAs.
-// The tensor-core kernels serve the whole group in one CTA.
+// The CUDA-core kernel (GQA_Q8_KERNEL=fma for int8 caches, GQA_F16_KERNEL=fma for f16) splits
+// a KV head's query heads over head_split CTAs of at most four heads each -- the smallest
+// divisor of the group size that gets there -- so a wide group (12 heads) spreads over three
+// times as many CTAs.  The int8 tensor-core kernel takes up to eight heads a CTA (more CTAs on
+// a grid smaller than the GPU: attn_decode_plan); the f16 tensor-core kernels the whole group.
+// int8 caches run on the tensor-core kernel (partial_mma_q8.cuh) unless GQA_Q8_KERNEL=fma asks
+// for the CUDA-core one (comparison and parity cross-check).
+bool q8_on_mma() {
+  const char* k = std::getenv("GQA_Q8_KERNEL");
+  return !(k && std::strcmp(k, "fma") == 0);
+}
+
 int head_split_for(int kind, int group) {
   if (kind == GQA_KIND_TQ) {  // the TurboQuant kernels serve up to 8 heads of a group per CTA
     for (int hs = 1; hs <= group; ++hs)
@@ -143,12 +151,16 @@ int head_split_for(int kind, int group) {
     return group;
   }
   const char* k = std::getenv("GQA_F16_KERNEL");
-  const bool fma = kind == GQA_KIND_Q8 || (k && std::strcmp(k, "fma") == 0);
-  if (!fma) return 1;
+  const bool fma = kind == GQA_KIND_Q8 ? !q8_on_mma() : (k && std::strcmp(k, "fma") == 0);
+  if (!fma && kind != GQA_KIND_Q8) return 1;
   const int forced = env_int("GQA_HEAD_SPLIT");  // tuning sweeps: a divisor of the group size
   if (forced > 0 && group % forced == 0) return forced;
+  // the int8 tensor-core kernel serves up to 8 heads a CTA by default (one warp per row slice
+  // and output half: 16 heads a CTA measured 21.1 us against 16.4 on GB300, 1024 selected
+  // cells), up to 16 when a head split of 1 is forced; the CUDA-core kernels up to 4
+  const int per_cta = fma ? 4 : 8;
   for (int hs = 1; hs <= group; ++hs)
-    if (group % hs == 0 && group / hs <= 4) return hs;
+    if (group % hs == 0 && group / hs <= per_cta) return hs;
   return group;
 }
 
@@ -257,8 +269,9 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
                                (head_dim + 2) * sizeof(float);
     return GQA_OK;
   }
-  const int hsplit = gqa::head_split_for(kind, n_heads / n_kv_heads);
-  const int rgroup = gqa::row_group_for(kind, n_tok, n_seq, n_heads / n_kv_heads, head_dim);
+  const int group = n_heads / n_kv_heads;
+  int hsplit = gqa::head_split_for(kind, group);
+  const int rgroup = gqa::row_group_for(kind, n_tok, n_seq, group, head_dim);
   // CTAs that do work: one per row, or per group of rows sharing a sequence (at least one group
   // per sequence, and at least n_tok / rgroup groups)
   const long long groups =
@@ -269,39 +282,59 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
   if (umma_rows) tile = 64;  // the tcgen05 row kernel's tile, whatever head_dim
   const bool tq_rows = rgroup > 1 && tq;
   if (tq_rows) tile = 32;    // the TurboQuant row kernel's stage
-  const long long units = groups * n_kv_heads * hsplit * std::max(nmax, 1LL);
-  const long long slots =
-      (long long)(tq_rows ? kTqRowsCtasPerSm
-                  : tq    ? kTqCtasPerSm
-                  : umma_rows ? kUmmaRowsCtasPerSm
-                              : kCtasPerSm) *
-      num_sms;
-  long long chunk = (units + slots - 1) / slots;
-  chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
-  // a split chunk spans at least two stages, so its pipeline has something to overlap
-  // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
-  // D=64 4096 positions 14.7 against 16.1)
-  chunk = std::max(chunk, 2LL * tile);
-  const long long row_bytes =
-      kind == GQA_KIND_F16   ? 4LL * head_dim
-      : kind == GQA_KIND_Q8 ? 2LL * (head_dim + head_dim / 32)
-                             : 4LL * (head_dim / 16 + head_dim / 32 + 1) + 4LL * (head_dim / 16 + 1);
-  if (nmax * row_bytes <= (tq ? kTqMinSplitBytes : kMinSplitBytes)) chunk = std::max(nmax, 1LL);
   const int forced = env_int("GQA_FORCE_CHUNK");
-  if (forced > 0) {
-    chunk = forced;
-  } else if (umma_rows) {
-    // at most one CTA per SM in all, so that the chunk CTAs can merge their own partials (a
-    // cooperative launch); when even one chunk per group and KV head is too many, the merge
-    // kernel follows instead
-    const long long per_split = (long long)n_kv_heads * hsplit *
-                                std::min<long long>(groups, n_tok);
-    const long long cap = num_sms / std::max(per_split, 1LL);
-    if (cap >= 1) chunk = std::max(chunk, (std::max(nmax, 1LL) + cap - 1) / cap);
+  // the chunk length for a head split hs
+  auto chunk_for = [&](int hs) {
+    const long long units = groups * n_kv_heads * hs * std::max(nmax, 1LL);
+    const long long slots =
+        (long long)(tq_rows ? kTqRowsCtasPerSm
+                    : tq    ? kTqCtasPerSm
+                    : umma_rows ? kUmmaRowsCtasPerSm
+                                : kCtasPerSm) *
+        num_sms;
+    long long chunk = (units + slots - 1) / slots;
+    chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
+    // a split chunk spans at least two stages, so its pipeline has something to overlap
+    // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
+    // D=64 4096 positions 14.7 against 16.1)
+    chunk = std::max(chunk, 2LL * tile);
+    const long long row_bytes =
+        kind == GQA_KIND_F16   ? 4LL * head_dim
+        : kind == GQA_KIND_Q8 ? 2LL * (head_dim + head_dim / 32)
+                               : 4LL * (head_dim / 16 + head_dim / 32 + 1) + 4LL * (head_dim / 16 + 1);
+    if (nmax * row_bytes <= (tq ? kTqMinSplitBytes : kMinSplitBytes)) chunk = std::max(nmax, 1LL);
+    if (forced > 0) {
+      chunk = forced;
+    } else if (umma_rows) {
+      // at most one CTA per SM in all, so that the chunk CTAs can merge their own partials (a
+      // cooperative launch); when even one chunk per group and KV head is too many, the merge
+      // kernel follows instead
+      const long long per_split = (long long)n_kv_heads * hs * std::min<long long>(groups, n_tok);
+      const long long cap = num_sms / std::max(per_split, 1LL);
+      if (cap >= 1) chunk = std::max(chunk, (std::max(nmax, 1LL) + cap - 1) / cap);
+    }
+    chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;
+    const long long whole = (std::max(nmax, 1LL) + tile - 1) / tile * tile;
+    return std::min(chunk, whole);
+  };
+  long long chunk = chunk_for(hsplit);
+  if (kind == GQA_KIND_Q8 && gqa::q8_on_mma() && env_int("GQA_HEAD_SPLIT") <= 0) {
+    // a grid smaller than the GPU is latency-bound: the int8 tensor-core kernel then serves
+    // fewer heads per CTA (down to 4), as long as the grid still fits on the SMs -- a CTA's
+    // tile time does not shrink with fewer heads, but 1.5-3x more CTAs share the positions'
+    // merge and the per-CTA merge has fewer heads (GB300, 1024 selected cells, 12 heads per KV
+    // head: 21.1 us at 12 heads a CTA, 16.4 at 6, 15.8 at 4)
+    for (int hs = group; hs > hsplit; --hs) {
+      if (group % hs != 0 || group / hs < 4) continue;
+      const long long c = chunk_for(hs);
+      const long long ns = std::max(1LL, (nmax + c - 1) / c);
+      if (ns * n_kv_heads * hs * (long long)n_tok <= num_sms) {
+        hsplit = hs;
+        chunk = c;
+        break;
+      }
+    }
   }
-  chunk = (std::max(chunk, 1LL) + tile - 1) / tile * tile;
-  const long long whole = (std::max(nmax, 1LL) + tile - 1) / tile * tile;
-  if (chunk > whole) chunk = whole;
   const long long n_split = std::max(1LL, (nmax + chunk - 1) / chunk);
   if (n_split > (1LL << 30)) return fail(GQA_EUNSUPPORTED, "too many chunks");
   plan->chunk = (int)chunk;
@@ -447,16 +480,19 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     // selected-cell workload: 17.0 us per step against 18.9 with four)
     st = GQA_OK;
     const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
-    if (kind == GQA_KIND_Q8 && var.gw == 4 && var.nps == 4 && !plan.streamk &&
+    if (kind == GQA_KIND_Q8 && !var.mma && var.gw == 4 && var.nps == 4 && !plan.streamk &&
         ctas < current_sm_count(&st))
       var.nps = 8;
   }
   const int nhg = (p.group / p.head_split + var.gw - 1) / var.gw;
   const int threads = 32 * (nhg * var.nps + 1);
-  // f16 caches run on the tensor cores unless GQA_F16_KERNEL=fma asks for the CUDA-core kernel
+  // f16 caches run on the tensor cores unless GQA_F16_KERNEL=fma asks for the CUDA-core kernel,
+  // int8 caches unless GQA_Q8_KERNEL=fma does
   if (kind == GQA_KIND_F16) {
     const char* k = std::getenv("GQA_F16_KERNEL");
     var.mma = !(k && std::strcmp(k, "fma") == 0);
+  } else if (kind == GQA_KIND_Q8) {
+    var.mma = gqa::q8_on_mma() ? 1 : 0;
   }
   const dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
   // grouped rows on the tcgen05 kernel merge their own partials when the whole grid fits one

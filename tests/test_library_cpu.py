@@ -80,10 +80,31 @@ def test_plan_long_context_chunked(gd):
 
 def test_plan_selected_width_caps_chunks(gd):
     # int8 + 1024 ids over a context of 8192: the visited list is 1024 long (chunked mode);
-    # the 12 query heads of a KV head spread over 3 CTAs of 4 heads each
+    # the grid (8 chunks x 4 KV heads) is far below 152 SMs, so the tensor-core kernel's 12
+    # query heads of a KV head spread over 3 CTAs of 4 heads each (96 CTAs)
     p = gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
     assert p.streamk == 0 and p.tile == 64 and p.n_split == -(-1024 // p.chunk)
     assert p.grid_y == 4 * 3 and p.chunk == 128
+
+
+def test_plan_q8_head_split(gd, monkeypatch):
+    # a grid that fills the GPU keeps the default of up to 8 heads a CTA (12 -> 2 x 6)
+    p = gd.plan(64, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
+    assert p.grid_y == 4 * 2 and p.grid_z == 64
+    # a small grid splits further while it still fits on the SMs, never below 4 heads a CTA:
+    # 16 heads -> 4 CTAs of 4 (8 chunks x 4 KV heads x 4 = 128 CTAs)
+    q = gd.plan(1, 64, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152)
+    assert q.grid_y == 4 * 4 and q.n_split == 8
+    # ... but not past the SM count: on 64 SMs, 8 x 4 x 2 = 64 CTAs
+    assert gd.plan(1, 64, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=64).grid_y == 4 * 2
+    # 4 heads a KV head: nothing to split
+    assert gd.plan(1, 16, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152).grid_y == 4
+    # a forced split wins; the CUDA-core kernel keeps its 4 heads a CTA
+    monkeypatch.setenv("GQA_HEAD_SPLIT", "1")
+    assert gd.plan(1, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152).grid_y == 4
+    monkeypatch.delenv("GQA_HEAD_SPLIT")
+    monkeypatch.setenv("GQA_Q8_KERNEL", "fma")
+    assert gd.plan(64, 48, 4, 256, 8192, 1024, gd.KIND_Q8, num_sms=152).grid_y == 4 * 3
 
 
 def test_plan_groups_rows_sharing_a_sequence(gd, monkeypatch):
