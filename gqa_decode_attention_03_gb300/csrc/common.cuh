@@ -135,6 +135,32 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// ---------------------------------------------------------------- thread-block clusters
+
+// Every thread of every CTA of the cluster: arrive (release), then wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
+// The address of this CTA's shared word `a` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // The inverse rotation of a TurboQuant row (flash_attention_tq.metal's epilogue), on a row held
 // D/32 consecutive dims per lane: scale by 1/sqrt(D), the Walsh-Hadamard butterflies (within
 // the lane for strides below D/32, across lanes by shuffle above), then the sign flip.

@@ -25,6 +25,7 @@ bool use_streamk(int kind, int n_tok);  // f16 on the tensor cores with few enou
 int row_group_for(int kind, int n_tok, int n_seq, int group, int head_dim);
 bool rows_on_umma();  // grouped rows on the tcgen05 kernel (default) or the mma.sync one
 bool q8_on_mma();     // int8 caches on the tensor-core kernel (default) or the CUDA-core one
+bool q8_cluster_merge();  // int8 tensor-core kernel: split rows merge inside a cluster
 
 // Defined in the inst_*.cu files, one per (cache kind, head_dim).
 cudaError_t launch_partial_f16_d64(Variant v, const CUtensorMap&, const CUtensorMap&,

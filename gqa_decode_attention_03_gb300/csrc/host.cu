@@ -144,6 +144,14 @@ bool q8_on_mma() {
   return !(k && std::strcmp(k, "fma") == 0);
 }
 
+// A split row of at most 8 chunks on the int8 tensor-core kernel merges inside a thread-block
+// cluster of its chunk CTAs unless GQA_Q8_CLUSTER=0 asks for the last-CTA merge through the
+// workspace (comparison and parity cross-check).
+bool q8_cluster_merge() {
+  const char* k = std::getenv("GQA_Q8_CLUSTER");
+  return !(k && std::strcmp(k, "0") == 0);
+}
+
 int head_split_for(int kind, int group) {
   if (kind == GQA_KIND_TQ) {  // the TurboQuant kernels serve up to 8 heads of a group per CTA
     for (int hs = 1; hs <= group; ++hs)

@@ -16,22 +16,13 @@ static cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, cons
   return cudaGetLastError();
 }
 
-template <int NHG>
-static cudaError_t launch_mma_q8(const PartialParams& p, dim3 grid, cudaStream_t s) {
-  using C = MmaQ8Cfg<64, NHG>;
-  const void* fn = reinterpret_cast<const void*>(&partial_mma_q8_kernel<64, NHG>);
-  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  partial_mma_q8_kernel<64, NHG><<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(p);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_partial_q8_d64(Variant v, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PartialParams& p, dim3 grid, int threads,
                                     cudaStream_t s) {
   constexpr Kind K = Kind::Q8;
   if (v.mma)
-    return p.group / p.head_split <= 8 ? launch_mma_q8<1>(p, grid, s) : launch_mma_q8<2>(p, grid, s);
+    return p.group / p.head_split <= 8 ? launch_mma_q8<64, 1>(p, grid, s)
+                                       : launch_mma_q8<64, 2>(p, grid, s);
   if (v.nps == 8) return launch_one<K, 64, 4, 8>(tk, tv, p, grid, threads, s);
   if (v.nps == 4) {
     if (v.gw == 1) return launch_one<K, 64, 1, 4>(tk, tv, p, grid, threads, s);

@@ -62,6 +62,9 @@ struct PartialParams {
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at
   long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
   int pdl;                 // f16 tensor-core kernel launched as a programmatic dependent
+  int cluster;             // int8 tensor-core kernel: > 1 when the row's chunk CTAs form one
+                           // thread-block cluster (dims (n_split, 1, 1)) and merge through
+                           // distributed shared memory instead of the arrival counters
 };
 
 // The sigmoid output gate that both pages apply to the merged row (qsa2.metal, qsa_merge2;

@@ -25,6 +25,8 @@
 // position's bytes 4n .. 4n+3 serves all four n-tiles.
 #pragma once
 
+#include <atomic>
+
 #include "partial_mma.cuh"
 
 namespace gqa {
@@ -64,7 +66,12 @@ struct MmaQ8Cfg {
   static constexpr int XC_OFF = QF_OFF + QF_BYTES;
   static constexpr int XC_BYTES = DSPLIT > 1 ? NPAIR * 2 * DSPLIT * 32 * 16 : 0;
   static constexpr int SMEM_BYTES = 1024 + XC_OFF + XC_BYTES;
+  // a cluster-merged row: this CTA's partial [head][D + 2] (acc | m | l), beside the merge area
+  static constexpr int CP_OFF = align_up(MERGE_BYTES, 16);
+  static constexpr int CP_BYTES = NHG * 8 * (D + 2) * 4;
+  static constexpr int MAX_CLUSTER = 8;
   static constexpr float RESCALE_LOG2 = 8.f;
+  static_assert(CP_OFF + CP_BYTES <= NST * STAGE_BYTES, "cluster partial inside the stages");
   static_assert(TPW % 16 == 0, "whole 16-row blocks per warp");
   static_assert(DSPLIT <= 2 && 2 + NPAIR <= 16, "one named barrier per warp pair");
   static_assert(MERGE_BYTES <= NST * STAGE_BYTES, "merge area aliases the stages");
@@ -96,6 +103,8 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
   const int G = p.group / p.head_split;           // query heads served by this CTA (<= 8 NHG)
   const int head0 = g * p.group + (blockIdx.y % p.head_split) * G;  // its first query head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the row's chunk CTAs merge inside their cluster (only when the launch made one of them)
+  const bool clus = p.cluster > 1 && cluster_nctarank() == static_cast<uint32_t>(p.cluster);
 
   // ---- the row's visited list (uniform over the CTA)
   int L = __ldg(p.kv_len + t);
@@ -122,6 +131,10 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
     if (c == 0)  // empty context: zeros (flash_attention.metal, seq_len == 0), split or not
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)
         p.out[((size_t)t * p.n_heads + head0 + i / D) * D + i % D] = 0.f;
+    if (clus) {  // the cluster's two barriers count every thread of every CTA
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
   const int ntiles = (c1 - c0 + C::TP - 1) / C::TP;
@@ -141,6 +154,10 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
 
   if (warp == C::NCW) {  // ---- producer warp
     produce_gather<C, D>(p, stages, full, empty, ntiles, t, g, s, L, c0, c1, lane);
+    if (clus) {
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
@@ -394,7 +411,14 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
       Ls = fmaf(rr2[D + 1], e, Ls);
     }
     const int head = head0 + h2;
-    if (p.merge) {
+    if (clus) {  // log2 units, as the cluster merge below takes them
+      float* cp = reinterpret_cast<float*>(stages + C::CP_OFF) + h2 * (D + 2);
+      cp[d] = A;
+      if (d == 0) {
+        cp[D] = M;
+        cp[D + 1] = Ls;
+      }
+    } else if (p.merge) {
       float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
       pr[d] = A;
       if (d == 0) {
@@ -405,8 +429,83 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
       p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
     }
   }
+  if (clus) {
+    // ---- merge the row's chunks through distributed shared memory: chunk CTA r holds chunk
+    //      r's partial; the CTAs of chunks 0 .. nchunks-1 share the (head, dim) outputs
+    cluster_sync();  // every chunk's partial is in place
+    const uint32_t cpa = smem_addr(stages + C::CP_OFF);
+    for (int idx = c * C::NCW * 32 + threadIdx.x; idx < G * D; idx += nchunks * C::NCW * 32) {
+      const int h2 = idx / D, d = idx % D;
+      const uint32_t rec = cpa + static_cast<uint32_t>(h2 * (D + 2)) * 4u;
+      float mr[C::MAX_CLUSTER], ar[C::MAX_CLUSTER], lr[C::MAX_CLUSTER];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+        mr[r] = -INFINITY;
+        ar[r] = lr[r] = 0.f;
+        if (r < nchunks) {
+          mr[r] = ld_cluster_f32(cluster_map(rec + D * 4u, r));
+          lr[r] = ld_cluster_f32(cluster_map(rec + (D + 1) * 4u, r));
+          ar[r] = ld_cluster_f32(cluster_map(rec + d * 4u, r));
+        }
+        M = fmaxf(M, mr[r]);
+      }
+      float A = 0.f, Ls = 0.f;
+#pragma unroll
+      for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+        const float e = mr[r] == -INFINITY ? 0.f : fast_exp2(mr[r] - M);
+        A = fmaf(ar[r], e, A);
+        Ls = fmaf(lr[r], e, Ls);
+      }
+      const int head = head0 + h2;
+      p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    return;
+  }
   if (p.merge)
     merge_if_last<D>(p, t, head0, G, (size_t)t * gridDim.y + blockIdx.y, nchunks, C::NCW);
+}
+
+// Launches the kernel.  A split row whose chunks fit one cluster (2 .. 8 CTAs) goes out as
+// clusters of its chunk CTAs, which merge in distributed shared memory (no partial records, no
+// arrival counters), unless GQA_Q8_CLUSTER=0 or the GPU cannot hold such a cluster.
+template <int D, int NHG>
+cudaError_t launch_mma_q8(PartialParams p, dim3 grid, cudaStream_t s) {
+  using C = MmaQ8Cfg<D, NHG>;
+  auto kern = &partial_mma_q8_kernel<D, NHG>;
+  const void* fn = reinterpret_cast<const void*>(kern);
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  p.cluster = 0;
+  if (p.merge && grid.x > 1 && grid.x <= static_cast<unsigned>(C::MAX_CLUSTER) &&
+      q8_cluster_merge()) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = grid.x;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::MAX_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    static std::atomic<int> fits[C::MAX_CLUSTER + 1];  // per cluster size: 0 unknown, 1, 2 no
+    if (fits[grid.x].load() == 0) {
+      int n = 0;
+      const bool ok = cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0;
+      if (!ok) (void)cudaGetLastError();
+      fits[grid.x].store(ok ? 1 : 2);
+    }
+    if (fits[grid.x].load() == 1) {
+      p.cluster = static_cast<int>(grid.x);
+      return cudaLaunchKernelEx(&cfg, kern, p);
+    }
+  }
+  kern<<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace gqa
