@@ -342,7 +342,7 @@ template <class C, int D>
 __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* stages,
                                                uint64_t* full, uint64_t* empty, int ntiles,
                                                int t, int g, int s, int L, int c0, int c1,
-                                               int lane) {
+                                               int lane, const int* first = nullptr) {
   const uint8_t* kq = static_cast<const uint8_t*>(p.kc);
   const uint8_t* vq = static_cast<const uint8_t*>(p.vc);
   constexpr int RPL = C::TP / 32;  // rows of a tile per lane
@@ -355,7 +355,12 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
     }
   };
   int cur[RPL], nxt[RPL];
-  fetch(0, cur);
+  if (first) {  // tile 0's entries, fetched by the caller (any value where j >= c1)
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) cur[k] = first[k];
+  } else {
+    fetch(0, cur);
+  }
   int issued = 0;
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {

@@ -105,6 +105,27 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the row's chunk CTAs merge inside their cluster (only when the launch made one of them)
   const bool clus = p.cluster > 1 && cluster_nctarank() == static_cast<uint32_t>(p.cluster);
+  if (p.pdl) {
+    // launched as a programmatic dependent of the previous kernel on the stream (e.g. the
+    // top-k selection that writes ids): wait for its completion and memory before touching
+    // global memory; the next such launch may be scheduled from here on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
+
+  // ---- the first tile's visited-list entries, loaded by the producer warp beside the row's
+  //      length rather than after it (any chunk's entries lie below min(chunk end, budget))
+  constexpr int RPL = C::TP / 32;
+  int first[RPL];
+  const bool pre = warp == C::NCW && p.ids != nullptr;
+  if (pre) {
+    const int j0 = c * p.chunk, lim = min(j0 + p.chunk, p.budget);
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int j = j0 + lane + 32 * k;
+      first[k] = j < lim ? __ldg(p.ids + (size_t)t * p.budget + j) : 0;
+    }
+  }
 
   // ---- the row's visited list (uniform over the CTA)
   int L = __ldg(p.kv_len + t);
@@ -153,7 +174,8 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
   __syncthreads();
 
   if (warp == C::NCW) {  // ---- producer warp
-    produce_gather<C, D>(p, stages, full, empty, ntiles, t, g, s, L, c0, c1, lane);
+    produce_gather<C, D>(p, stages, full, empty, ntiles, t, g, s, L, c0, c1, lane,
+                         pre ? first : nullptr);
     if (clus) {
       cluster_sync();
       cluster_sync();
@@ -477,21 +499,23 @@ cudaError_t launch_mma_q8(PartialParams p, dim3 grid, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(kern);
   cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = grid.x;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::MAX_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;  // the cluster alone (occupancy query)
   p.cluster = 0;
   if (p.merge && grid.x > 1 && grid.x <= static_cast<unsigned>(C::MAX_CLUSTER) &&
       q8_cluster_merge()) {
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = grid.x;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(C::MAX_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
     static std::atomic<int> fits[C::MAX_CLUSTER + 1];  // per cluster size: 0 unknown, 1, 2 no
     if (fits[grid.x].load() == 0) {
       int n = 0;
@@ -499,13 +523,12 @@ cudaError_t launch_mma_q8(PartialParams p, dim3 grid, cudaStream_t s) {
       if (!ok) (void)cudaGetLastError();
       fits[grid.x].store(ok ? 1 : 2);
     }
-    if (fits[grid.x].load() == 1) {
-      p.cluster = static_cast<int>(grid.x);
-      return cudaLaunchKernelEx(&cfg, kern, p);
-    }
+    if (fits[grid.x].load() == 1) p.cluster = static_cast<int>(grid.x);
   }
-  kern<<<grid, C::MAX_THREADS, C::SMEM_BYTES, s>>>(p);
-  return cudaGetLastError();
+  // [cluster][programmatic dependent], whichever apply
+  cfg.attrs = p.cluster ? at : at + 1;
+  cfg.numAttrs = (p.cluster ? 1 : 0) + (p.pdl ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace gqa

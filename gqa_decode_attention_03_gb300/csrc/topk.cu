@@ -76,6 +76,9 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ uint32_t slots[2][kSelWarps];
   __shared__ uint32_t hist[2][kSelWarps][kSelBins];  // per-warp digit histograms, two steps
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // a decode launched after this kernel as a programmatic dependent may be scheduled now: its
+  // CTAs set up beside this one and wait for this grid's completion before reading ids
+  asm volatile("griddepcontrol.launch_dependents;");
   int n = __ldg(kv_len + t);
   if (n < 0 || n > max_kv_len) {
     if (tid == 0) flag_error(err, GQA_ERR_KVLEN_RANGE);
