@@ -338,19 +338,22 @@ __device__ __forceinline__ void produce_tma(const CUtensorMap* tmK, const CUtens
 // the staged bytes stay finite.  The ids of tile i + 1 are loaded before tile i's copies are
 // issued (a lane's rows of a tile at once), so their latency overlaps the copies instead of
 // preceding each row's.
-template <class C, int D>
+template <class C, int D, int NPW = 1>
 __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* stages,
                                                uint64_t* full, uint64_t* empty, int ntiles,
                                                int t, int g, int s, int L, int c0, int c1,
-                                               int lane, const int* first = nullptr) {
+                                               int lane, const int* first = nullptr,
+                                               int pw = 0) {
   const uint8_t* kq = static_cast<const uint8_t*>(p.kc);
   const uint8_t* vq = static_cast<const uint8_t*>(p.vc);
-  constexpr int RPL = C::TP / 32;  // rows of a tile per lane
+  // rows of a tile per lane: producer warp pw of NPW takes rows lane + 32 (pw + NPW k)
+  constexpr int RPL = C::TP / 32 / NPW;
+  static_assert(C::TP % (32 * NPW) == 0, "whole rows per lane");
   static_assert(C::TP % 32 == 0, "whole rows per lane");
   auto fetch = [&](int i, int (&cell)[RPL]) {  // the visited-list entries of tile i
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
-      const int j = c0 + i * C::TP + lane + 32 * k;
+      const int j = c0 + i * C::TP + lane + 32 * (pw + NPW * k);
       cell[k] = j < c1 ? (p.ids ? __ldg(p.ids + (size_t)t * p.budget + j) : j) : 0;
     }
   };
@@ -380,7 +383,7 @@ __device__ __forceinline__ void produce_gather(const PartialParams& p, uint8_t* 
     int* rowok = reinterpret_cast<int*>(sk + C::KV_BYTES + C::SC_BYTES);
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
-      const int r = lane + 32 * k;
+      const int r = lane + 32 * (pw + NPW * k);
       const int j = c0 + i * C::TP + r;  // index into the visited list
       int okr = 0;
       if (j < c1) {

@@ -52,7 +52,11 @@ struct MmaQ8Cfg {
   static constexpr int NJ = DW / 32;               // 32-dim blocks of p.v per warp
   static constexpr int KS = D / 16;
   static constexpr int NCW = NPS * NHG * DSPLIT;
-  static constexpr int MAX_THREADS = 32 * (NCW + 1);
+  // gather warps: two share a tile's rows (GB300, 1024 selected cells: a 64-row tile's copies
+  // go out in ~1.3 us either way -- the SM's bytes in flight bound them -- and two warps take
+  // ~0.2 us off the first)
+  static constexpr int NPW = 2;
+  static constexpr int MAX_THREADS = 32 * (NCW + NPW);
   static constexpr int MERGE_BYTES = NPS * NHG * 8 * (D + 2) * 4;
   // at D = 256 q's A fragments live in shared memory ([head group][k-step][lane] x 16 bytes),
   // not in 64 registers a thread
@@ -115,14 +119,15 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
 
   // ---- the first tile's visited-list entries, loaded by the producer warp beside the row's
   //      length rather than after it (any chunk's entries lie below min(chunk end, budget))
-  constexpr int RPL = C::TP / 32;
+  constexpr int RPL = C::TP / 32 / C::NPW;
   int first[RPL];
-  const bool pre = warp == C::NCW && p.ids != nullptr;
+  const int pw = warp - C::NCW;  // gather warp index (consumers: negative)
+  const bool pre = pw >= 0 && p.ids != nullptr;
   if (pre) {
     const int j0 = c * p.chunk, lim = min(j0 + p.chunk, p.budget);
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
-      const int j = j0 + lane + 32 * k;
+      const int j = j0 + lane + 32 * (pw + C::NPW * k);
       first[k] = j < lim ? __ldg(p.ids + (size_t)t * p.budget + j) : 0;
     }
   }
@@ -166,16 +171,16 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
   uint64_t* empty = full + C::NST;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&full[i], 64);  // the gather: 32 lanes' arrivals and their cp.async arrivals
+      mbar_init(&full[i], 64 * C::NPW);  // per gather lane: an arrival and a cp.async one
       mbar_init(&empty[i], C::NCW);
     }
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == C::NCW) {  // ---- producer warp
-    produce_gather<C, D>(p, stages, full, empty, ntiles, t, g, s, L, c0, c1, lane,
-                         pre ? first : nullptr);
+  if (pw >= 0) {  // ---- gather warps
+    produce_gather<C, D, C::NPW>(p, stages, full, empty, ntiles, t, g, s, L, c0, c1, lane,
+                                 pre ? first : nullptr, pw);
     if (clus) {
       cluster_sync();
       cluster_sync();
