@@ -68,15 +68,18 @@ inline cudaError_t launch_streamk_f16(int head_dim, const CUtensorMap& tk, const
   return launch_streamk_f16_d256(tk, tv, p, grid, s);
 }
 
-cudaError_t launch_rows_f16_d64(const CUtensorMap&, const CUtensorMap&, const PartialParams&,
-                               dim3, cudaStream_t);
-cudaError_t launch_rows_f16_d128(const CUtensorMap&, const CUtensorMap&, const PartialParams&,
-                                dim3, cudaStream_t);
+// tq: the q tensor map of the tcgen05 row kernel ([n_tok][n_heads][D] fp32, box D x G x rows
+// of a group); the mma.sync row kernel reads q directly
+cudaError_t launch_rows_f16_d64(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                               const PartialParams&, dim3, cudaStream_t);
+cudaError_t launch_rows_f16_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                const PartialParams&, dim3, cudaStream_t);
 
 inline cudaError_t launch_rows_f16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const PartialParams& p, dim3 grid, cudaStream_t s) {
-  return head_dim == 64 ? launch_rows_f16_d64(tk, tv, p, grid, s)
-                        : launch_rows_f16_d128(tk, tv, p, grid, s);
+                                   const CUtensorMap& tq, const PartialParams& p, dim3 grid,
+                                   cudaStream_t s) {
+  return head_dim == 64 ? launch_rows_f16_d64(tk, tv, tq, p, grid, s)
+                        : launch_rows_f16_d128(tk, tv, tq, p, grid, s);
 }
 
 cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid, int n_split,

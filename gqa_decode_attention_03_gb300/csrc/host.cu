@@ -459,9 +459,10 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     p.n_valid = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + cnt + (part + 255) / 256 * 256);
   }
 
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   std::memset(&tk, 0, sizeof tk);
   std::memset(&tv, 0, sizeof tv);
+  std::memset(&tq, 0, sizeof tq);
   if (kind == GQA_KIND_F16) {
     auto encode = tensor_map_encoder();
     if (!encode) return fail(GQA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
@@ -477,6 +478,20 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(GQA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    if (plan.row_group > 1 && gqa::rows_on_umma()) {
+      // the tcgen05 row kernel stages a group's fp32 q [rows][G heads][D] with one copy: box
+      // D x G x 64 / G rows (rows past n_tok read as zeros)
+      const int G = n_heads / n_kv_heads;
+      const cuuint64_t qdims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_heads, (cuuint64_t)n_tok};
+      const cuuint64_t qstr[2] = {(cuuint64_t)head_dim * 4,
+                                  (cuuint64_t)head_dim * 4 * (cuuint64_t)n_heads};
+      const cuuint32_t qbox[3] = {(cuuint32_t)head_dim, (cuuint32_t)G, (cuuint32_t)(64 / G)};
+      CUresult r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(q), qdims,
+                          qstr, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(GQA_ECUDA, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
     }
   }
 
@@ -516,12 +531,12 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
   p.merge_spin = spin ? (unsigned)std::strtoul(spin, nullptr, 10) : gqa::kSpinLimit;
   cudaError_t e =
       plan.streamk        ? gqa::launch_streamk_f16(head_dim, tk, tv, p, grid, stream)
-      : plan.row_group > 1 ? gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream)
+      : plan.row_group > 1 ? gqa::launch_rows_f16(head_dim, tk, tv, tq, p, grid, stream)
                            : gqa::launch_partial(kind, head_dim, var, tk, tv, p, grid, threads, stream);
   if (e == cudaErrorCooperativeLaunchTooLarge && p.fused_merge) {  // not all resident after all
     (void)cudaGetLastError();
     p.fused_merge = 0;
-    e = gqa::launch_rows_f16(head_dim, tk, tv, p, grid, stream);
+    e = gqa::launch_rows_f16(head_dim, tk, tv, tq, p, grid, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "partial kernel launch");
   if (plan.merge && !plan.streamk && plan.row_group > 1 && !p.fused_merge) {

@@ -59,7 +59,7 @@ cudaError_t launch_streamk_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv
   return p.group <= 8 ? launch_sk<1>(tk, tv, p, grid, s) : launch_sk<2>(tk, tv, p, grid, s);
 }
 
-cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                                 const PartialParams& p, dim3 grid, cudaStream_t s) {
   if (rows_on_umma()) {
     using U = UmmaRowsCfg<128>;
@@ -78,7 +78,7 @@ cudaError_t launch_rows_f16_d128(const CUtensorMap& tk, const CUtensorMap& tv,
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.fused_merge ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, umma_rows_kernel<128>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, umma_rows_kernel<128>, tk, tv, tq, p);
   }
   using C = RowsCfg<128>;
   const void* fn = reinterpret_cast<const void*>(&partial_mma_rows_kernel<128>);

@@ -94,9 +94,9 @@ struct RowGroup {
   int t0, nr, s, lmax;
 };
 
-__device__ __forceinline__ int rows_len(const PartialParams& p, int t, bool seq_ok, int* err) {
+// Row t's length L (kv_len[t] as read), clamped to the cache and zero for a bad sequence.
+__device__ __forceinline__ int rows_len_of(const PartialParams& p, int L, bool seq_ok, int* err) {
   const int lmax = static_cast<int>(p.cache_cap < p.max_kv_len ? p.cache_cap : p.max_kv_len);
-  int L = __ldg(p.kv_len + t);
   if (L < 0 || L > lmax) {
     *err |= GQA_ERR_KVLEN_RANGE;
     L = L < 0 ? 0 : lmax;
@@ -108,7 +108,14 @@ __device__ __forceinline__ int rows_len(const PartialParams& p, int t, bool seq_
   return L;
 }
 
-__device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, int R, int lane) {
+__device__ __forceinline__ int rows_len(const PartialParams& p, int t, bool seq_ok, int* err) {
+  return rows_len_of(p, __ldg(p.kv_len + t), seq_ok, err);
+}
+
+// len0: kv_len[lane] for rows 0..31 when the caller loaded them beside the leader search (so
+// that a group among the first 32 rows costs no second round trip); used when have_len0.
+__device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, int R, int lane,
+                                               int len0 = 0, bool have_len0 = false) {
   RowGroup gr;
   gr.t0 = t0;
   gr.s = rows_seq(p, t0);
@@ -126,7 +133,11 @@ __device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, i
   const bool seq_ok = gr.s >= 0 && gr.s < p.n_seq;
   int err = 0;
   int L = 0;
-  for (int jj = lane; jj < gr.nr; jj += 32) L = max(L, rows_len(p, t0 + jj, seq_ok, &err));
+  const int lw = __shfl_sync(0xffffffffu, len0, (t0 + lane) & 31);  // row t0 + lane's, if < 32
+  for (int jj = lane; jj < gr.nr; jj += 32) {
+    const int t = t0 + jj;
+    L = max(L, have_len0 && t < 32 ? rows_len_of(p, lw, seq_ok, &err) : rows_len(p, t, seq_ok, &err));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L = max(L, __shfl_xor_sync(0xffffffffu, L, o));
   gr.lmax = L;

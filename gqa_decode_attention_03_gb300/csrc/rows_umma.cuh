@@ -5,23 +5,28 @@
 // serves a group of up to 64 / G such rows for one KV head and one chunk of positions, so every
 // K/V tile is read from HBM once for all of the group's (row, head) pairs (attention_gqa.metal's
 // "load K/V once, reuse across the group", widened from the heads of a group to the rows of a
-// sequence).  The group's 64 pairs are the M = 64 rows of the MMAs.
+// sequence).  The group's 64 pairs are the rows of the MMAs.
 //
 // Per 64-position tile, flash-attention style:
-//   S  = Q . K^T    M = 64 pairs, N = 64 positions, K = D: Q (scale * log2 e folded in) as an f16
-//                   hi part and an f16 lo remainder (about 22 bits of the fp32 q, two MMAs per
-//                   k-step accumulating into the same S) and the K tile K-major in shared memory;
-//                   S in TMEM (row i in lane 32 (i / 16) + i % 16).
+//   S  = Q . K^T    M = 128, N = 64 positions, K = D: Q (scale * log2 e folded in) as an f16 hi
+//                   part in row 32 (p / 16) + p % 16 for pair p and its f16 lo remainder 16 rows
+//                   below (about 22 bits of the fp32 q), the K tile K-major in shared memory; S
+//                   in TMEM, row r in lane r, so a pair's hi and lo rows sit in the lanes of one
+//                   softmax warp.  (An M = 64 MMA costs what an M = 128 one does: one MMA per
+//                   k-step carries both parts.)
 //   softmax         two threads per pair: thread (warp w, lane l) owns pair 16 w + l % 16 and
-//                   the tile's positions [32 h, 32 h + 32), h = l / 16 (one tcgen05.ld 16x32bx2).
+//                   the tile's positions [32 h, 32 h + 32), h = l / 16.  Each reads its own
+//                   lane's 64 columns (two tcgen05.ld 32x32b) and swaps 32 of them with its
+//                   partner (lane l xor 16), so that it holds hi + lo for its half.
 //                   It masks positions at or past its row's length; the two halves' maxima meet
 //                   by one shuffle, so both keep the same running max, and each keeps its own
 //                   part of the running sum.  The max moves lazily (only when a tile's max
 //                   exceeds it by more than 2^8, so p <= 256); when it moves, each thread
 //                   rescales its half of the pair's O row in TMEM (ld, scale, st) after the
 //                   previous tile's P.V has completed.
-//   O += P . V      P (f16, written by the softmax threads into shared memory, K-major) times the
-//                   V tile read MN-major (N = D contiguous), accumulated in TMEM.
+//   O += P . V      M = 64 pairs: P (f16, written by the softmax threads into shared memory,
+//                   K-major) times the V tile read MN-major (N = D contiguous), accumulated in
+//                   TMEM (row i in lane 32 (i / 16) + i % 16).
 // Three S buffers in TMEM and three P buffers in shared memory let the tensor cores run up to two
 // tiles' S ahead of the softmax.  K/V tiles stream through a four-stage TMA ring;
 // the group's fp32 q arrives first, by bulk copies from the producer into a staging area, and is
@@ -41,9 +46,8 @@
 // step).  Before TMEM is freed each issuer waits for all of its MMAs to complete.
 //
 // MMA cost (measured on GB300, one thread issuing back to back): M64 N64 K16 ~56 cycles, M64
-// N128 K16 ~70, M128 N256 K16 ~133 (the dense peak).  M = 64 half-fills the tensor core, which a
-// group of 64 pairs cannot avoid; the kernel is bound by its K/V stream and the softmax, not the
-// MMAs.
+// N128 K16 ~70, M128 N256 K16 ~133 (the dense peak).  M = 64 half-fills the tensor core: P.V
+// leaves that half empty, S fills it with q's lo rows.
 //
 // Groups, slots, the per-row bookkeeping (n_valid, empty rows) and the partial format are those
 // of the mma.sync row kernel (rows_mma.cuh).  Split rows are merged inside this kernel when the
@@ -68,9 +72,12 @@ struct UmmaRowsCfg {
   static constexpr int KV_BYTES = NBOX * BOX_BYTES;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K boxes, then V boxes
   static constexpr int NST = 4;
-  static constexpr int Q_BOX = M * 128;            // Q: [box][64 pairs][128 bytes]
-  static constexpr int Q_PLANE = NBOX * Q_BOX;     // one f16 part of Q
-  static constexpr int Q_BYTES = 2 * Q_PLANE;      // its hi part, then its lo part
+  // S = Q.K^T runs at M = 128: pair p's q as f16 hi in row 32 (p / 16) + p % 16 and its f16 lo
+  // remainder 16 rows below, so that both land in the TMEM lanes of one softmax warp.  An
+  // M = 64 MMA costs as much as an M = 128 one: the lo rows ride along for free.
+  static constexpr int MS = 128;
+  static constexpr int Q_BOX = MS * 128;           // Q: [box][128 rows][128 bytes]
+  static constexpr int Q_BYTES = NBOX * Q_BOX;
   static constexpr int P_BYTES = M * TP * 2;       // P: [64 pairs][64 positions] f16
   static constexpr int NPB = 3;                    // S buffers (TMEM) and P buffers (smem)
   static constexpr int S_COL = 0, O_COL = NPB * TP;
@@ -207,7 +214,8 @@ __device__ void rows_fused_merge(const PartialParams& p, const RowGroup& gr, int
 template <int D>
 __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     umma_rows_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const PartialParams p) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const PartialParams p) {
   using C = UmmaRowsCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y, slot = blockIdx.z, nslots = gridDim.z;
@@ -253,9 +261,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
   // Every warp walks the same groups (k = slot, slot + nslots, ...) in the same order.  The first
   // group is looked up while thread 0 sets up the barriers and the issuer warp allocates TMEM.
   int scan_t = 0, scan_cnt = 0;
+  // rows 0..31's lengths, loaded beside the leader search's reads of seq_of
+  const int len0 = lane < p.n_tok ? __ldg(p.kv_len + lane) : 0;
   const int t0_first = rows_find_leader(p, R, slot, scan_t, scan_cnt, lane);
   RowGroup gr_first{};
-  if (t0_first >= 0) gr_first = rows_group(p, t0_first, R, lane);
+  if (t0_first >= 0) gr_first = rows_group(p, t0_first, R, lane, len0, true);
   auto group = [&](int k, RowGroup& gr) {  // the k-th group's leader (-1 past the last)
     if (k == slot) {
       gr = gr_first;
@@ -276,6 +286,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmQ);
     }
     int it = 0, gn = 0;
     for (int k = slot; ok; k += nslots) {
@@ -284,16 +295,15 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       if (t0 < 0) break;
       const int c1 = min(c0 + p.chunk, gr.lmax);
       if (c1 <= c0) continue;
-      // the group's fp32 q first (one bulk copy per row: its G heads are contiguous), into the
-      // staging area once the previous group's epilogue is done with it
+      // the group's fp32 q first (one TMA box: its rows' G heads, rows past the group read
+      // too and ignored), into the staging area once the previous group's epilogue is done
+      // with it (16 bulk copies, one per row, took ~1.1 us to issue)
       if (gn > 0) ok = __all_sync(0xffffffffu, mbar_wait(x_free, (gn - 1) & 1));
       if (!ok) break;
       ++gn;
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_land, gr.nr * G * D * 4);
-        for (int jj = 0; jj < gr.nr; ++jj)
-          bulk_load(sX + jj * G * D * 4, p.q + ((size_t)(t0 + jj) * p.n_heads + g * G) * D,
-                    G * D * 4, q_land);
+        mbar_arrive_expect_tx(q_land, C::NP * D * 4);
+        tma_load_3d(sX, &tmQ, 0, g * G, t0, q_land);
       }
       const int zb = gr.s * static_cast<int>(p.cache_cap);
       for (int pos = c0; pos < c1; pos += C::TP, ++it) {
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
     //      O += P . V (two issuing threads keep both MMA streams going; MMAs of one shape issued
     //      back to back also run faster than alternating ones)
     const bool is_s = warp == C::ISSUER;
-    constexpr uint32_t kIdS = umma_idesc_f16(C::M, C::TP, false);
+    constexpr uint32_t kIdS = umma_idesc_f16(C::MS, C::TP, false);
     constexpr uint32_t kIdO = umma_idesc_f16(C::M, D, true);
     const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
     int it = 0, qn = 0;
@@ -358,12 +368,10 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
             for (int kk = 0; kk < C::KS_S; ++kk) {
               const uint32_t ko = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
               const uint32_t qo = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-              // q = hi + lo (f16 parts, about 22 bits), both against the f16 K tile
-              const uint64_t kdesc = umma_desc_sw128(sk + ko, 16, 1024);
+              // q's hi and lo rows (f16 parts, about 22 bits) against the f16 K tile
               umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
-                       umma_desc_sw128(q_addr + qo, 16, 1024), kdesc, kIdS, kk > 0 ? 1u : 0u);
-              umma_f16(tbase + C::S_COL + (i % C::NPB) * C::TP,
-                       umma_desc_sw128(q_addr + C::Q_PLANE + qo, 16, 1024), kdesc, kIdS, 1u);
+                       umma_desc_sw128(q_addr + qo, 16, 1024),
+                       umma_desc_sw128(sk + ko, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
             }
             umma_commit(&s_full[i % C::NPB]);
           } else {
@@ -466,10 +474,11 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
           uint2 hv, lv;  // the f16 hi part and the f16 lo remainder of q * scale * log2(e)
           split_hi_lo(v[u].x * sc, v[u].y * sc, hv.x, lv.x);
           split_hi_lo(v[u].z * sc, v[u].w * sc, hv.y, lv.y);
-          uint8_t* dst = sQ + (ch >> 3) * C::Q_BOX + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4) +
+          const int rh = 32 * (qr >> 4) + (qr & 15);  // the hi row; the lo row is rh + 16
+          uint8_t* dst = sQ + (ch >> 3) * C::Q_BOX + rh * 128 + (((ch & 7) ^ (rh & 7)) << 4) +
                          (c4 & 1) * 8;
           *reinterpret_cast<uint2*>(dst) = hv;
-          *reinterpret_cast<uint2*>(dst + C::Q_PLANE) = lv;
+          *reinterpret_cast<uint2*>(dst + 16 * 128) = lv;
         }
       }
       fence_async_smem();
@@ -482,9 +491,18 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
         const int it_j = it + j, b = it_j % C::NPB;
         wait(&s_full[b], (it_j / C::NPB) & 1);
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld16x2<C::CPT>(t_q + C::S_COL + b * C::TP, sr);
+        // lane l < 16 of this warp's quadrant holds q_hi.K of pair i, lane l + 16 its q_lo.K:
+        // each thread reads its lane's 64 columns, and the two swap halves so that this
+        // thread keeps the hi + lo sum of its 32 columns [32 h, 32 h + 32)
+        uint32_t sr[32], s0[32], s1[32];
+        tmem_ld32(t_q + C::S_COL + b * C::TP, s0);
+        tmem_ld32(t_q + C::S_COL + b * C::TP + 32, s1);
         tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float y = __uint_as_float(__shfl_xor_sync(0xffffffffu, h ? s0[e] : s1[e], 16));
+          sr[e] = __float_as_uint(__uint_as_float(h ? s1[e] : s0[e]) + y);
+        }
         const int lim = lim0 - j * C::TP;  // columns [0, lim) of this thread's 32
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
