@@ -87,7 +87,7 @@ cudaError_t launch_merge(int head_dim, const float* part, const int32_t* n_valid
                          const float* gate = nullptr, long long gate_stride = 0,
                          bool after_partials = false, const float* signs = nullptr);
 
-// Raises the function's dynamic shared-memory limit once per (function, device).
-cudaError_t ensure_smem(const void* fn, int bytes);
+// ensure_smem (raises a function's dynamic shared-memory limit) is declared in
+// partial_kernel.cuh.
 
 }  // namespace gqa

@@ -525,6 +525,15 @@ gqa_status decode_common(int kind, const float* q, const void* kc, const void* v
     const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
     p.fused_merge = ctas <= current_sm_count(&st) ? 1 : 0;
   }
+  // a split f16 grid that fits the GPU (latency-bound: a few short rows) may merge each row's
+  // chunks inside a thread-block cluster (partial_mma.cuh); GQA_F16_CLUSTER=0 keeps the
+  // last-CTA merge through the workspace
+  if (kind == GQA_KIND_F16 && plan.merge && !plan.streamk && plan.row_group == 1 && var.mma) {
+    st = GQA_OK;
+    const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
+    const char* k = std::getenv("GQA_F16_CLUSTER");
+    p.cluster = ctas <= current_sm_count(&st) && !(k && std::strcmp(k, "0") == 0) ? 1 : 0;
+  }
   // polls of the fused merge's wait before it gives up; GQA_MERGE_SPIN (tests) sets fewer,
   // 0 making every such wait run out at once
   const char* spin = std::getenv("GQA_MERGE_SPIN");

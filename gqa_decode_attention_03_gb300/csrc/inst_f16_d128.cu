@@ -21,26 +21,6 @@ static cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, cons
   return cudaGetLastError();
 }
 
-template <int D, int NHG>
-static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& p,
-                              dim3 grid, cudaStream_t s) {
-  using C = MmaCfg<D, NHG>;
-  const void* fn = reinterpret_cast<const void*>(&partial_mma_kernel<D, NHG>);
-  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(C::MAX_THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = p.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, partial_mma_kernel<D, NHG>, tk, tv, p);
-}
-
 template <int NHG>
 static cudaError_t launch_sk(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& p,
                              dim3 grid, cudaStream_t s) {
@@ -92,8 +72,8 @@ cudaError_t launch_partial_f16_d128(Variant v, const CUtensorMap& tk, const CUte
                                     const PartialParams& p, dim3 grid, int threads,
                                     cudaStream_t s) {
   constexpr Kind K = Kind::F16;
-  if (v.mma) return p.group <= 8 ? launch_mma<128, 1>(tk, tv, p, grid, s)
-                                 : launch_mma<128, 2>(tk, tv, p, grid, s);
+  if (v.mma) return p.group <= 8 ? launch_mma_f16<128, 1>(tk, tv, p, grid, s)
+                                 : launch_mma_f16<128, 2>(tk, tv, p, grid, s);
   if (v.nps == 4) {
     if (v.gw == 1) return launch_one<K, 128, 1, 4>(tk, tv, p, grid, threads, s);
     if (v.gw == 2) return launch_one<K, 128, 2, 4>(tk, tv, p, grid, threads, s);

@@ -24,6 +24,8 @@
 // all GW heads; p comes from a per-warp shared buffer (broadcast reads).
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gqa {
@@ -62,9 +64,10 @@ struct PartialParams {
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at
   long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
   int pdl;                 // f16 tensor-core kernel launched as a programmatic dependent
-  int cluster;             // int8 tensor-core kernel: > 1 when the row's chunk CTAs form one
-                           // thread-block cluster (dims (n_split, 1, 1)) and merge through
-                           // distributed shared memory instead of the arrival counters
+  int cluster;             // tensor-core per-row kernels: > 1 when the row's chunk CTAs form
+                           // one thread-block cluster (dims (n_split, 1, 1)) and merge through
+                           // distributed shared memory instead of the arrival counters (the
+                           // host sets 1 where the f16 kernel may, the launcher the size)
 };
 
 // The sigmoid output gate that both pages apply to the merged row (qsa2.metal, qsa_merge2;
@@ -295,6 +298,92 @@ __device__ __forceinline__ void merge_if_last(const PartialParams& p, int t, int
       for (int k = 0; k < DPL; k += 2) *reinterpret_cast<float2*>(o + k) = make_float2(a[k], a[k + 1]);
     }
   }
+}
+
+// The row's chunk CTAs, one thread-block cluster (chunk c = cluster rank c), each holding its
+// partial [head][D + 2] (acc | m in log2 units | l) at `cp` in its shared memory, merge by
+// log-sum-exp through distributed shared memory: after a cluster barrier, the CTAs of chunks
+// 0 .. nchunks-1 share the (head, dim) outputs, reading every chunk's partial, and write the
+// (gated) output; a second barrier keeps every CTA resident until all reads are done.  Every
+// thread of every CTA of the cluster must take both barriers (CTAs whose chunk is empty and
+// producer warps call cluster_sync twice instead).
+template <int D, int MAXC>
+__device__ __forceinline__ void cluster_merge(const PartialParams& p, int t, int head0, int nheads,
+                                              int c, int nchunks, const uint8_t* cp, int ncw) {
+  cluster_sync();  // every chunk's partial is in place
+  const uint32_t cpa = smem_addr(cp);
+  for (int idx = c * ncw * 32 + threadIdx.x; idx < nheads * D; idx += nchunks * ncw * 32) {
+    const int h2 = idx / D, d = idx % D;
+    const uint32_t rec = cpa + static_cast<uint32_t>(h2 * (D + 2)) * 4u;
+    float mr[MAXC], ar[MAXC], lr[MAXC];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < MAXC; ++r) {
+      mr[r] = -INFINITY;
+      ar[r] = lr[r] = 0.f;
+      if (r < nchunks) {
+        mr[r] = ld_cluster_f32(cluster_map(rec + D * 4u, r));
+        lr[r] = ld_cluster_f32(cluster_map(rec + (D + 1) * 4u, r));
+        ar[r] = ld_cluster_f32(cluster_map(rec + d * 4u, r));
+      }
+      M = fmaxf(M, mr[r]);
+    }
+    float A = 0.f, Ls = 0.f;
+#pragma unroll
+    for (int r = 0; r < MAXC; ++r) {
+      const float e = mr[r] == -INFINITY ? 0.f : fast_exp2(mr[r] - M);
+      A = fmaf(ar[r], e, A);
+      Ls = fmaf(lr[r], e, Ls);
+    }
+    const int head = head0 + h2;
+    p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
+  }
+  cluster_sync();  // no CTA leaves while another still reads its shared memory
+}
+
+// Host: raises the function's dynamic shared-memory limit once per (function, device)
+// (launch_util.cu).
+cudaError_t ensure_smem(const void* fn, int bytes);
+
+// Host: whether clusters of n CTAs of this launch configuration fit the GPU at all (asked once
+// per cluster size and kernel instantiation), and the launch attributes for a cluster of n
+// (n > 1) and a programmatic dependent launch; returns how many were written to at[0..1].
+template <int MAXC>
+bool cluster_fits(const void* fn, const cudaLaunchConfig_t& cfg0, unsigned n) {
+  static std::atomic<int> fits[MAXC + 1];  // 0 unknown, 1 yes, 2 no
+  if (n < 2 || n > static_cast<unsigned>(MAXC)) return false;
+  if (fits[n].load() == 0) {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = n;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = cfg0;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int k = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&k, fn, &cfg) == cudaSuccess && k > 0;
+    if (!ok) (void)cudaGetLastError();
+    fits[n].store(ok ? 1 : 2);
+  }
+  return fits[n].load() == 1;
+}
+
+inline int cluster_attrs(cudaLaunchAttribute* at, int cluster, int pdl) {
+  int n = 0;
+  if (cluster > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  return n;
 }
 
 // ------------------------------------------------------------------------------ producers

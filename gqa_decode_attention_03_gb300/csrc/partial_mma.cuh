@@ -50,8 +50,13 @@ struct MmaCfg {
   static constexpr int MERGE_BYTES = NPS * NHG * 8 * (D + 2) * 4;
   static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + 2 * NST * 8;
   static constexpr float RESCALE_LOG2 = 8.f;                  // lazy-rescale threshold
+  // a cluster-merged row: this CTA's partial [head][D + 2] (acc | m | l), beside the merge area
+  static constexpr int CP_OFF = align_up(MERGE_BYTES, 16);
+  static constexpr int CP_BYTES = NHG * 8 * (D + 2) * 4;
+  static constexpr int MAX_CLUSTER = 8;
   static_assert(TPW % 16 == 0, "whole 16-row blocks per warp");
   static_assert(MERGE_BYTES <= NST * STAGE_BYTES, "merge area aliases the stages");
+  static_assert(CP_OFF + CP_BYTES <= NST * STAGE_BYTES, "cluster partial inside the stages");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -97,6 +102,8 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y;
   const int t = blockIdx.z;
+  // the row's chunk CTAs merge inside their cluster (only when the launch made one of them)
+  const bool clus = p.cluster > 1 && cluster_nctarank() == static_cast<uint32_t>(p.cluster);
   if (p.pdl) {
     // launched as a programmatic dependent of the previous kernel on the stream: wait for its
     // completion and memory before touching global memory, and let the next such launch be
@@ -132,6 +139,10 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
     if (c == 0)  // empty context: zeros (flash_attention.metal, seq_len == 0), split or not
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)
         p.out[((size_t)t * p.n_heads + g * G + i / D) * D + i % D] = 0.f;
+    if (clus) {  // the cluster's two barriers count every thread of every CTA
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
   const int ntiles = (c1 - c0 + C::TP - 1) / C::TP;
@@ -153,6 +164,11 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
     if (lane == 0)
       produce_tma<C>(&tmK, &tmV, stages, full, empty, ntiles, g,
                      s * static_cast<int>(p.cache_cap) + c0, p.err);
+    __syncwarp();
+    if (clus) {
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
@@ -314,7 +330,14 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
       Ls = fmaf(rr2[D + 1], e, Ls);
     }
     const int head = g * G + h2;
-    if (p.merge) {
+    if (clus) {  // log2 units, as the cluster merge below takes them
+      float* cp = reinterpret_cast<float*>(stages + C::CP_OFF) + h2 * (D + 2);
+      cp[d] = A;
+      if (d == 0) {
+        cp[D] = M;
+        cp[D + 1] = Ls;
+      }
+    } else if (p.merge) {
       float* pr = p.part + (((size_t)t * p.n_split + c) * p.n_heads + head) * (D + 2);
       pr[d] = A;
       if (d == 0) {
@@ -325,9 +348,39 @@ __global__ void __launch_bounds__(MmaCfg<D, NHG>::MAX_THREADS, MmaCfg<D, NHG>::M
       p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
     }
   }
+  if (clus) {
+    cluster_merge<D, C::MAX_CLUSTER>(p, t, g * G, G, c, nchunks, stages + C::CP_OFF, C::NCW);
+    return;
+  }
   if (p.merge)
     merge_if_last<D>(p, t, g * G, G, (size_t)t * p.n_kv_heads + g, nchunks,
                      C::NCW);
+}
+
+// Launches the kernel, as a programmatic dependent when p.pdl.  When the host allows it
+// (p.cluster != 0: a split grid that fits the GPU) and a row's chunks fit one cluster (2 .. 8),
+// the chunk CTAs of a row go out as one thread-block cluster and merge in distributed shared
+// memory instead of through the workspace.
+template <int D, int NHG>
+cudaError_t launch_mma_f16(const CUtensorMap& tk, const CUtensorMap& tv, PartialParams p,
+                           dim3 grid, cudaStream_t s) {
+  using C = MmaCfg<D, NHG>;
+  auto kern = &partial_mma_kernel<D, NHG>;
+  const void* fn = reinterpret_cast<const void*>(kern);
+  cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::MAX_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  const bool want = p.cluster != 0 && p.merge && grid.x > 1 &&
+                    grid.x <= static_cast<unsigned>(C::MAX_CLUSTER);
+  p.cluster = want && cluster_fits<C::MAX_CLUSTER>(fn, cfg, grid.x) ? static_cast<int>(grid.x) : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = cluster_attrs(at, p.cluster, p.pdl);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace gqa

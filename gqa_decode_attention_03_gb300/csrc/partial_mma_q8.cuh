@@ -25,8 +25,6 @@
 // position's bytes 4n .. 4n+3 serves all four n-tiles.
 #pragma once
 
-#include <atomic>
-
 #include "partial_mma.cuh"
 
 namespace gqa {
@@ -457,46 +455,17 @@ __global__ void __launch_bounds__(MmaQ8Cfg<D, NHG>::MAX_THREADS, 1)
     }
   }
   if (clus) {
-    // ---- merge the row's chunks through distributed shared memory: chunk CTA r holds chunk
-    //      r's partial; the CTAs of chunks 0 .. nchunks-1 share the (head, dim) outputs
-    cluster_sync();  // every chunk's partial is in place
-    const uint32_t cpa = smem_addr(stages + C::CP_OFF);
-    for (int idx = c * C::NCW * 32 + threadIdx.x; idx < G * D; idx += nchunks * C::NCW * 32) {
-      const int h2 = idx / D, d = idx % D;
-      const uint32_t rec = cpa + static_cast<uint32_t>(h2 * (D + 2)) * 4u;
-      float mr[C::MAX_CLUSTER], ar[C::MAX_CLUSTER], lr[C::MAX_CLUSTER];
-      float M = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < C::MAX_CLUSTER; ++r) {
-        mr[r] = -INFINITY;
-        ar[r] = lr[r] = 0.f;
-        if (r < nchunks) {
-          mr[r] = ld_cluster_f32(cluster_map(rec + D * 4u, r));
-          lr[r] = ld_cluster_f32(cluster_map(rec + (D + 1) * 4u, r));
-          ar[r] = ld_cluster_f32(cluster_map(rec + d * 4u, r));
-        }
-        M = fmaxf(M, mr[r]);
-      }
-      float A = 0.f, Ls = 0.f;
-#pragma unroll
-      for (int r = 0; r < C::MAX_CLUSTER; ++r) {
-        const float e = mr[r] == -INFINITY ? 0.f : fast_exp2(mr[r] - M);
-        A = fmaf(ar[r], e, A);
-        Ls = fmaf(lr[r], e, Ls);
-      }
-      const int head = head0 + h2;
-      p.out[((size_t)t * p.n_heads + head) * D + d] = gated(p, t, head, d, Ls > 0.f ? A / Ls : 0.f);
-    }
-    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    cluster_merge<D, C::MAX_CLUSTER>(p, t, head0, G, c, nchunks, stages + C::CP_OFF, C::NCW);
     return;
   }
   if (p.merge)
     merge_if_last<D>(p, t, head0, G, (size_t)t * gridDim.y + blockIdx.y, nchunks, C::NCW);
 }
 
-// Launches the kernel.  A split row whose chunks fit one cluster (2 .. 8 CTAs) goes out as
-// clusters of its chunk CTAs, which merge in distributed shared memory (no partial records, no
-// arrival counters), unless GQA_Q8_CLUSTER=0 or the GPU cannot hold such a cluster.
+// Launches the kernel, as a programmatic dependent when p.pdl.  A split row whose chunks fit one
+// cluster (2 .. 8 CTAs) goes out as clusters of its chunk CTAs, which merge in distributed
+// shared memory (no partial records, no arrival counters), unless GQA_Q8_CLUSTER=0 or the GPU
+// cannot hold such a cluster.
 template <int D, int NHG>
 cudaError_t launch_mma_q8(PartialParams p, dim3 grid, cudaStream_t s) {
   using C = MmaQ8Cfg<D, NHG>;
@@ -504,35 +473,17 @@ cudaError_t launch_mma_q8(PartialParams p, dim3 grid, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(kern);
   cudaError_t e = ensure_smem(fn, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = grid.x;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::MAX_THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  const bool want = p.merge && grid.x > 1 && grid.x <= static_cast<unsigned>(C::MAX_CLUSTER) &&
+                    q8_cluster_merge();
+  p.cluster = want && cluster_fits<C::MAX_CLUSTER>(fn, cfg, grid.x) ? static_cast<int>(grid.x) : 0;
   cfg.attrs = at;
-  cfg.numAttrs = 1;  // the cluster alone (occupancy query)
-  p.cluster = 0;
-  if (p.merge && grid.x > 1 && grid.x <= static_cast<unsigned>(C::MAX_CLUSTER) &&
-      q8_cluster_merge()) {
-    static std::atomic<int> fits[C::MAX_CLUSTER + 1];  // per cluster size: 0 unknown, 1, 2 no
-    if (fits[grid.x].load() == 0) {
-      int n = 0;
-      const bool ok = cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0;
-      if (!ok) (void)cudaGetLastError();
-      fits[grid.x].store(ok ? 1 : 2);
-    }
-    if (fits[grid.x].load() == 1) p.cluster = static_cast<int>(grid.x);
-  }
-  // [cluster][programmatic dependent], whichever apply
-  cfg.attrs = p.cluster ? at : at + 1;
-  cfg.numAttrs = (p.cluster ? 1 : 0) + (p.pdl ? 1 : 0);
+  cfg.numAttrs = cluster_attrs(at, p.cluster, p.pdl);
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
