@@ -343,6 +343,22 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
       }
     }
   }
+  {
+    // a split grid that fits the GPU merges each row inside a thread-block cluster of its chunk
+    // CTAs (the per-row tensor-core kernels): then up to 8 chunks a row, one stage each at the
+    // least (GB300, D=64 GQA rows: 4096 positions 14.5 -> 12.6 us, 1024 positions 10.5 -> 9.5)
+    const char* fk = std::getenv("GQA_F16_KERNEL");
+    const char* fc = std::getenv("GQA_F16_CLUSTER");
+    const bool f16_cl = kind == GQA_KIND_F16 && !(fk && std::strcmp(fk, "fma") == 0) &&
+                        !(fc && std::strcmp(fc, "0") == 0);
+    const bool q8_cl = kind == GQA_KIND_Q8 && gqa::q8_on_mma() && gqa::q8_cluster_merge();
+    if ((f16_cl || q8_cl) && rgroup == 1 && forced <= 0 && chunk < nmax) {
+      long long c8 = (nmax + 7) / 8;
+      c8 = std::max((c8 + tile - 1) / tile * tile, (long long)tile);
+      const long long ns8 = (nmax + c8 - 1) / c8;
+      if (groups * n_kv_heads * hsplit * ns8 <= num_sms) chunk = c8;
+    }
+  }
   const long long n_split = std::max(1LL, (nmax + chunk - 1) / chunk);
   if (n_split > (1LL << 30)) return fail(GQA_EUNSUPPORTED, "too many chunks");
   plan->chunk = (int)chunk;

@@ -61,7 +61,7 @@ def test_plan_long_context_stream_k(gd, monkeypatch):
     assert q.streamk == 1 and q.grid_x == 1
 
 
-def test_plan_long_context_chunked(gd):
+def test_plan_long_context_chunked(gd, monkeypatch):
     # the default: chunks of min(8192, one wave of 2 CTAs per SM at max length) positions
     p = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_F16, num_sms=152)
     assert p.streamk == 0 and p.tile == 64 and p.chunk == 8192
@@ -70,12 +70,24 @@ def test_plan_long_context_chunked(gd):
     part = 16 * 4 * 32 * 130 * 4
     counters = -(-16 * 8 * 4 // 256) * 256          # per-(row, KV head) arrival counters
     assert p.ws_bytes == counters + -(-part // 256) * 256 + 16 * 4
-    # short rows: chunks of at least two 128-position stages (1 row x 8 KV heads x 4096
-    # positions, D=64)
+    # a grid that fits the GPU merges each row inside a cluster of its chunk CTAs: 8 chunks
+    # a row (1 row x 8 KV heads x 4096 positions, D=64: 64 CTAs)
     q = gd.plan(1, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
-    assert q.chunk == 256 and q.n_split == 16
+    assert q.chunk == 512 and q.n_split == 8
+    # ... down to one 128-position stage a chunk (1024 positions)
+    q = gd.plan(1, 32, 8, 64, 1024, -1, gd.KIND_F16, num_sms=152)
+    assert q.chunk == 128 and q.n_split == 8
     r = gd.plan(1, 4, 1, 64, 100, -1, gd.KIND_F16, num_sms=152)
     assert r.n_split == 1 and r.merge == 0 and r.ws_bytes == 0 and r.chunk == 128
+    # without the cluster merge: chunks of at least two 128-position stages
+    monkeypatch.setenv("GQA_F16_CLUSTER", "0")
+    q = gd.plan(1, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
+    assert q.chunk == 256 and q.n_split == 16
+    # a grid past the SM count keeps the rule: 8 rows x 8 KV heads x 5 chunks of 896
+    off = gd.plan(8, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
+    monkeypatch.delenv("GQA_F16_CLUSTER")
+    on = gd.plan(8, 32, 8, 64, 4096, -1, gd.KIND_F16, num_sms=152)
+    assert (on.chunk, on.n_split) == (off.chunk, off.n_split) == (896, 5)
 
 
 def test_plan_selected_width_caps_chunks(gd):
