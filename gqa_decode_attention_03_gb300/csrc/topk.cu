@@ -38,6 +38,7 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelStageBlocks = 46080;  // 180 KB of staged keys: rows of up to 184,319 cells
 constexpr int kSelBins = 257;           // digits 0..255 of a step, and "above every candidate"
+constexpr int kSelSpecBlocks = 4096;    // block scores read before the row length is known
 
 // fp32 bit pattern -> uint32 whose unsigned order is the float order (-0 below +0; NaNs at the
 // ends): negative values have every bit flipped, the others get the sign bit set.
@@ -65,9 +66,6 @@ __device__ __forceinline__ uint32_t cta_exclusive(uint32_t v, uint32_t* slot, ui
   return before + inc - v;
 }
 
-// The first warp's row of a histogram that has been read: room for the 257 suffix sums.
-__device__ __forceinline__ uint32_t* staged_scratch(uint32_t (*h)[kSelBins]) { return h[0]; }
-
 __global__ void __launch_bounds__(kSelThreads)
     select_cells_kernel(const float* __restrict__ scores, long long stride,
                         const int32_t* __restrict__ kv_len, int budget, int max_kv_len,
@@ -80,6 +78,16 @@ __global__ void __launch_bounds__(kSelThreads)
   // CTAs set up beside this one and wait for this grid's completion before reading ids
   asm volatile("griddepcontrol.launch_dependents;");
   int n = __ldg(kv_len + t);
+  // the row's first kSelSpecBlocks block scores are read beside its length, not after it (the
+  // row holds stride >= stage_cap of them: in bounds whatever the length)
+  const float* row = scores + (size_t)t * stride;
+  const int spec = min(stage_cap, kSelSpecBlocks);
+  float pre[kSelSpecBlocks / kSelThreads];
+#pragma unroll
+  for (int i = 0; i < kSelSpecBlocks / kSelThreads; ++i) {
+    const int b = tid + i * kSelThreads;
+    pre[i] = b < spec ? __ldg(row + b) : 0.f;
+  }
   if (n < 0 || n > max_kv_len) {
     if (tid == 0) flag_error(err, GQA_ERR_KVLEN_RANGE);
     n = n < 0 ? 0 : max_kv_len;
@@ -90,11 +98,16 @@ __global__ void __launch_bounds__(kSelThreads)
     return;
   }
   const int nb = (n + 3) >> 2;  // blocks; the last one may hold fewer than 4 cells
-  const float* row = scores + (size_t)t * stride;
   const bool stage = nb <= stage_cap;
   for (int i = lane; i < kSelBins; i += 32) hist[0][warp][i] = hist[1][warp][i] = 0u;
-  if (stage)
-    for (int b = tid; b < nb; b += kSelThreads) staged[b] = monotone_key(__ldg(row + b));
+  if (stage) {
+#pragma unroll
+    for (int i = 0; i < kSelSpecBlocks / kSelThreads; ++i) {
+      const int b = tid + i * kSelThreads;
+      if (b < min(nb, spec)) staged[b] = monotone_key(pre[i]);
+    }
+    for (int b = spec + tid; b < nb; b += kSelThreads) staged[b] = monotone_key(__ldg(row + b));
+  }
   __syncthreads();
   auto key = [&](int b) { return stage ? staged[b] : monotone_key(__ldg(row + b)); };
   auto cells = [&](int b) { return static_cast<uint32_t>(min(4, n - 4 * b)); };
@@ -122,25 +135,21 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid < kSelBins)
       for (int w = 0; w < kSelWarps; ++w) bin += h[w][tid];
     uint32_t total;
-    const uint32_t suf = [&] {
-      const uint32_t before = cta_exclusive(bin, slots[sn++ & 1], &total);
-      return total - before;
-    }();
-    // the digit: the one i in 0 .. 255 with suf_i >= budget > suf_(i+1) (suf_0 >= budget, and
-    // suf does not grow with i); suf_256 sits in the slot of thread 256
-    uint32_t* sufs = staged_scratch(h);  // the histogram just read, reused for suf
-    __syncthreads();                     // every gather read of h is done
-    if (tid < kSelBins) sufs[tid] = suf;
-    __syncthreads();
-    if (tid < 256 && suf >= want && sufs[tid + 1] < want) {
+    const uint32_t before = cta_exclusive(bin, slots[sn++ & 1], &total);
+    const uint32_t suf = total - before;
+    // the digit: the one i in 0 .. 255 with suf_i >= budget > suf_(i+1) = suf_i - bin_i
+    // (suf_0 >= budget, and suf does not grow with i)
+    if (tid < 256 && suf >= want && suf - bin < want) {
       pick[0] = tid;
-      pick[1] = sufs[tid + 1];
+      pick[1] = suf - bin;
     }
     __syncthreads();
     T |= pick[0] << sh;
     above = pick[1];  // cells at or above T + 2^sh
-    // the other histogram was last read two barriers ago: clear it for the next step
+    // the other histogram was last read in the previous step, before two barriers: clear it
+    // (this warp's own rows) for the next step
     for (int i = lane; i < kSelBins; i += 32) hist[(step + 1) & 1][warp][i] = 0u;
+    __syncwarp();
   }
   const uint32_t need = want - above;  // cells taken from blocks at the threshold, >= 1
 
