@@ -10,8 +10,14 @@
 
 namespace gqa {
 
+// A byte permute of the 8-byte table {hi4, lo4} by the low 16 bits of sel.  The PTX form takes
+// each selector nibble as it is (bit 3 would ask for sign replication: every selector built here
+// keeps it clear); __byte_perm would first mask the selector, one more integer instruction per
+// permute on the kernel's busiest pipe.
 __device__ __forceinline__ uint32_t prmt(uint32_t lo4, uint32_t hi4, uint32_t sel) {
-  return __byte_perm(lo4, hi4, sel);
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(lo4), "r"(hi4), "r"(sel));
+  return d;
 }
 
 // Four 2-bit fields (bytes 0..3 of y, values 0..3) -> prmt selectors picking f16 numbers

@@ -5,22 +5,24 @@
 // units.  Here both contractions of a 16-position tile run on the tensor cores, with the
 // decoded values built directly as f16 fragments:
 //
-//   q.k  C[pos][head, part] = sum_d A[pos][d] B[d][head, part]: A holds the decoded centroids
-//        c[kidx(d)] (PolarQuant term) or the signs +-1 of the QJL bits (QJL term), B the
-//        rotated (JL-projected) query split into f16 hi and lo parts, one column each.
-//   p.v  C[d][head, part] = sum_pos A[d][pos] B[pos][head, part]: A holds c[vidx(d)], B the
-//        weights p * vnorm split into hi and lo parts.
+//   q.k  C[pos][head, part] = sum_d A[pos][d] B[d][head, part]: A holds bit planes of the keys'
+//        2-bit centroid indices (PolarQuant term) or their QJL sign bits, B the rotated
+//        (JL-projected) query split into f16 hi and lo parts, one column each.
+//   p.v  C[d][head, part] = sum_pos A[d][pos] B[pos][head, part]: A holds bit planes of the
+//        values' indices, B the weights p * vnorm times a plane coefficient, split into hi / lo.
 //
-// Centroids are split the same way (hi and lo f16 planes, one MMA each), so products carry
-// about 22 significant bits and sums are fp32, as on the scalar path.  Power-of-two scales keep
-// the f16 parts clear of overflow and of the subnormal range; they are exact and undone in fp32.
-//
-// Decoding a 2-bit field into an f16 costs a byte permute: a word's four 2-bit fields picked
-// into four bytes (shift, and) become a prmt selector (times 0x22, plus 0x10101010: nibbles
-// 2k and 2k + 1 for field value k) that gathers two f16 centroids from the 8-byte table
-// {c0, c1, c2, c3}.  The k index of the fragments is permuted so that a thread's four fields
-// sit at bit offsets 2i, 2i + 8, 2i + 16, 2i + 24 of one word; B is permuted the same way.  A
-// sign bit becomes +-1 by moving it to an f16 sign position: ((w << s) & 0x80008000) ^ 0xBC00BC00.
+// No centroid is ever decoded.  Over the two bits (b0, b1) of an index the centroid is exactly
+//   c[idx] = c0 + (c1 - c0) b0 + (c2 - c0) b1 + (c3 - c2 - c1 + c0) b0 b1,
+// so sum_d q[d] c[idx(d)] = c0 sum_d q[d] + the planes' sums (the last plane drops out for any
+// centroid set symmetric about zero, and the kernel is instantiated without it then), and a
+// sign sum is 2 sum_{bit set} q_jl - sum_d q_jl.  A plane bit enters the MMA as the f16 whose
+// only set bit is the field's own bit, masked in place: bit k of a half-word is the f16
+// 2^(k - 24) for k <= 10 (subnormal below 10), 2^-11 at bit 12 and 2 at bit 14 -- one exact
+// power of two per k, folded into the other operand (or undone per output row) in fp32.  One
+// AND then makes a fragment register (two elements), where a centroid lookup took two byte
+// permutes (hi and lo planes) and a selector.  The per-head sums of q_rot and q_jl are taken
+// once per CTA; products carry about 22 significant bits of q and of the weights, sums are
+// fp32, as on the scalar path.  Power-of-two scales keep the f16 parts clear of overflow.
 //
 // Each warp streams its own tiles (positions base + 16 * (warp + 4 k)) through a 4-stage
 // cp.async ring in shared memory and keeps its own online-softmax state per head; the states
@@ -58,7 +60,7 @@ struct TqMmaLayout {
 
 // Three CTAs per SM at one n-block (up to 170 registers): 5 % faster on GB300 than four CTAs
 // at 128 registers, which spill
-template <int D, int NB>
+template <int D, int NB, bool B01>
 __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
     tq_mma_kernel(const TqParams tp) {
   using Lay = TqMmaLayout<D>;
@@ -77,18 +79,6 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   if (!tq_row_setup(p, t, c, cta, D, L, s, c0, c1)) return;
 
   // The first tiles' loads go out before the query setup, so their latency hides behind it.
-  // per-thread constants of the decode: sign-bit multipliers (1 << (15 - bit)) of the QJL
-  // fragments, and the byte gather / shift of the p.v fields
-  uint32_t jmul[2][2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    jmul[j][0] = 1u << (15 - (8 * j + fq));
-    jmul[j][1] = 1u << (11 - (8 * j + fq));
-  }
-  const uint32_t vb = static_cast<uint32_t>(fr >> 2);
-  const uint32_t vsel = vb | ((4u + vb) << 4) | ((2u + vb) << 8) | ((6u + vb) << 12);
-  const int vsh = 2 * (fr & 3);
-
   // ---- this warp's tiles through its cp.async ring
   uint32_t* ring = sbuf + warp * S * Lay::SW;
   const int ntiles = (c1 - c0 + 15) / 16;
@@ -147,7 +137,7 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   }
   __syncthreads();
 
-  // ---- scales and f16 fragments of the queries (B operands of q.k) and of the centroids
+  // ---- scales, per-head sums and the f16 fragments of the queries (B operands of q.k)
   float amr = 0.f, amj = 0.f;
   for (int i = lane; i < G * D; i += 32) {
     amr = fmaxf(amr, fabsf(qr[i / D][i % D]));
@@ -156,47 +146,71 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   amr = warp_max(amr);
   amj = warp_max(amj);
   const float sr = pow2_scale(amr), sjq = pow2_scale(amj);
-  const float sc = pow2_scale(fmaxf(fmaxf(fabsf(tp.c0), fabsf(tp.c1)), fmaxf(fabsf(tp.c2), fabsf(tp.c3))));
-  uint32_t th01, th23, tl01, tl23;  // centroid tables: hi and lo planes, f16 {c0, c1 | c2, c3}
-  {
-    uint32_t h, l;
-    split_hi_lo(tp.c0 * sc, tp.c1 * sc, h, l);
-    th01 = h;
-    tl01 = l;
-    split_hi_lo(tp.c2 * sc, tp.c3 * sc, h, l);
-    th23 = h;
-    tl23 = l;
-  }
   const int part = fr & 1;
   uint32_t qb[PW][NB][2], qjb[JW][2][NB][2];
+  float base[NB], cj[NB];  // per softmax head 4 nb + fq: c0 sum_d q_rot, qjl_scale sum_d q_jl
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int hd = 4 * nb + (fr >> 1);
     const bool hv = hd < G;
     const int hr = hv ? hd : 0;
 #pragma unroll
-    for (int kb = 0; kb < PW; ++kb) {
+    for (int kb = 0; kb < PW; ++kb) {  // dims fq, fq + 8 (bit 0 of a half) and fq + 4, fq + 12 (bit 8)
       const float* q = &qr[hr][16 * kb + fq];
-      qb[kb][nb][0] = hv ? f16_part(q[0] * sr, q[4] * sr, part) : 0u;
-      qb[kb][nb][1] = hv ? f16_part(q[8] * sr, q[12] * sr, part) : 0u;
+      qb[kb][nb][0] = hv ? f16_part(q[0] * sr, q[8] * sr, part) : 0u;
+      qb[kb][nb][1] = hv ? f16_part(q[4] * (sr * 0x1p-8f), q[12] * (sr * 0x1p-8f), part) : 0u;
     }
 #pragma unroll
     for (int w = 0; w < JW; ++w)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < 2; ++j) {  // sign bits fq + 8 j (+16) at bit 8 j, fq + 8 j + 4 (+16) at 8 j + 4
         const float* q = &qj[hr][32 * w + 8 * j + fq];
-        qjb[w][j][nb][0] = hv ? f16_part(q[0] * sjq, q[16] * sjq, part) : 0u;
-        qjb[w][j][nb][1] = hv ? f16_part(q[4] * sjq, q[20] * sjq, part) : 0u;
+        const float s0 = j ? sjq * 0x1p-8f : sjq, s1 = j ? sjq * 0x1p-13f : sjq * 0x1p-4f;
+        qjb[w][j][nb][0] = hv ? f16_part(q[0] * s0, q[16] * s0, part) : 0u;
+        qjb[w][j][nb][1] = hv ? f16_part(q[4] * s1, q[20] * s1, part) : 0u;
       }
+    // the softmax head of this thread: 4 nb + fq; its sums over D dims, 8 lanes (fr) a share
+    const int hs = 4 * nb + fq < G ? 4 * nb + fq : 0;
+    float sq = 0.f, sj = 0.f;
+#pragma unroll
+    for (int e = 0; e < D / 8; ++e) {
+      sq += qr[hs][fr * (D / 8) + e];
+      sj += qj[hs][fr * (D / 8) + e];
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sj += __shfl_xor_sync(0xffffffffu, sj, o);
+    }
+    base[nb] = tp.c0 * sq * p.scale_log2;
+    cj[nb] = tp.qjl_scale * sj * p.scale_log2;
   }
-  // x = norm (polar sp + rn signed sj), in log2 units
-  const float sp = p.scale_log2 / (sr * sc), sj = p.scale_log2 * tp.qjl_scale / sjq;
+  // c[idx] = c0 + (c1 - c0) b0 + (c2 - c0) b1 + (c3 - c2 - c1 + c0) b0 b1 over the index bits.
+  // Plane sums come out of the MMAs in units of sr 2^-24 (b1: twice that, read at bit 1), the
+  // sign sum in units of sjq 2^-24; x = norm (base + sum_p kq_p P_p + rn (kj J - cj)), log2 units
+  const float d1 = tp.c1 - tp.c0, d2 = tp.c2 - tp.c0, d3 = (tp.c3 - tp.c2) - (tp.c1 - tp.c0);
+  const float kq0 = d1 * (0x1p24f / sr) * p.scale_log2, kq1 = d2 * (0x1p23f / sr) * p.scale_log2;
+  const float kq2 = d3 * (0x1p24f / sr) * p.scale_log2;
+  const float kj = 2.f * tp.qjl_scale * (0x1p24f / sjq) * p.scale_log2;
+  // p.v weights times the plane coefficients, scaled by a power of two that keeps them <= 1 x w
+  float cs;
+  {
+    int e;
+    frexpf(fmaxf(fmaxf(fabsf(d1), fabsf(d2)), fmaxf(fabsf(d3), 0x1p-100f)), &e);
+    cs = ldexpf(1.f, -e);
+  }
+  const float cw0 = d1 * cs, cw1 = d2 * cs, cw2 = d3 * cs;
+  // this thread's p.v rows are dims fr and fr + 8 of a 16-dim word: field fr of each half of the
+  // interleaved word, bit 2 fr -> an f16 of 2^(2 fr - 24) (2^-11 at bit 12, 2 at bit 14)
+  const uint32_t vmask = 0x00010001u << (2 * fr);
+  const float vunit = fr < 6 ? ldexpf(1.f, 2 * fr - 24) : (fr == 6 ? 0x1p-11f : 2.f);
 
-  float acc[PW][NB][4], m_run[NB], l_run[NB];
+  float acc[PW][NB][4], m_run[NB], l_run[NB], w_run[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     m_run[nb] = -INFINITY;
     l_run[nb] = 0.f;
+    w_run[nb] = 0.f;
 #pragma unroll
     for (int mb = 0; mb < PW; ++mb) acc[mb][nb][0] = acc[mb][nb][1] = acc[mb][nb][2] = acc[mb][nb][3] = 0.f;
   }
@@ -210,59 +224,63 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
     const uint32_t* st = ring + (k % S) * Lay::SW;
     const int nv = c1 - (c0 + 16 * (warp + kTqWarps * k));  // valid positions (>= 1)
 
-    // q.k: PolarQuant term (hi and lo centroid planes) and QJL term, 16 positions x heads
-    float pol[NB][4], pol2[NB][4], jl[NB][4], jl2[NB][4];
+    // q.k: the index bit planes (exact 0 / power-of-two f16) against q, 16 positions x heads
+    float pl0[NB][4], pl1[NB][4], pl2[NB][4], jl[NB][4], jl2[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pol[nb][e] = pol2[nb][e] = jl[nb][e] = jl2[nb][e] = 0.f;
+      for (int e = 0; e < 4; ++e) pl0[nb][e] = pl1[nb][e] = pl2[nb][e] = jl[nb][e] = jl2[nb][e] = 0.f;
 #pragma unroll
     for (int kb = 0; kb < PW; ++kb) {
-      const uint32_t w0 = st[Lay::oKp + fr * KPS + kb], w1 = st[Lay::oKp + (fr + 8) * KPS + kb];
-      uint32_t s0, s0h, s1, s1h;
-      field_sel((w0 >> (2 * fq)) & 0x03030303u, s0, s0h);
-      field_sel((w1 >> (2 * fq)) & 0x03030303u, s1, s1h);
-      const uint32_t ah[4] = {prmt(th01, th23, s0), prmt(th01, th23, s1),
-                              prmt(th01, th23, s0h), prmt(th01, th23, s1h)};
-      const uint32_t al[4] = {prmt(tl01, tl23, s0), prmt(tl01, tl23, s1),
-                              prmt(tl01, tl23, s0h), prmt(tl01, tl23, s1h)};
+      // fields fq, fq + 4, fq + 8, fq + 12 of each position's word at bits 0, 8, 16, 24
+      const uint32_t u0 = st[Lay::oKp + fr * KPS + kb] >> (2 * fq);
+      const uint32_t u1 = st[Lay::oKp + (fr + 8) * KPS + kb] >> (2 * fq);
+      const uint32_t a0[4] = {u0 & 0x00010001u, u1 & 0x00010001u, u0 & 0x01000100u, u1 & 0x01000100u};
+      const uint32_t a1[4] = {u0 & 0x00020002u, u1 & 0x00020002u, u0 & 0x02000200u, u1 & 0x02000200u};
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {  // two accumulators: shorter MMA dependency chains
-        mma_f16(pol[nb], ah, qb[kb][nb][0], qb[kb][nb][1]);
-        mma_f16(pol2[nb], al, qb[kb][nb][0], qb[kb][nb][1]);
+      for (int nb = 0; nb < NB; ++nb) {
+        mma_f16(pl0[nb], a0, qb[kb][nb][0], qb[kb][nb][1]);
+        mma_f16(pl1[nb], a1, qb[kb][nb][0], qb[kb][nb][1]);
+      }
+      if constexpr (B01) {
+        const uint32_t v0 = u0 >> 1, v1 = u1 >> 1;
+        const uint32_t a2[4] = {u0 & v0 & 0x00010001u, u1 & v1 & 0x00010001u,
+                                u0 & v0 & 0x01000100u, u1 & v1 & 0x01000100u};
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_f16(pl2[nb], a2, qb[kb][nb][0], qb[kb][nb][1]);
       }
     }
 #pragma unroll
     for (int w = 0; w < JW; ++w) {
-      const uint32_t z0 = st[Lay::oKj + fr * JW + w], z1 = st[Lay::oKj + (fr + 8) * JW + w];
+      // sign bits fq, fq + 4, fq + 8, fq + 12 of each half at bits 0, 4, 8, 12
+      const uint32_t z0 = st[Lay::oKj + fr * JW + w] >> fq, z1 = st[Lay::oKj + (fr + 8) * JW + w] >> fq;
+      const uint32_t a0[4] = {z0 & 0x00010001u, z1 & 0x00010001u, z0 & 0x00100010u, z1 & 0x00100010u};
+      const uint32_t a1[4] = {z0 & 0x01000100u, z1 & 0x01000100u, z0 & 0x10001000u, z1 & 0x10001000u};
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        // bit -> f16 sign bit 15 (and bit + 16 -> 31): a left shift, as a multiply
-        const uint32_t m0 = jmul[j][0], m1 = jmul[j][1];
-        const uint32_t a[4] = {((z0 * m0) & 0x80008000u) ^ 0xBC00BC00u,
-                               ((z1 * m0) & 0x80008000u) ^ 0xBC00BC00u,
-                               ((z0 * m1) & 0x80008000u) ^ 0xBC00BC00u,
-                               ((z1 * m1) & 0x80008000u) ^ 0xBC00BC00u};
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          if (j == 0) mma_f16(jl[nb], a, qjb[w][j][nb][0], qjb[w][j][nb][1]);
-          else mma_f16(jl2[nb], a, qjb[w][j][nb][0], qjb[w][j][nb][1]);
-        }
+      for (int nb = 0; nb < NB; ++nb) {
+        mma_f16(jl[nb], a0, qjb[w][0][nb][0], qjb[w][0][nb][1]);
+        mma_f16(jl2[nb], a1, qjb[w][1][nb][0], qjb[w][1][nb][1]);
       }
     }
 
     // scores of positions fr and fr + 8 for head 4 nb + fq; online softmax; p.v weights
     const uint32_t kn0 = st[Lay::oKn + fr], kn1 = st[Lay::oKn + fr + 8];
     const float vn0 = half_lo(st[Lay::oVn + fr]), vn1 = half_lo(st[Lay::oVn + fr + 8]);
-    uint32_t pb[NB][2];
+    uint32_t pb[NB][3][2];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      const float P0 = (pol[nb][0] + pol2[nb][0]) + (pol[nb][1] + pol2[nb][1]);
-      const float P1 = (pol[nb][2] + pol2[nb][2]) + (pol[nb][3] + pol2[nb][3]);
+      float t0 = fmaf(kq1, pl1[nb][0] + pl1[nb][1], fmaf(kq0, pl0[nb][0] + pl0[nb][1], base[nb]));
+      float t1 = fmaf(kq1, pl1[nb][2] + pl1[nb][3], fmaf(kq0, pl0[nb][2] + pl0[nb][3], base[nb]));
+      if constexpr (B01) {
+        t0 = fmaf(kq2, pl2[nb][0] + pl2[nb][1], t0);
+        t1 = fmaf(kq2, pl2[nb][2] + pl2[nb][3], t1);
+      }
       const float J0 = (jl[nb][0] + jl2[nb][0]) + (jl[nb][1] + jl2[nb][1]);
       const float J1 = (jl[nb][2] + jl2[nb][2]) + (jl[nb][3] + jl2[nb][3]);
-      const float x0 = fr < nv ? half_lo(kn0) * fmaf(half_hi(kn0) * sj, J0, P0 * sp) : -INFINITY;
-      const float x1 = fr + 8 < nv ? half_lo(kn1) * fmaf(half_hi(kn1) * sj, J1, P1 * sp) : -INFINITY;
+      t0 = fmaf(half_hi(kn0), fmaf(kj, J0, -cj[nb]), t0);
+      t1 = fmaf(half_hi(kn1), fmaf(kj, J1, -cj[nb]), t1);
+      const float x0 = fr < nv ? half_lo(kn0) * t0 : -INFINITY;
+      const float x1 = fr + 8 < nv ? half_lo(kn1) * t1 : -INFINITY;
       float mx = fmaxf(x0, x1);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -279,38 +297,52 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
       }
       m_run[nb] = m_new;
       // B of p.v: column fr = (head 4 nb + fr / 2, part fr % 2) at positions 2 fq, 2 fq + 1,
-      // 2 fq + 8, 2 fq + 9, held by lanes 4 (2 fq) + fr / 2 and 4 (2 fq + 1) + fr / 2
-      // norms past the chunk may be anything (NaN past a sequence's length): select, never
-      // multiply by a zero weight
+      // 2 fq + 8, 2 fq + 9, held by lanes 4 (2 fq) + fr / 2 and 4 (2 fq + 1) + fr / 2; one
+      // B per index plane (the weights times its coefficient).  Norms past the chunk may be
+      // anything (NaN past a sequence's length): select, never multiply by a zero weight
       const float v0 = fr < nv ? p0 * vn0 : 0.f, v1 = fr + 8 < nv ? p1 * vn1 : 0.f;
+      w_run[nb] = fmaf(w_run[nb], corr, v0 + v1);
       const int la = 8 * fq + (fr >> 1), lb = la + 4;
       const float e0 = __shfl_sync(0xffffffffu, v0, la), e1 = __shfl_sync(0xffffffffu, v0, lb);
       const float e2 = __shfl_sync(0xffffffffu, v1, la), e3 = __shfl_sync(0xffffffffu, v1, lb);
       const bool hv = 4 * nb + (fr >> 1) < G;
-      pb[nb][0] = hv ? f16_part(e0, e1, part) : 0u;
-      pb[nb][1] = hv ? f16_part(e2, e3, part) : 0u;
+      pb[nb][0][0] = hv ? f16_part(cw0 * e0, cw0 * e1, part) : 0u;
+      pb[nb][0][1] = hv ? f16_part(cw0 * e2, cw0 * e3, part) : 0u;
+      pb[nb][1][0] = hv ? f16_part(cw1 * e0, cw1 * e1, part) : 0u;
+      pb[nb][1][1] = hv ? f16_part(cw1 * e2, cw1 * e3, part) : 0u;
+      if constexpr (B01) {
+        pb[nb][2][0] = hv ? f16_part(cw2 * e0, cw2 * e1, part) : 0u;
+        pb[nb][2][1] = hv ? f16_part(cw2 * e2, cw2 * e3, part) : 0u;
+      }
     }
 
-    // p.v: rows = dims fr, fr + 8 of each 16-dim polar word, k = the tile's positions
+    // p.v: rows = dims fr, fr + 8 of each 16-dim polar word, k = the tile's positions; the
+    // positions' words interleaved by halves (2 fq | 2 fq + 1 and 2 fq + 8 | 2 fq + 9)
 #pragma unroll
     for (int mb = 0; mb < PW; ++mb) {
       const uint32_t wa = st[Lay::oVp + (2 * fq) * KPS + mb];
       const uint32_t wb = st[Lay::oVp + (2 * fq + 1) * KPS + mb];
       const uint32_t wc = st[Lay::oVp + (2 * fq + 8) * KPS + mb];
       const uint32_t wd = st[Lay::oVp + (2 * fq + 9) * KPS + mb];
-      // bytes (wa.b[fr/4], wb.b[fr/4], wa.b[2 + fr/4], wb.b[2 + fr/4]) hold the fields of dims
-      // fr and fr + 8 at bit 2 (fr % 4) of each byte
-      uint32_t sa, sah, sc2, sch;
-      field_sel((__byte_perm(wa, wb, vsel) >> vsh) & 0x03030303u, sa, sah);
-      field_sel((__byte_perm(wc, wd, vsel) >> vsh) & 0x03030303u, sc2, sch);
-      const uint32_t ah[4] = {prmt(th01, th23, sa), prmt(th01, th23, sah),
-                              prmt(th01, th23, sc2), prmt(th01, th23, sch)};
-      const uint32_t al[4] = {prmt(tl01, tl23, sa), prmt(tl01, tl23, sah),
-                              prmt(tl01, tl23, sc2), prmt(tl01, tl23, sch)};
+      const uint32_t x[4] = {prmt(wa, wb, 0x5410u), prmt(wa, wb, 0x7632u), prmt(wc, wd, 0x5410u),
+                             prmt(wc, wd, 0x7632u)};
+      uint32_t a0[4], a1[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a0[e] = x[e] & vmask;
+        a1[e] = (x[e] >> 1) & vmask;
+      }
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        mma_f16(acc[mb][nb], ah, pb[nb][0], pb[nb][1]);
-        mma_f16(acc[mb][nb], al, pb[nb][0], pb[nb][1]);
+        mma_f16(acc[mb][nb], a0, pb[nb][0][0], pb[nb][0][1]);
+        mma_f16(acc[mb][nb], a1, pb[nb][1][0], pb[nb][1][1]);
+      }
+      if constexpr (B01) {
+        uint32_t a2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a2[e] = x[e] & (x[e] >> 1) & vmask;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mb][nb], a2, pb[nb][2][0], pb[nb][2][1]);
       }
     }
   }
@@ -319,24 +351,28 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   // ---- this warp's state per head into shared memory (the ring is no longer read)
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
-    float l = l_run[nb];
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    float l = l_run[nb], wsum = w_run[nb];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, o);
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    }
     l_run[nb] = l;
+    w_run[nb] = wsum;
   }
   __syncthreads();
   float* mg = reinterpret_cast<float*>(sbuf);
-  const float sv = 1.f / sc;
+  const float sv = 1.f / (vunit * cs);  // the planes' bit value and the coefficients' scale
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int hd = 4 * nb + fq;
     if (hd < G) {
       float* r = mg + (warp * kTqMaxGroup + hd) * (D + 2);
+      const float cw = tp.c0 * w_run[nb];  // the c0 term of every dim
 #pragma unroll
       for (int mb = 0; mb < PW; ++mb) {
-        r[16 * mb + fr] = (acc[mb][nb][0] + acc[mb][nb][1]) * sv;
-        r[16 * mb + fr + 8] = (acc[mb][nb][2] + acc[mb][nb][3]) * sv;
+        r[16 * mb + fr] = fmaf(acc[mb][nb][0] + acc[mb][nb][1], sv, cw);
+        r[16 * mb + fr + 8] = fmaf(acc[mb][nb][2] + acc[mb][nb][3], sv, cw);
       }
       if (fr == 0) {
         r[D] = m_run[nb];
@@ -351,13 +387,22 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
 cudaError_t launch_tq_mma(int head_dim, int nb, dim3 grid, const TqParams& tp,
                           cudaStream_t stream) {
   const int threads = 32 * kTqWarps;
+  // the b0 b1 plane only when the centroids need it (c3 - c2 - c1 + c0 = 0 for any centroid set
+  // symmetric about zero, such as the Lloyd-Max points of a symmetric distribution)
+  const bool b01 = (tp.c3 - tp.c2) - (tp.c1 - tp.c0) != 0.f;
+#define GQA_TQ_LAUNCH(DD, NBB)                                                          \
+  do {                                                                                  \
+    if (b01) tq_mma_kernel<DD, NBB, true><<<grid, threads, 0, stream>>>(tp);            \
+    else tq_mma_kernel<DD, NBB, false><<<grid, threads, 0, stream>>>(tp);               \
+  } while (0)
   if (head_dim == 64) {
-    if (nb == 1) tq_mma_kernel<64, 1><<<grid, threads, 0, stream>>>(tp);
-    else tq_mma_kernel<64, 2><<<grid, threads, 0, stream>>>(tp);
+    if (nb == 1) GQA_TQ_LAUNCH(64, 1);
+    else GQA_TQ_LAUNCH(64, 2);
   } else {
-    if (nb == 1) tq_mma_kernel<128, 1><<<grid, threads, 0, stream>>>(tp);
-    else tq_mma_kernel<128, 2><<<grid, threads, 0, stream>>>(tp);
+    if (nb == 1) GQA_TQ_LAUNCH(128, 1);
+    else GQA_TQ_LAUNCH(128, 2);
   }
+#undef GQA_TQ_LAUNCH
   return cudaGetLastError();
 }
 

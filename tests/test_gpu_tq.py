@@ -79,6 +79,22 @@ def test_tq_split_ragged_rows(chunk):
     assert torch.count_nonzero(got[2]) == 0
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H", [8, 32, 48])
+@pytest.mark.parametrize("chunk", [None, 128])
+def test_tq_asymmetric_centroids(D, H, chunk):
+    """Centroids that are not symmetric about zero (c3 - c2 - c1 + c0 != 0): the tensor-core
+    kernel then needs the b0 b1 index plane as well; every other test draws the symmetric
+    Lloyd-Max points, for which that plane drops out."""
+    L = [700, 1, 0, 333]
+    c = W.make_tq_case(2250 + D + H, len(L), H, 4, D, L, cache_cap=768)
+    c.centroids = (np.array([-1.31, -0.17, 0.58, 1.73]) / np.sqrt(D)).astype(np.float32)
+    assert c.centroids[3] - c.centroids[2] - c.centroids[1] + c.centroids[0] != 0
+    with forced_chunk(chunk):
+        got = run_tq(c)
+    check(got, ref_tq(c))
+
+
 @pytest.mark.parametrize("chunk", [None, 128])
 def test_tq_shared_sequence_causal_rows(chunk):
     # chunked-prefill rows over one sequence: row r sees start + r + 1 positions
