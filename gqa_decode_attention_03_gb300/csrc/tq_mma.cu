@@ -37,7 +37,7 @@
 
 namespace gqa {
 
-constexpr int kTqStages = 4;
+constexpr int kTqStages = 5;
 
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -58,17 +58,25 @@ struct TqMmaLayout {
   static constexpr int kBuf = kStageRing > kMg ? kStageRing : kMg;
 };
 
-// Three CTAs per SM at one n-block (up to 170 registers): 5 % faster on GB300 than four CTAs
-// at 128 registers, which spill
+// Each warp takes its tiles two at a time: both tiles' q.k, one softmax step over their 32
+// positions, both tiles' p.v -- two independent instruction streams in every phase, where a
+// single tile left the warp waiting on each MMA's and mask's latency (3 warps per scheduler).
+// The q.k B fragments (the same for every warp) live in shared memory, over the staged queries,
+// which frees the registers the second tile needs: three CTAs per SM at one n-block.
 template <int D, int NB, bool B01>
-__global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
+__global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
     tq_mma_kernel(const TqParams tp) {
   using Lay = TqMmaLayout<D>;
   constexpr int PW = Lay::PW, JW = Lay::JW, KPS = Lay::KPS, S = kTqStages;
   const PartialParams& p = tp.base;
   __shared__ __align__(16) uint32_t sbuf[Lay::kBuf];  // stage ring, then the warps' states
-  __shared__ __align__(16) float qr[kTqMaxGroup][D];
-  __shared__ __align__(16) float qj[kTqMaxGroup][D];
+  // the group's staged queries [q_rot | q_jl][head][D], then the q.k B fragments [slot][lane]
+  __shared__ __align__(16) float qs[2][kTqMaxGroup][D];
+  static_assert((PW + 2 * JW) * NB * 32 * 8 <= (int)sizeof(qs), "B fragments fit the staging");
+  float(&qr)[kTqMaxGroup][D] = qs[0];
+  float(&qj)[kTqMaxGroup][D] = qs[1];
+  const uint2* fqb = reinterpret_cast<const uint2*>(&qs[0][0][0]);  // [kb][nb][lane]
+  const uint2* fjb = fqb + PW * NB * 32;                              // [w][j][nb][lane]
   const int c = blockIdx.x, t = blockIdx.z;
   const TqCta cta = tq_cta(p);
   const int g = cta.g, G = cta.G;
@@ -79,7 +87,7 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   if (!tq_row_setup(p, t, c, cta, D, L, s, c0, c1)) return;
 
   // The first tiles' loads go out before the query setup, so their latency hides behind it.
-  // ---- this warp's tiles through its cp.async ring
+  // ---- this warp's tiles (chunk tiles warp, warp + 4, ...) through its cp.async ring
   uint32_t* ring = sbuf + warp * S * Lay::SW;
   const int ntiles = (c1 - c0 + 15) / 16;
   const int my_n = ntiles > warp ? (ntiles - warp + kTqWarps - 1) / kTqWarps : 0;
@@ -124,8 +132,9 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
         cp_async_4(st + Lay::oKn + pp, tp.k_norms + row);
     }
   };
+  // S - 2 tiles ahead: each step consumes two stages and refills the two its predecessor freed
 #pragma unroll
-  for (int k = 0; k < S - 1; ++k) {
+  for (int k = 0; k < S - 2; ++k) {
     if (k < my_n) issue(k);
     cp_async_commit();
   }
@@ -147,43 +156,63 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
   amj = warp_max(amj);
   const float sr = pow2_scale(amr), sjq = pow2_scale(amj);
   const int part = fr & 1;
-  uint32_t qb[PW][NB][2], qjb[JW][2][NB][2];
   float base[NB], cj[NB];  // per softmax head 4 nb + fq: c0 sum_d q_rot, qjl_scale sum_d q_jl
+  {
+    uint32_t qb[PW][NB][2], qjb[JW][2][NB][2];
 #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    const int hd = 4 * nb + (fr >> 1);
-    const bool hv = hd < G;
-    const int hr = hv ? hd : 0;
+    for (int nb = 0; nb < NB; ++nb) {
+      const int hd = 4 * nb + (fr >> 1);
+      const bool hv = hd < G;
+      const int hr = hv ? hd : 0;
 #pragma unroll
-    for (int kb = 0; kb < PW; ++kb) {  // dims fq, fq + 8 (bit 0 of a half) and fq + 4, fq + 12 (bit 8)
-      const float* q = &qr[hr][16 * kb + fq];
-      qb[kb][nb][0] = hv ? f16_part(q[0] * sr, q[8] * sr, part) : 0u;
-      qb[kb][nb][1] = hv ? f16_part(q[4] * (sr * 0x1p-8f), q[12] * (sr * 0x1p-8f), part) : 0u;
-    }
-#pragma unroll
-    for (int w = 0; w < JW; ++w)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {  // sign bits fq + 8 j (+16) at bit 8 j, fq + 8 j + 4 (+16) at 8 j + 4
-        const float* q = &qj[hr][32 * w + 8 * j + fq];
-        const float s0 = j ? sjq * 0x1p-8f : sjq, s1 = j ? sjq * 0x1p-13f : sjq * 0x1p-4f;
-        qjb[w][j][nb][0] = hv ? f16_part(q[0] * s0, q[16] * s0, part) : 0u;
-        qjb[w][j][nb][1] = hv ? f16_part(q[4] * s1, q[20] * s1, part) : 0u;
+      for (int kb = 0; kb < PW; ++kb) {  // dims fq, fq + 8 (bit 0 of a half), fq + 4, fq + 12 (bit 8)
+        const float* q = &qr[hr][16 * kb + fq];
+        qb[kb][nb][0] = hv ? f16_part(q[0] * sr, q[8] * sr, part) : 0u;
+        qb[kb][nb][1] = hv ? f16_part(q[4] * (sr * 0x1p-8f), q[12] * (sr * 0x1p-8f), part) : 0u;
       }
-    // the softmax head of this thread: 4 nb + fq; its sums over D dims, 8 lanes (fr) a share
-    const int hs = 4 * nb + fq < G ? 4 * nb + fq : 0;
-    float sq = 0.f, sj = 0.f;
 #pragma unroll
-    for (int e = 0; e < D / 8; ++e) {
-      sq += qr[hs][fr * (D / 8) + e];
-      sj += qj[hs][fr * (D / 8) + e];
-    }
+      for (int w = 0; w < JW; ++w)
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sj += __shfl_xor_sync(0xffffffffu, sj, o);
+        for (int j = 0; j < 2; ++j) {  // sign bits fq + 8 j (+16) at bit 8 j, fq + 8 j + 4 (+16) at 8 j + 4
+          const float* q = &qj[hr][32 * w + 8 * j + fq];
+          const float s0 = j ? sjq * 0x1p-8f : sjq, s1 = j ? sjq * 0x1p-13f : sjq * 0x1p-4f;
+          qjb[w][j][nb][0] = hv ? f16_part(q[0] * s0, q[16] * s0, part) : 0u;
+          qjb[w][j][nb][1] = hv ? f16_part(q[4] * s1, q[20] * s1, part) : 0u;
+        }
+      // the softmax head of this thread: 4 nb + fq; its sums over D dims, 8 lanes (fr) a share
+      const int hs = 4 * nb + fq < G ? 4 * nb + fq : 0;
+      float sq = 0.f, sj = 0.f;
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e) {
+        sq += qr[hs][fr * (D / 8) + e];
+        sj += qj[hs][fr * (D / 8) + e];
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sj += __shfl_xor_sync(0xffffffffu, sj, o);
+      }
+      base[nb] = tp.c0 * sq * p.scale_log2;
+      cj[nb] = tp.qjl_scale * sj * p.scale_log2;
     }
-    base[nb] = tp.c0 * sq * p.scale_log2;
-    cj[nb] = tp.qjl_scale * sj * p.scale_log2;
+    __syncthreads();  // every warp is done with the staged queries
+    if (warp == 0) {
+      uint2* fq2 = reinterpret_cast<uint2*>(&qs[0][0][0]);
+      uint2* fj2 = fq2 + PW * NB * 32;
+#pragma unroll
+      for (int kb = 0; kb < PW; ++kb)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+          fq2[(kb * NB + nb) * 32 + lane] = make_uint2(qb[kb][nb][0], qb[kb][nb][1]);
+#pragma unroll
+      for (int w = 0; w < JW; ++w)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            fj2[((w * 2 + j) * NB + nb) * 32 + lane] = make_uint2(qjb[w][j][nb][0], qjb[w][j][nb][1]);
+    }
+    __syncthreads();
   }
   // c[idx] = c0 + (c1 - c0) b0 + (c2 - c0) b1 + (c3 - c2 - c1 + c0) b0 b1 over the index bits.
   // Plane sums come out of the MMAs in units of sr 2^-24 (b1: twice that, read at bit 1), the
@@ -215,80 +244,122 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
     for (int mb = 0; mb < PW; ++mb) acc[mb][nb][0] = acc[mb][nb][1] = acc[mb][nb][2] = acc[mb][nb][3] = 0.f;
   }
 
-  for (int k = 0; k < my_n; ++k) {
-    __syncwarp();  // every lane is done with the stage the next issue overwrites
-    if (k + S - 1 < my_n) issue(k + S - 1);
-    cp_async_commit();
-    cp_async_wait<S - 1>();
+  for (int k = 0; k < my_n; k += 2) {
+    __syncwarp();  // every lane is done with the two stages the next issues overwrite
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (k + S - 2 + i < my_n) issue(k + S - 2 + i);
+      cp_async_commit();
+    }
+    cp_async_wait<S - 2>();  // tiles k and k + 1 have landed
     __syncwarp();
-    const uint32_t* st = ring + (k % S) * Lay::SW;
-    const int nv = c1 - (c0 + 16 * (warp + kTqWarps * k));  // valid positions (>= 1)
+    const uint32_t* st[2] = {ring + (k % S) * Lay::SW, ring + ((k + 1) % S) * Lay::SW};
+    // valid positions of the two tiles (the second: <= 0 when this warp has no tile k + 1;
+    // its stage then holds an earlier tile's words, whose scores and weights are selected away)
+    const int nv0 = c1 - (c0 + 16 * (warp + kTqWarps * k));
+    const int nv[2] = {nv0, nv0 - 16 * kTqWarps};
 
     // q.k: the index bit planes (exact 0 / power-of-two f16) against q, 16 positions x heads
-    float pl0[NB][4], pl1[NB][4], pl2[NB][4], jl[NB][4], jl2[NB][4];
+    float pl0[2][NB][4], pl1[2][NB][4], pl2[2][NB][4], jl[2][NB][4];
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pl0[nb][e] = pl1[nb][e] = pl2[nb][e] = jl[nb][e] = jl2[nb][e] = 0.f;
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pl0[u][nb][e] = pl1[u][nb][e] = pl2[u][nb][e] = jl[u][nb][e] = 0.f;
 #pragma unroll
     for (int kb = 0; kb < PW; ++kb) {
-      // fields fq, fq + 4, fq + 8, fq + 12 of each position's word at bits 0, 8, 16, 24
-      const uint32_t u0 = st[Lay::oKp + fr * KPS + kb] >> (2 * fq);
-      const uint32_t u1 = st[Lay::oKp + (fr + 8) * KPS + kb] >> (2 * fq);
-      const uint32_t a0[4] = {u0 & 0x00010001u, u1 & 0x00010001u, u0 & 0x01000100u, u1 & 0x01000100u};
-      const uint32_t a1[4] = {u0 & 0x00020002u, u1 & 0x00020002u, u0 & 0x02000200u, u1 & 0x02000200u};
+      uint2 b[NB];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        mma_f16(pl0[nb], a0, qb[kb][nb][0], qb[kb][nb][1]);
-        mma_f16(pl1[nb], a1, qb[kb][nb][0], qb[kb][nb][1]);
-      }
-      if constexpr (B01) {
-        const uint32_t v0 = u0 >> 1, v1 = u1 >> 1;
-        const uint32_t a2[4] = {u0 & v0 & 0x00010001u, u1 & v1 & 0x00010001u,
-                                u0 & v0 & 0x01000100u, u1 & v1 & 0x01000100u};
+      for (int nb = 0; nb < NB; ++nb) b[nb] = fqb[(kb * NB + nb) * 32 + lane];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_f16(pl2[nb], a2, qb[kb][nb][0], qb[kb][nb][1]);
+      for (int u = 0; u < 2; ++u) {
+        // fields fq, fq + 4, fq + 8, fq + 12 of each position's word at bits 0, 8, 16, 24
+        const uint32_t u0 = st[u][Lay::oKp + fr * KPS + kb] >> (2 * fq);
+        const uint32_t u1 = st[u][Lay::oKp + (fr + 8) * KPS + kb] >> (2 * fq);
+        const uint32_t a0[4] = {u0 & 0x00010001u, u1 & 0x00010001u, u0 & 0x01000100u, u1 & 0x01000100u};
+        const uint32_t a1[4] = {u0 & 0x00020002u, u1 & 0x00020002u, u0 & 0x02000200u, u1 & 0x02000200u};
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_f16(pl0[u][nb], a0, b[nb].x, b[nb].y);
+          mma_f16(pl1[u][nb], a1, b[nb].x, b[nb].y);
+        }
+        if constexpr (B01) {
+          const uint32_t v0 = u0 >> 1, v1 = u1 >> 1;
+          const uint32_t a2[4] = {u0 & v0 & 0x00010001u, u1 & v1 & 0x00010001u,
+                                  u0 & v0 & 0x01000100u, u1 & v1 & 0x01000100u};
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(pl2[u][nb], a2, b[nb].x, b[nb].y);
+        }
       }
     }
 #pragma unroll
     for (int w = 0; w < JW; ++w) {
-      // sign bits fq, fq + 4, fq + 8, fq + 12 of each half at bits 0, 4, 8, 12
-      const uint32_t z0 = st[Lay::oKj + fr * JW + w] >> fq, z1 = st[Lay::oKj + (fr + 8) * JW + w] >> fq;
-      const uint32_t a0[4] = {z0 & 0x00010001u, z1 & 0x00010001u, z0 & 0x00100010u, z1 & 0x00100010u};
-      const uint32_t a1[4] = {z0 & 0x01000100u, z1 & 0x01000100u, z0 & 0x10001000u, z1 & 0x10001000u};
+      uint2 b0[NB], b1[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        mma_f16(jl[nb], a0, qjb[w][0][nb][0], qjb[w][0][nb][1]);
-        mma_f16(jl2[nb], a1, qjb[w][1][nb][0], qjb[w][1][nb][1]);
+        b0[nb] = fjb[((w * 2 + 0) * NB + nb) * 32 + lane];
+        b1[nb] = fjb[((w * 2 + 1) * NB + nb) * 32 + lane];
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        // sign bits fq, fq + 4, fq + 8, fq + 12 of each half at bits 0, 4, 8, 12
+        const uint32_t z0 = st[u][Lay::oKj + fr * JW + w] >> fq;
+        const uint32_t z1 = st[u][Lay::oKj + (fr + 8) * JW + w] >> fq;
+        const uint32_t a0[4] = {z0 & 0x00010001u, z1 & 0x00010001u, z0 & 0x00100010u, z1 & 0x00100010u};
+        const uint32_t a1[4] = {z0 & 0x01000100u, z1 & 0x01000100u, z0 & 0x10001000u, z1 & 0x10001000u};
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_f16(jl[u][nb], a0, b0[nb].x, b0[nb].y);
+          mma_f16(jl[u][nb], a1, b1[nb].x, b1[nb].y);
+        }
       }
     }
 
-    // scores of positions fr and fr + 8 for head 4 nb + fq; online softmax; p.v weights
-    const uint32_t kn0 = st[Lay::oKn + fr], kn1 = st[Lay::oKn + fr + 8];
-    const float vn0 = half_lo(st[Lay::oVn + fr]), vn1 = half_lo(st[Lay::oVn + fr + 8]);
-    uint32_t pb[NB][3][2];
+    // scores of positions fr and fr + 8 of both tiles for head 4 nb + fq; one online-softmax
+    // step over the 32 positions; p.v weights
+    uint32_t kn[2][2];
+    float vn[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      kn[u][0] = st[u][Lay::oKn + fr];
+      kn[u][1] = st[u][Lay::oKn + fr + 8];
+      vn[u][0] = half_lo(st[u][Lay::oVn + fr]);
+      vn[u][1] = half_lo(st[u][Lay::oVn + fr + 8]);
+    }
+    uint32_t pb[2][NB][3][2];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      float t0 = fmaf(kq1, pl1[nb][0] + pl1[nb][1], fmaf(kq0, pl0[nb][0] + pl0[nb][1], base[nb]));
-      float t1 = fmaf(kq1, pl1[nb][2] + pl1[nb][3], fmaf(kq0, pl0[nb][2] + pl0[nb][3], base[nb]));
-      if constexpr (B01) {
-        t0 = fmaf(kq2, pl2[nb][0] + pl2[nb][1], t0);
-        t1 = fmaf(kq2, pl2[nb][2] + pl2[nb][3], t1);
-      }
-      const float J0 = (jl[nb][0] + jl2[nb][0]) + (jl[nb][1] + jl2[nb][1]);
-      const float J1 = (jl[nb][2] + jl2[nb][2]) + (jl[nb][3] + jl2[nb][3]);
-      t0 = fmaf(half_hi(kn0), fmaf(kj, J0, -cj[nb]), t0);
-      t1 = fmaf(half_hi(kn1), fmaf(kj, J1, -cj[nb]), t1);
-      const float x0 = fr < nv ? half_lo(kn0) * t0 : -INFINITY;
-      const float x1 = fr + 8 < nv ? half_lo(kn1) * t1 : -INFINITY;
-      float mx = fmaxf(x0, x1);
+      float x[2][2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float tt = fmaf(kq1, pl1[u][nb][2 * r] + pl1[u][nb][2 * r + 1],
+                          fmaf(kq0, pl0[u][nb][2 * r] + pl0[u][nb][2 * r + 1], base[nb]));
+          if constexpr (B01) tt = fmaf(kq2, pl2[u][nb][2 * r] + pl2[u][nb][2 * r + 1], tt);
+          const float J = jl[u][nb][2 * r] + jl[u][nb][2 * r + 1];
+          tt = fmaf(half_hi(kn[u][r]), fmaf(kj, J, -cj[nb]), tt);
+          x[u][r] = fr + 8 * r < nv[u] ? half_lo(kn[u][r]) * tt : -INFINITY;
+        }
+      float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float m_new = fmaxf(m_run[nb], mx);
-      const float corr = fast_exp2(m_run[nb] - m_new);  // first tile: exp2(-inf) = 0
-      const float p0 = fast_exp2(x0 - m_new), p1 = fast_exp2(x1 - m_new);
-      l_run[nb] = fmaf(l_run[nb], corr, p0 + p1);
+      const float corr = fast_exp2(m_run[nb] - m_new);  // first step: exp2(-inf) = 0
+      float pr[2][2], v[2][2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          pr[u][r] = fast_exp2(x[u][r] - m_new);
+          // norms past the chunk may be anything (NaN past a sequence's length): select, never
+          // multiply by a zero weight
+          v[u][r] = fr + 8 * r < nv[u] ? pr[u][r] * vn[u][r] : 0.f;
+        }
+      l_run[nb] = fmaf(l_run[nb], corr, (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+      w_run[nb] = fmaf(w_run[nb], corr, (v[0][0] + v[0][1]) + (v[1][0] + v[1][1]));
       if (__any_sync(0xffffffffu, m_new > m_run[nb])) {
 #pragma unroll
         for (int mb = 0; mb < PW; ++mb)
@@ -298,51 +369,54 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 3 : 2)
       m_run[nb] = m_new;
       // B of p.v: column fr = (head 4 nb + fr / 2, part fr % 2) at positions 2 fq, 2 fq + 1,
       // 2 fq + 8, 2 fq + 9, held by lanes 4 (2 fq) + fr / 2 and 4 (2 fq + 1) + fr / 2; one
-      // B per index plane (the weights times its coefficient).  Norms past the chunk may be
-      // anything (NaN past a sequence's length): select, never multiply by a zero weight
-      const float v0 = fr < nv ? p0 * vn0 : 0.f, v1 = fr + 8 < nv ? p1 * vn1 : 0.f;
-      w_run[nb] = fmaf(w_run[nb], corr, v0 + v1);
+      // B per index plane (the weights times its coefficient)
       const int la = 8 * fq + (fr >> 1), lb = la + 4;
-      const float e0 = __shfl_sync(0xffffffffu, v0, la), e1 = __shfl_sync(0xffffffffu, v0, lb);
-      const float e2 = __shfl_sync(0xffffffffu, v1, la), e3 = __shfl_sync(0xffffffffu, v1, lb);
       const bool hv = 4 * nb + (fr >> 1) < G;
-      pb[nb][0][0] = hv ? f16_part(cw0 * e0, cw0 * e1, part) : 0u;
-      pb[nb][0][1] = hv ? f16_part(cw0 * e2, cw0 * e3, part) : 0u;
-      pb[nb][1][0] = hv ? f16_part(cw1 * e0, cw1 * e1, part) : 0u;
-      pb[nb][1][1] = hv ? f16_part(cw1 * e2, cw1 * e3, part) : 0u;
-      if constexpr (B01) {
-        pb[nb][2][0] = hv ? f16_part(cw2 * e0, cw2 * e1, part) : 0u;
-        pb[nb][2][1] = hv ? f16_part(cw2 * e2, cw2 * e3, part) : 0u;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float e0 = __shfl_sync(0xffffffffu, v[u][0], la), e1 = __shfl_sync(0xffffffffu, v[u][0], lb);
+        const float e2 = __shfl_sync(0xffffffffu, v[u][1], la), e3 = __shfl_sync(0xffffffffu, v[u][1], lb);
+        pb[u][nb][0][0] = hv ? f16_part(cw0 * e0, cw0 * e1, part) : 0u;
+        pb[u][nb][0][1] = hv ? f16_part(cw0 * e2, cw0 * e3, part) : 0u;
+        pb[u][nb][1][0] = hv ? f16_part(cw1 * e0, cw1 * e1, part) : 0u;
+        pb[u][nb][1][1] = hv ? f16_part(cw1 * e2, cw1 * e3, part) : 0u;
+        if constexpr (B01) {
+          pb[u][nb][2][0] = hv ? f16_part(cw2 * e0, cw2 * e1, part) : 0u;
+          pb[u][nb][2][1] = hv ? f16_part(cw2 * e2, cw2 * e3, part) : 0u;
+        }
       }
     }
 
-    // p.v: rows = dims fr, fr + 8 of each 16-dim polar word, k = the tile's positions; the
+    // p.v: rows = dims fr, fr + 8 of each 16-dim polar word, k = a tile's positions; the
     // positions' words interleaved by halves (2 fq | 2 fq + 1 and 2 fq + 8 | 2 fq + 9)
 #pragma unroll
     for (int mb = 0; mb < PW; ++mb) {
-      const uint32_t wa = st[Lay::oVp + (2 * fq) * KPS + mb];
-      const uint32_t wb = st[Lay::oVp + (2 * fq + 1) * KPS + mb];
-      const uint32_t wc = st[Lay::oVp + (2 * fq + 8) * KPS + mb];
-      const uint32_t wd = st[Lay::oVp + (2 * fq + 9) * KPS + mb];
-      const uint32_t x[4] = {prmt(wa, wb, 0x5410u), prmt(wa, wb, 0x7632u), prmt(wc, wd, 0x5410u),
-                             prmt(wc, wd, 0x7632u)};
-      uint32_t a0[4], a1[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        a0[e] = x[e] & vmask;
-        a1[e] = (x[e] >> 1) & vmask;
-      }
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t wa = st[u][Lay::oVp + (2 * fq) * KPS + mb];
+        const uint32_t wb = st[u][Lay::oVp + (2 * fq + 1) * KPS + mb];
+        const uint32_t wc = st[u][Lay::oVp + (2 * fq + 8) * KPS + mb];
+        const uint32_t wd = st[u][Lay::oVp + (2 * fq + 9) * KPS + mb];
+        const uint32_t x[4] = {prmt(wa, wb, 0x5410u), prmt(wa, wb, 0x7632u),
+                               prmt(wc, wd, 0x5410u), prmt(wc, wd, 0x7632u)};
+        uint32_t a0[4], a1[4];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        mma_f16(acc[mb][nb], a0, pb[nb][0][0], pb[nb][0][1]);
-        mma_f16(acc[mb][nb], a1, pb[nb][1][0], pb[nb][1][1]);
-      }
-      if constexpr (B01) {
-        uint32_t a2[4];
+        for (int e = 0; e < 4; ++e) {
+          a0[e] = x[e] & vmask;
+          a1[e] = (x[e] >> 1) & vmask;
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a2[e] = x[e] & (x[e] >> 1) & vmask;
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_f16(acc[mb][nb], a0, pb[u][nb][0][0], pb[u][nb][0][1]);
+          mma_f16(acc[mb][nb], a1, pb[u][nb][1][0], pb[u][nb][1][1]);
+        }
+        if constexpr (B01) {
+          uint32_t a2[4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mb][nb], a2, pb[nb][2][0], pb[nb][2][1]);
+          for (int e = 0; e < 4; ++e) a2[e] = x[e] & (x[e] >> 1) & vmask;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mb][nb], a2, pb[u][nb][2][0], pb[u][nb][2][1]);
+        }
       }
     }
   }
