@@ -1,6 +1,7 @@
 """Decode-attention benchmark: µs per decode step and KV-read GB/s on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_ctx] [--impl gb300|reference]
+                    [--l2 rotate|flush]
 
 One step = one call of the whole path over the workload's batch: a single kernel launch that
 computes the split-KV partials and, in the last CTA of each (row, KV head), their log-sum-exp
@@ -9,8 +10,11 @@ independent replica of the workload on its own GPU (weak scaling; the path needs
 
 Timing: W untimed warm-up steps, then K steps on the launching stream between CUDA events.
 When the KV read of a step is at least 4x the 129 MB L2 (the default workload reads 941 MB),
-the K steps run back to back between two events ("inputs larger than L2"); smaller workloads get
-a 512 MiB device write between steps, outside each step's own pair of events.
+the K steps run back to back between two events ("inputs larger than L2").  Smaller workloads
+rotate: their cache-side inputs (K/V or packed cache, scales, ids, block scores) are copied n times
+so that the copies hold at least 3x the L2, and the K steps run back to back between two events,
+step i on copy i % n, so every step reads its cache from HBM.  ``--l2 flush`` times them one step
+at a time instead, with a 512 MiB device write before each step, outside the step's events.
 ``value`` = algorithmic bytes per step (KV rows read once per KV head + q + out) / mean step time.
 ``e2e`` repeats the step through host buffers: pinned q and kv_len copied in, out copied back
 every step.  For the large workloads it runs as a decode loop does, the copies on their own
@@ -74,16 +78,20 @@ def _dist():
     return ws, rank, local
 
 
-def _config(case, extra=None):
+def _config(case, extra=None, l2_mode="rotate", copies=1, rot_bytes=0):
     big = case.kv_bytes() >= 4 * L2_BYTES
+    small = ("flushed between steps: 512 MiB device write outside each step's events"
+             if l2_mode == "flush" else
+             f"rotated inputs: {copies} device copies of the step's cache-side inputs "
+             f"({rot_bytes / 1e6:.0f} MB, >= 3x the 129 MB L2), steps back to back, each on "
+             "the next copy")
     cfg = {"workload": case.name, "n_tok": int(case.n_tok), "n_heads": int(case.n_heads),
            "n_kv_heads": int(case.n_kv_heads), "head_dim": int(case.head_dim),
            "cache_cap": int(case.cache_cap), "kv_kind": case.kind,
            "visited_positions": int(sum(case.visited(t) for t in range(case.n_tok))),
            "seed": int(case.seed),
            "l2": (f"inputs larger than L2: {case.kv_bytes() / 1e6:.0f} MB of KV read per step vs "
-                  "a 129 MB L2, steps back to back" if big else
-                  "flushed between steps: 512 MiB device write outside each step's events")}
+                  "a 129 MB L2, steps back to back" if big else small)}
     if case.ids is not None:
         cfg["budget"] = int(case.budget)
     cfg.update(extra or {})
@@ -296,6 +304,23 @@ def _e2e_pipelined(torch, step, stream, x, out, q_h, qj_h, kv_h, out_h, steps):
     return t0.elapsed_time(t1) / steps
 
 
+# inputs a step reads from HBM (rotated for the small workloads); q, kv_len, seq_of stay put
+_ROTATED = ("k", "v", "kq", "vq", "ksc", "vsc", "ids", "k_polar", "k_jl", "k_norms", "v_polar",
+            "v_norms", "scores")
+
+
+def _rotation(x, torch):
+    """Copies of the step's large inputs whose total is at least 3x the L2 (SURVEY 8(d)'s cold-L2
+    recipe for workloads smaller than the cache): step i reads copy i % n, so by the time a copy
+    comes round again the n - 1 others have passed through the L2.  Returns one input dict per
+    copy (views into stacked tensors)."""
+    names = [k for k in _ROTATED if x.get(k) is not None]
+    per_copy = sum(x[k].numel() * x[k].element_size() for k in names)
+    n = max(2, min(8192, -(-3 * L2_BYTES // max(per_copy, 1))))
+    stacked = {k: x[k].unsqueeze(0).repeat((n,) + (1,) * x[k].dim()) for k in names}
+    return [dict(x, **{k: stacked[k][i] for k in names}) for i in range(n)]
+
+
 def run_gpu(args):
     import torch
     world, rank, local = _dist()
@@ -321,7 +346,7 @@ def run_gpu(args):
         x["scores"] = torch.from_numpy(scores).cuda()
         x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
 
-    def step(q=None, kv=None, q_jl=None, o=None):
+    def step(q=None, kv=None, q_jl=None, o=None, x=x):
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
         o = out if o is None else o
@@ -345,15 +370,16 @@ def run_gpu(args):
                                   out=o, ws=ws, stream=stream)
 
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    for _ in range(args.warmup):
+    big = case.kv_bytes() >= 4 * L2_BYTES
+    rot = _rotation(x, torch) if not big and args.l2 == "rotate" else [x]
+    for i in range(args.warmup):
         flush.zero_()
-        step()
+        step(x=rot[i % len(rot)])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
     K = args.steps
-    big = case.kv_bytes() >= 4 * L2_BYTES
     with ClockSampler(local) as clk:
         if big:
             # inputs far larger than L2: K back-to-back steps between two events
@@ -364,7 +390,7 @@ def run_gpu(args):
             b.record(stream)
             torch.cuda.synchronize()
             step_ms = np.array([a.elapsed_time(b) / K])
-        else:
+        elif args.l2 == "flush":
             # small inputs: a 512 MiB device write between steps, outside each step's events
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(K)]
@@ -374,7 +400,17 @@ def run_gpu(args):
                 step()
                 ev[i][1].record(stream)
             torch.cuda.synchronize()
-            step_ms = np.array([x.elapsed_time(y) for x, y in ev])
+            step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
+        else:
+            # small inputs: K back-to-back steps between two events, step i on input copy
+            # i % n (n copies >= 3x the L2: every step reads its K/V from HBM)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(K):
+                step(x=rot[i % len(rot)])
+            b.record(stream)
+            torch.cuda.synchronize()
+            step_ms = np.array([a.elapsed_time(b) / K])
     if world > 1:
         torch.distributed.barrier()
 
@@ -461,7 +497,11 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": data,
         "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
-                                 "n_split": plan.n_split, "parallelism": f"replicas x{world}"}),
+                                 "n_split": plan.n_split, "parallelism": f"replicas x{world}"},
+                          l2_mode=args.l2, copies=len(rot),
+                          rot_bytes=len(rot) * sum(v.numel() * v.element_size()
+                                                   for k, v in rot[0].items() if k in _ROTATED
+                                                   and v is not None)),
         "roofline": roofline,
         "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
@@ -633,6 +673,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="long_ctx", choices=sorted(W.NAMED))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
+                    help="cold L2 for workloads smaller than 4x the L2: rotate input copies "
+                         "(steps back to back) or flush with a 512 MiB write before each step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
