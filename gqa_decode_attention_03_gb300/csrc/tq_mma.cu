@@ -46,6 +46,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// The 8x8 16-bit matrix held across the warp in mma fragment order (lane 4 r + c: row r, columns
+// 2 c, 2 c + 1), transposed in registers.
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 template <int D>
 struct TqMmaLayout {
   static constexpr int PW = D / 16, JW = D / 32;
@@ -229,10 +237,17 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
     cs = ldexpf(1.f, -e);
   }
   const float cw0 = d1 * cs, cw1 = d2 * cs, cw2 = d3 * cs;
-  // this thread's p.v rows are dims fr and fr + 8 of a 16-dim word: field fr of each half of the
-  // interleaved word, bit 2 fr -> an f16 of 2^(2 fr - 24) (2^-11 at bit 12, 2 at bit 14)
-  const uint32_t vmask = 0x00010001u << (2 * fr);
-  const float vunit = fr < 6 ? ldexpf(1.f, 2 * fr - 24) : (fr == 6 ? 0x1p-11f : 2.f);
+  // p.v A operands.  Each value word is masked in the keys' layout (position rows fr, fr + 8;
+  // fields fq, fq + 8 and fq + 4, fq + 12 of a 16-dim word at bits 2 fq and 8 + 2 fq of each
+  // half), one AND a register, and every 8x8 block is transposed in registers (movmatrix): rows
+  // become dims, columns positions.  Slot m of a word is dim (m % 8) / 2 + 4 (m / 8) + 8 (m % 2),
+  // field j = (m % 8) / 2 + 4 (m / 8) at bit 2 j of its half: the f16 2^(2 j - 24) (2^-11 for
+  // j = 6, 2 for j = 7).  This thread's accumulator rows are slots fr (dim dr0), fr + 8 (dr1).
+  const uint32_t vm0 = 0x00010001u << (2 * fq), vm1 = 0x01000100u << (2 * fq);
+  const int j0 = fr >> 1, j1 = j0 + 4;
+  const int dr0 = j0 + 8 * (fr & 1), dr1 = j1 + 8 * (fr & 1);
+  auto bitval = [](int j) { return j < 6 ? ldexpf(1.f, 2 * j - 24) : (j == 6 ? 0x1p-11f : 2.f); };
+  const float vu0 = bitval(j0), vu1 = bitval(j1);
 
   float acc[PW][NB][4], m_run[NB], l_run[NB], w_run[NB];
 #pragma unroll
@@ -387,33 +402,26 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
       }
     }
 
-    // p.v: rows = dims fr, fr + 8 of each 16-dim polar word, k = a tile's positions; the
-    // positions' words interleaved by halves (2 fq | 2 fq + 1 and 2 fq + 8 | 2 fq + 9)
+    // p.v: rows = the 16 dims of a polar word (slot order above), k = a tile's positions
 #pragma unroll
     for (int mb = 0; mb < PW; ++mb) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint32_t wa = st[u][Lay::oVp + (2 * fq) * KPS + mb];
-        const uint32_t wb = st[u][Lay::oVp + (2 * fq + 1) * KPS + mb];
-        const uint32_t wc = st[u][Lay::oVp + (2 * fq + 8) * KPS + mb];
-        const uint32_t wd = st[u][Lay::oVp + (2 * fq + 9) * KPS + mb];
-        const uint32_t x[4] = {prmt(wa, wb, 0x5410u), prmt(wa, wb, 0x7632u),
-                               prmt(wc, wd, 0x5410u), prmt(wc, wd, 0x7632u)};
-        uint32_t a0[4], a1[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          a0[e] = x[e] & vmask;
-          a1[e] = (x[e] >> 1) & vmask;
-        }
+        const uint32_t w0 = st[u][Lay::oVp + fr * KPS + mb];
+        const uint32_t w8 = st[u][Lay::oVp + (fr + 8) * KPS + mb];
+        const uint32_t h0 = w0 >> 1, h8 = w8 >> 1;  // b1 at b0's bit
+        const uint32_t a0[4] = {movm_t(w0 & vm0), movm_t(w0 & vm1), movm_t(w8 & vm0),
+                                movm_t(w8 & vm1)};
+        const uint32_t a1[4] = {movm_t(h0 & vm0), movm_t(h0 & vm1), movm_t(h8 & vm0),
+                                movm_t(h8 & vm1)};
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           mma_f16(acc[mb][nb], a0, pb[u][nb][0][0], pb[u][nb][0][1]);
           mma_f16(acc[mb][nb], a1, pb[u][nb][1][0], pb[u][nb][1][1]);
         }
         if constexpr (B01) {
-          uint32_t a2[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) a2[e] = x[e] & (x[e] >> 1) & vmask;
+          const uint32_t a2[4] = {movm_t(w0 & h0 & vm0), movm_t(w0 & h0 & vm1),
+                                  movm_t(w8 & h8 & vm0), movm_t(w8 & h8 & vm1)};
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) mma_f16(acc[mb][nb], a2, pb[u][nb][2][0], pb[u][nb][2][1]);
         }
@@ -436,7 +444,8 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
   }
   __syncthreads();
   float* mg = reinterpret_cast<float*>(sbuf);
-  const float sv = 1.f / (vunit * cs);  // the planes' bit value and the coefficients' scale
+  // the planes' bit values and the coefficients' scale, undone per row
+  const float sv0 = 1.f / (vu0 * cs), sv1 = 1.f / (vu1 * cs);
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int hd = 4 * nb + fq;
@@ -445,8 +454,8 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
       const float cw = tp.c0 * w_run[nb];  // the c0 term of every dim
 #pragma unroll
       for (int mb = 0; mb < PW; ++mb) {
-        r[16 * mb + fr] = fmaf(acc[mb][nb][0] + acc[mb][nb][1], sv, cw);
-        r[16 * mb + fr + 8] = fmaf(acc[mb][nb][2] + acc[mb][nb][3], sv, cw);
+        r[16 * mb + dr0] = fmaf(acc[mb][nb][0] + acc[mb][nb][1], sv0, cw);
+        r[16 * mb + dr1] = fmaf(acc[mb][nb][2] + acc[mb][nb][3], sv1, cw);
       }
       if (fr == 0) {
         r[D] = m_run[nb];
