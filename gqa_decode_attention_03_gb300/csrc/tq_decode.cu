@@ -273,6 +273,10 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   p.merge = plan.merge;
   p.gate = gate;
   p.gate_stride = gate ? gate_stride : 0;
+  {  // the tensor-core kernel goes out as a programmatic dependent; GQA_PDL=0 launches it plainly
+    const char* pd = std::getenv("GQA_PDL");
+    p.pdl = !(pd && std::strcmp(pd, "0") == 0);
+  }
   if (plan.merge) {
     const size_t cnt = ((size_t)n_tok * plan.grid_y * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t part = (size_t)n_tok * plan.n_split * n_heads * (head_dim + 2) * sizeof(float);

@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
   float(&qj)[kTqMaxGroup][D] = qs[1];
   const uint2* fqb = reinterpret_cast<const uint2*>(&qs[0][0][0]);  // [kb][nb][lane]
   const uint2* fjb = fqb + PW * NB * 32;                              // [w][j][nb][lane]
+  // launched as a programmatic dependent of the previous kernel on the stream (a no-op
+  // otherwise): nothing in global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c = blockIdx.x, t = blockIdx.z;
   const TqCta cta = tq_cta(p);
   const int g = cta.g, G = cta.G;
@@ -465,6 +468,9 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
   }
   __syncthreads();
   tq_finish<D>(tp, mg, t, cta, c, L);
+  // the next kernel on the stream may be scheduled once every CTA is here (not earlier: this
+  // grid runs in several waves, whose slots a waiting dependent would take)
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 cudaError_t launch_tq_mma(int head_dim, int nb, dim3 grid, const TqParams& tp,
@@ -473,20 +479,29 @@ cudaError_t launch_tq_mma(int head_dim, int nb, dim3 grid, const TqParams& tp,
   // the b0 b1 plane only when the centroids need it (c3 - c2 - c1 + c0 = 0 for any centroid set
   // symmetric about zero, such as the Lloyd-Max points of a symmetric distribution)
   const bool b01 = (tp.c3 - tp.c2) - (tp.c1 - tp.c0) != 0.f;
+  // a programmatic dependent of whatever precedes it on the stream: the launch overlaps that
+  // kernel's tail (the kernel waits for it before touching global memory)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = tp.base.pdl ? 1 : 0;
 #define GQA_TQ_LAUNCH(DD, NBB)                                                          \
   do {                                                                                  \
-    if (b01) tq_mma_kernel<DD, NBB, true><<<grid, threads, 0, stream>>>(tp);            \
-    else tq_mma_kernel<DD, NBB, false><<<grid, threads, 0, stream>>>(tp);               \
+    if (b01) return cudaLaunchKernelEx(&cfg, tq_mma_kernel<DD, NBB, true>, tp);         \
+    return cudaLaunchKernelEx(&cfg, tq_mma_kernel<DD, NBB, false>, tp);                 \
   } while (0)
   if (head_dim == 64) {
     if (nb == 1) GQA_TQ_LAUNCH(64, 1);
-    else GQA_TQ_LAUNCH(64, 2);
-  } else {
-    if (nb == 1) GQA_TQ_LAUNCH(128, 1);
-    else GQA_TQ_LAUNCH(128, 2);
+    GQA_TQ_LAUNCH(64, 2);
   }
+  if (nb == 1) GQA_TQ_LAUNCH(128, 1);
+  GQA_TQ_LAUNCH(128, 2);
 #undef GQA_TQ_LAUNCH
-  return cudaGetLastError();
 }
 
 }  // namespace gqa
