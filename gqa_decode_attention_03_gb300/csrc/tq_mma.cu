@@ -106,9 +106,54 @@ __global__ void __launch_bounds__(32 * kTqWarps, NB == 1 ? 4 : 2)
   // words and norms are each one contiguous run, copied by consecutive lanes in 16-byte pieces
   const size_t hrow0 = ((size_t)s * p.n_kv_heads + g) * p.cache_cap;
   const bool norms16 = (p.cache_cap & 3) == 0;  // 16-byte pieces of 4 norms stay in the head
+  // A tile wholly inside the chunk (and 4-position norm pieces inside the head) goes out
+  // branch-free: every lane's copies are fixed pieces at a fixed offset from the tile's first
+  // position, one 16-byte copy each (a predicated one for lanes with none of a kind).
+  // D = 128: lane = 2 row + half for the polar rows (K and V); lanes 0-15 a sign row, 16-19 and
+  // 20-23 four K / V norms.  D = 64: lanes 0-15 a K polar row, 16-31 a V one; lanes 0-7 two
+  // sign rows, 8-11 and 12-15 four K / V norms.
+  const size_t pos0 = hrow0 + c0 + 16 * warp;  // the warp's first tile, first position
+  const uint32_t* fa;
+  const uint32_t* fb;
+  const uint32_t* fc;
+  int da, db, dc;
+  bool hc;
+  if constexpr (PW == 8) {
+    const int pp = lane >> 1, ch = lane & 1;
+    fa = tp.k_polar + (pos0 + pp) * PW + 4 * ch;
+    da = Lay::oKp + pp * KPS + 4 * ch;
+    fb = tp.v_polar + (pos0 + pp) * PW + 4 * ch;
+    db = Lay::oVp + pp * KPS + 4 * ch;
+    const int q = (lane - 16) & 3;
+    fc = lane < 16 ? tp.k_jl + (pos0 + lane) * JW
+                   : (lane < 20 ? tp.k_norms : tp.v_norms) + pos0 + 4 * q;
+    dc = lane < 16 ? Lay::oKj + lane * JW : (lane < 20 ? Lay::oKn : Lay::oVn) + 4 * q;
+    hc = lane < 24;
+  } else {
+    const int pp = lane & 15;
+    fa = (lane < 16 ? tp.k_polar : tp.v_polar) + (pos0 + pp) * PW;
+    da = (lane < 16 ? Lay::oKp : Lay::oVp) + pp * KPS;
+    fb = fa;
+    db = da;
+    const int q = lane & 3;
+    fc = lane < 8 ? tp.k_jl + (pos0 + 2 * lane) * JW
+                  : (lane < 12 ? tp.k_norms : tp.v_norms) + pos0 + 4 * q;
+    dc = lane < 8 ? Lay::oKj + 2 * lane * JW : (lane < 12 ? Lay::oKn : Lay::oVn) + 4 * q;
+    hc = lane < 16;
+  }
+  // per tile the warp moves on by 16 x kTqWarps positions: the same number of words per
+  // position for each piece of a kind (polar PW, signs JW, norms 1)
+  constexpr size_t kStep = 16 * kTqWarps;
+  const size_t ic = PW == 8 ? (lane < 16 ? kStep * JW : kStep) : (lane < 8 ? kStep * JW : kStep);
   auto issue = [&](int k) {
     uint32_t* st = ring + (k % S) * Lay::SW;
     const int tb = c0 + 16 * (warp + kTqWarps * k);
+    if (norms16 && tb + 16 <= c1) {
+      cp_async_16(st + da, fa + k * kStep * PW);
+      if constexpr (PW == 8) cp_async_16(st + db, fb + k * kStep * PW);
+      cp_async_16_if(st + dc, fc + k * ic, hc);
+      return;
+    }
     constexpr int CPP = PW / 4;  // 16-byte pieces of a polar row
     if (lane < 16 * CPP) {
       const int pp = lane / CPP, ch = lane % CPP;
