@@ -111,13 +111,6 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
-// The same copy under a per-thread predicate, as one predicated instruction (no branch).
-__device__ __forceinline__ void cp_async_16_if(void* dst, const void* src, bool on) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}"
-      ::"r"(smem_addr(dst)), "l"(src), "r"((int)on)
-      : "memory");
-}
 __device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");

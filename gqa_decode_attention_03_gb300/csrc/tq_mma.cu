@@ -40,6 +40,14 @@ namespace gqa {
 constexpr int kTqStages = 5;
 
 
+// A 16-byte cp.async under a per-thread predicate, as one predicated instruction (no branch).
+__device__ __forceinline__ void cp_async_16_if(void* dst, const void* src, bool on) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}"
+      ::"r"(smem_addr(dst)), "l"(src), "r"((int)on)
+      : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
