@@ -230,6 +230,20 @@ def _merge_launch(plan, kind="f16"):
     return 0
 
 
+def _precision(case, plan):
+    """The operand precision of the step's contractions (all accumulate in fp32 and keep the
+    online softmax in fp32; f16 K/V, int8 codes and TurboQuant bit planes enter exactly)."""
+    if case.kind == "tq":
+        return ("q_rot / q_jl and softmax weights as f16 hi + lo pairs (~22 bits); index and sign "
+                "bit planes exact" + ("; centroids as f16 hi + lo planes" if plan.row_group > 1
+                                      else "; centroids applied in fp32"))
+    if plan.row_group > 1 and case.kind == "f16":
+        if os.environ.get("GQA_F16_ROWS") == "mma":
+            return "q and softmax weights as single f16 (11 bits) on mma.sync"
+        return "q as f16 hi + lo (~22 bits); softmax weights as single f16 (11 bits) into P.V"
+    return "q and softmax weights as f16 hi + lo pairs (~22 bits)"
+
+
 def _kernel_name(case, plan):
     if case.kind == "tq":
         if plan.row_group > 1:
@@ -495,6 +509,7 @@ def run_gpu(args):
         "frac_of_nominal_hbm": round(gbs / world / NOMINAL_HBM_GBS, 4),
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "precision": _precision(case, plan),
         "data": data,
         "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
                                  "n_split": plan.n_split, "parallelism": f"replicas x{world}"},
