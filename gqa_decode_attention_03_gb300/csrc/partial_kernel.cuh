@@ -64,6 +64,9 @@ struct PartialParams {
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at
   long long gate_stride;   //   gate[(t * n_heads + h) * gate_stride + d]
   int pdl;                 // f16 tensor-core kernel launched as a programmatic dependent
+  int rows_fixed;          // tcgen05 row kernel, one sequence: group k is rows [k R, k R + R),
+                           // found without a scan of seq_of, a row valid iff its seq_of is 0
+                           // (host-set when n_seq == 1)
   int cluster;             // tensor-core per-row kernels: > 1 when the row's chunk CTAs form
                            // one thread-block cluster (dims (n_split, 1, 1)) and merge through
                            // distributed shared memory instead of the arrival counters (the

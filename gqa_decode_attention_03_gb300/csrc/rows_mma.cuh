@@ -74,6 +74,7 @@ __device__ __forceinline__ bool rows_is_leader(const PartialParams& p, int t, in
 // Every lane of the warp calls it with the same arguments and gets the same answer.
 __device__ __forceinline__ int rows_find_leader(const PartialParams& p, int R, int k, int& scan_t,
                                                 int& scan_cnt, int lane) {
+  if (p.rows_fixed) return k * R < p.n_tok ? k * R : -1;  // one sequence: groups of R rows
   while (scan_t < p.n_tok) {
     const int t = scan_t + lane;
     const unsigned m = __ballot_sync(0xffffffffu, t < p.n_tok && rows_is_leader(p, t, R));
@@ -112,17 +113,23 @@ __device__ __forceinline__ int rows_len(const PartialParams& p, int t, bool seq_
   return rows_len_of(p, __ldg(p.kv_len + t), seq_ok, err);
 }
 
+// Whether row t's sequence is valid: its group's verdict (a group's rows share one sequence),
+// or with fixed groups (one sequence) its own seq_of entry, which must be that sequence, 0.
+__device__ __forceinline__ bool rows_row_ok(const PartialParams& p, int t, bool group_ok) {
+  return p.rows_fixed ? rows_seq(p, t) == 0 : group_ok;
+}
+
 // len0: kv_len[lane] for rows 0..31 when the caller loaded them beside the leader search (so
 // that a group among the first 32 rows costs no second round trip); used when have_len0.
 __device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, int R, int lane,
                                                int len0 = 0, bool have_len0 = false) {
   RowGroup gr;
   gr.t0 = t0;
-  gr.s = rows_seq(p, t0);
+  gr.s = p.rows_fixed ? 0 : rows_seq(p, t0);
   // rows t0 + 1 + i belong to the group while seq_of stays and no multiple of R is crossed;
-  // checked 32 rows at a time (R can reach 64)
-  gr.nr = 1;
-  for (int base = 0; base < R - 1; base += 32) {
+  // checked 32 rows at a time (R can reach 64); with fixed groups, the next R rows
+  gr.nr = p.rows_fixed ? min(R, p.n_tok - t0) : 1;
+  for (int base = 0; !p.rows_fixed && base < R - 1; base += 32) {
     const int i = base + lane, t = t0 + 1 + i;
     const bool same = i < R - 1 && t < p.n_tok && t % R != 0 && rows_seq(p, t) == gr.s;
     const unsigned run = __ballot_sync(0xffffffffu, same);
@@ -136,7 +143,8 @@ __device__ __forceinline__ RowGroup rows_group(const PartialParams& p, int t0, i
   const int lw = __shfl_sync(0xffffffffu, len0, (t0 + lane) & 31);  // row t0 + lane's, if < 32
   for (int jj = lane; jj < gr.nr; jj += 32) {
     const int t = t0 + jj;
-    L = max(L, have_len0 && t < 32 ? rows_len_of(p, lw, seq_ok, &err) : rows_len(p, t, seq_ok, &err));
+    const bool ok = rows_row_ok(p, t, seq_ok);
+    L = max(L, have_len0 && t < 32 ? rows_len_of(p, lw, ok, &err) : rows_len(p, t, ok, &err));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L = max(L, __shfl_xor_sync(0xffffffffu, L, o));

@@ -148,7 +148,7 @@ __device__ void rows_fused_merge(const PartialParams& p, const RowGroup& gr, int
     for (int q = c + warp * (int)nctas; q < gr.nr * G; q += NSW * (int)nctas) {
       const int t = gr.t0 + q / G, h = g * G + q % G;
       int dummy = 0;
-      const int L = rows_len(p, t, seq_ok, &dummy);
+      const int L = rows_len(p, t, rows_row_ok(p, t, seq_ok), &dummy);
       if (L == 0) continue;  // zeroed by the bookkeeping
       const int nv = min((L + p.chunk - 1) / p.chunk, p.n_split);
       const float* base = p.part + ((size_t)t * p.n_split * p.n_heads + h) * (D + 2);
@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       if (c == 0 && warp == 0) {  // per-row bookkeeping: flags, chunk counts, empty rows
         for (int jb = 0; jb < gr.nr; jb += 32) {
           int err = 0;
-          const int L = jb + lane < gr.nr ? rows_len(p, t0 + jb + lane, seq_ok, &err) : 0;
+          const int tr = t0 + jb + lane;
+          const int L = jb + lane < gr.nr ? rows_len(p, tr, rows_row_ok(p, tr, seq_ok), &err) : 0;
           if (jb + lane < gr.nr) {
             if (err && g == 0) flag_error(p.err, err);
             if (g == 0 && p.merge) p.n_valid[t0 + jb + lane] = (L + p.chunk - 1) / p.chunk;
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(UmmaRowsCfg<D>::THREADS, 1)
       const bool rv = jr < gr.nr;  // this pair is a real row
       const int t = t0 + (rv ? jr : 0);
       int dummy = 0;
-      const int Lp = rv ? rows_len(p, t, seq_ok, &dummy) : 0;
+      const int Lp = rv ? rows_len(p, t, rows_row_ok(p, t, seq_ok), &dummy) : 0;
       // chunk positions [0, lim0) are the pair's, counted from this thread's half of a tile
       const int lim0 = min(Lp, c0 + p.chunk) - c0 - C::CPT * h;
 

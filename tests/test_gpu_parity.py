@@ -348,6 +348,34 @@ def test_rows_grouped_long_runs(G, rows):
     assert_close(got, oracle_ref(case), TOL_F16, f"long runs {rows} G{G}")
 
 
+@pytest.mark.parametrize("rows", ["umma", "mma"])
+@pytest.mark.parametrize("chunk", [None, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_one_sequence_rows_with_bad_entries(G, chunk, rows):
+    """Rows of a single sequence (the chunked-prefill layout, where the tcgen05 row kernel takes
+    fixed runs of rows as its groups): entries of seq_of out of range at a group's first and
+    last row, mid-group and at the end give zero rows and the flag; an empty row, a row of one
+    position and ragged lengths beside them stay exact."""
+    T = 150
+    L = [200 + (37 * t) % 101 for t in range(T)]
+    L[5], L[64] = 0, 1
+    case = W.make_f16_case(700 + G, T, 2 * G, 2, 64, L, cache_cap=320, seq_of=[0] * T, n_seq=1,
+                           scale=0.125)
+    bad = [0, 31, 32, 63, 100, 149]
+    seq_bad = case.seq_of.copy()
+    seq_bad[bad] = [1, -1, 3, 7, 1, 2]
+    good = [t for t in range(T) if t not in bad]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = oracle_ref(case)
+    case.seq_of = seq_bad
+    with forced_chunk(chunk), f16_kernel(ROWS_KERNELS[rows]):
+        assert _gd().plan(T, 2 * G, 2, 64, 320, n_seq=1).row_group == ROWS_PER_GROUP[rows] // G
+        got = run_case(case, err=err).cpu().numpy()
+    assert int(err.item()) & _gd().ERR_SEQ_RANGE
+    assert (got[bad] == 0).all()
+    assert_close(got[good], ref[good], TOL_F16, f"one sequence {rows} G{G} chunk{chunk}")
+
+
 @pytest.mark.parametrize("pair_layout", [False, True])
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_merge_with_sigmoid_gate(D, pair_layout):
