@@ -13,8 +13,11 @@ When the KV read of a step is at least 4x the 129 MB L2 (the default workload re
 the K steps run back to back between two events ("inputs larger than L2").  Smaller workloads
 rotate: their cache-side inputs (K/V or packed cache, scales, ids, block scores) are copied n times
 so that the copies hold at least 3x the L2, and the K steps run back to back between two events,
-step i on copy i % n, so every step reads its cache from HBM.  ``--l2 flush`` times them one step
-at a time instead, with a 512 MiB device write before each step, outside the step's events.
+step i on copy i % n, so every step reads its cache from HBM.  By default the K steps are
+captured into one CUDA graph (as a decode loop launches them) and timed as one replay, after an
+untimed replay; ``--launch stream`` calls the library once per step from Python instead.
+``--l2 flush`` times them one step at a time, with a 512 MiB device write before each step,
+outside the step's events.
 ``value`` = algorithmic bytes per step (KV rows read once per KV head + q + out) / mean step time.
 ``e2e`` repeats the step through host buffers: pinned q and kv_len copied in, out copied back
 every step.  For the large workloads it runs as a decode loop does, the copies on their own
@@ -324,15 +327,32 @@ _ROTATED = ("k", "v", "kq", "vq", "ksc", "vsc", "ids", "k_polar", "k_jl", "k_nor
 
 
 def _rotation(x, torch):
-    """Copies of the step's large inputs whose total is at least 3x the L2 (SURVEY 8(d)'s cold-L2
-    recipe for workloads smaller than the cache): step i reads copy i % n, so by the time a copy
-    comes round again the n - 1 others have passed through the L2.  Returns one input dict per
+    """Copies of the step's large inputs whose total is at least 3x the L2 (cold-L2 timing of
+    workloads smaller than the cache): step i reads copy i % n, so by the time a copy comes
+    round again the n - 1 others have passed through the L2.  Returns one input dict per
     copy (views into stacked tensors)."""
     names = [k for k in _ROTATED if x.get(k) is not None]
     per_copy = sum(x[k].numel() * x[k].element_size() for k in names)
     n = max(2, min(8192, -(-3 * L2_BYTES // max(per_copy, 1))))
     stacked = {k: x[k].unsqueeze(0).repeat((n,) + (1,) * x[k].dim()) for k in names}
     return [dict(x, **{k: stacked[k][i] for k in names}) for i in range(n)]
+
+
+def _capture(torch, step, seq):
+    """One CUDA graph of len(seq) steps, step i on input dict seq[i], replayed once (untimed)
+    so that the graph is uploaded and the caches and clocks are in their steady state."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(x=seq[0])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for xi in seq:
+            step(x=xi)
+    g.replay()
+    torch.cuda.synchronize()
+    return g
 
 
 def run_gpu(args):
@@ -361,6 +381,7 @@ def run_gpu(args):
         x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
 
     def step(q=None, kv=None, q_jl=None, o=None, x=x):
+        stream = torch.cuda.current_stream()  # the launching stream (a capture stream too)
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
         o = out if o is None else o
@@ -394,8 +415,20 @@ def run_gpu(args):
         torch.distributed.barrier()
 
     K = args.steps
+    graph = None
+    if args.launch == "graph" and (big or args.l2 == "rotate"):
+        graph = _capture(torch, step, [x] * K if big else [rot[i % len(rot)] for i in range(K)])
     with ClockSampler(local) as clk:
-        if big:
+        if graph:
+            # the K steps (each on its input copy, as below) replayed from one CUDA graph, the
+            # launch path of a decode loop; a first replay, untimed, uploaded it
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            step_ms = np.array([a.elapsed_time(b) / K])
+        elif big:
             # inputs far larger than L2: K back-to-back steps between two events
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -512,7 +545,9 @@ def run_gpu(args):
         "precision": _precision(case, plan),
         "data": data,
         "config": _config(case, {"algorithmic_bytes_per_step": alg, "chunk": plan.chunk,
-                                 "n_split": plan.n_split, "parallelism": f"replicas x{world}"},
+                                 "n_split": plan.n_split, "parallelism": f"replicas x{world}",
+                                 "launch": ("the K steps replayed from one CUDA graph" if graph
+                                            else "one library call per step from Python")},
                           l2_mode=args.l2, copies=len(rot),
                           rot_bytes=len(rot) * sum(v.numel() * v.element_size()
                                                    for k, v in rot[0].items() if k in _ROTATED
@@ -688,6 +723,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="long_ctx", choices=sorted(W.NAMED))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="timed steps replayed from one CUDA graph (default) or launched one "
+                         "call at a time from Python (--l2 flush always launches per call)")
     ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
                     help="cold L2 for workloads smaller than 4x the L2: rotate input copies "
                          "(steps back to back) or flush with a 512 MiB write before each step")
