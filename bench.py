@@ -344,12 +344,13 @@ def _capture(torch, step, seq):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        step(x=seq[0])
+        step(x=seq[0], s=side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
         for xi in seq:
-            step(x=xi)
+            step(x=xi, s=cs)
     g.replay()
     torch.cuda.synchronize()
     return g
@@ -373,15 +374,15 @@ def run_gpu(args):
     plan = gd.plan(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
     ws = gd.alloc_workspace(T, H, Hk, D, max_len, budget, kind, n_seq=case.n_seq)
     out = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
+    stream = launch = torch.cuda.current_stream()
 
     scores = case.meta.get("block_scores")
     if scores is not None:  # the step chooses its ids first (block top-k selection)
         x["scores"] = torch.from_numpy(scores).cuda()
         x["ids"] = torch.empty((T, case.budget), dtype=torch.int32, device="cuda")
 
-    def step(q=None, kv=None, q_jl=None, o=None, x=x):
-        stream = torch.cuda.current_stream()  # the launching stream (a capture stream too)
+    def step(q=None, kv=None, q_jl=None, o=None, x=x, s=None):
+        stream = launch if s is None else s  # s: a graph's capture stream
         q = x["q"] if q is None else q
         kv = x["kv_len"] if kv is None else kv
         o = out if o is None else o

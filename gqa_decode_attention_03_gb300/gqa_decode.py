@@ -105,9 +105,17 @@ def _ptr(x):
     return None if x is None else ctypes.c_void_p(x.data_ptr())
 
 
+# the current stream's raw handle without building a torch Stream object (several us a call)
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_GET_DEVICE = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _RAW_STREAM is not None and _GET_DEVICE is not None:
+        return ctypes.c_void_p(_RAW_STREAM(_GET_DEVICE()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _need(x, dtype, name, ndim=None):
