@@ -85,6 +85,11 @@ int env_int(const char* name) {
 // bandwidth on both the mixed-length and the uniform batch.
 constexpr int kCtasPerSm = 2;
 constexpr long long kMaxChunk = 8192;
+// f16 rows longer than kMaxChunk are cut into chunks of at most kLongRowChunk: with ragged
+// lengths the finer pieces even out the wave's tail, with uniform ones they add merge work
+// (GB300, 16 rows, D = 128, one box, chunk 8192 -> 4096: lengths U[1024, 32768] 141.6 -> 140.3
+// us, 4 such rows 72.2 -> 70.6; 16 x 32768 302.9 -> 305.5)
+constexpr long long kLongRowChunk = 4096;
 // The tcgen05 row kernel holds ~194 KB of shared memory: one CTA per SM.
 constexpr int kUmmaRowsCtasPerSm = 1;
 // Rows whose whole visited list is at most this many bytes of K/V (and scales) are not split:
@@ -302,6 +307,7 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
         num_sms;
     long long chunk = (units + slots - 1) / slots;
     chunk = std::min(chunk, tq ? kTqMaxChunk : kMaxChunk);
+    if (kind == GQA_KIND_F16 && rgroup == 1 && nmax > kMaxChunk) chunk = std::min(chunk, kLongRowChunk);
     // a split chunk spans at least two stages, so its pipeline has something to overlap
     // (GB300 sweeps: int8 gather 1024 cells 20 us at 2 stages a chunk against 23 us at 1; f16
     // D=64 4096 positions 14.7 against 16.1)

@@ -62,12 +62,16 @@ def test_plan_long_context_stream_k(gd, monkeypatch):
 
 
 def test_plan_long_context_chunked(gd, monkeypatch):
-    # the default: chunks of min(8192, one wave of 2 CTAs per SM at max length) positions
+    # the default: chunks of min(8192, one wave of 2 CTAs per SM at max length) positions, and
+    # at most 4096 for rows longer than 8192
     p = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_F16, num_sms=152)
-    assert p.streamk == 0 and p.tile == 64 and p.chunk == 8192
-    assert p.n_split == 4 and p.merge == 1
-    assert (p.grid_x, p.grid_y, p.grid_z) == (4, 8, 16)
-    part = 16 * 4 * 32 * 130 * 4
+    assert p.streamk == 0 and p.tile == 64 and p.chunk == 4096
+    assert p.n_split == 8 and p.merge == 1
+    assert (p.grid_x, p.grid_y, p.grid_z) == (8, 8, 16)
+    # rows of at most 8192 keep chunks of up to 8192 (64 x 8192: one chunk a row)
+    b = gd.plan(64, 32, 8, 128, 8192, -1, gd.KIND_F16, num_sms=152)
+    assert b.chunk == 8192 and b.n_split == 1 and b.merge == 0
+    part = 16 * 8 * 32 * 130 * 4
     counters = -(-16 * 8 * 4 // 256) * 256          # per-(row, KV head) arrival counters
     assert p.ws_bytes == counters + -(-part // 256) * 256 + 16 * 4
     # a grid that fits the GPU merges each row inside a cluster of its chunk CTAs: 8 chunks
