@@ -97,9 +97,11 @@ constexpr int kUmmaRowsCtasPerSm = 1;
 constexpr long long kMinSplitBytes = 128 << 10;
 // TurboQuant caches: 88 bytes per position and KV head at D = 128 against ~8 KB of decode and
 // tensor work, so the split is sized by compute: more, shorter chunks (8 CTAs per SM, at most
-// 2048 positions) and a split from 32 KB of packed row up.
+// 1792 positions) and a split from 32 KB of packed row up.  (GB300, 16 rows U[1024, 32768],
+// D = 128, bit-plane kernel, one box: chunks of 1024, 1280, 1536, 1792, 2048 positions gave
+// 113.1, 110.2, 110.0, 108.2, 113.8 us.)
 constexpr int kTqCtasPerSm = 8;
-constexpr long long kTqMaxChunk = 2048;
+constexpr long long kTqMaxChunk = 1792;
 constexpr long long kTqMinSplitBytes = 32 << 10;
 // The TurboQuant row kernel: 8 warps and ~94 KB of shared memory, one CTA per SM.
 constexpr int kTqRowsCtasPerSm = 1;

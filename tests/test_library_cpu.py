@@ -212,9 +212,9 @@ def test_plan_turboquant(gd):
     assert p.n_split == -(-32768 // p.chunk) and p.merge == 1
     # compute-sized chunks for 8 CTAs per SM: one row of 8 KV heads -> 8 x 32768 / 1216 -> 256
     assert p.chunk == 256 and p.n_split == 128
-    # ... and at most 2048 positions
+    # ... and at most 1792 positions
     r = gd.plan(16, 32, 8, 128, 32768, -1, gd.KIND_TQ, num_sms=152)
-    assert r.chunk == 2048 and (r.grid_x, r.grid_y, r.grid_z) == (16, 8, 16)
+    assert r.chunk == 1792 and (r.grid_x, r.grid_y, r.grid_z) == (19, 8, 16)
     # a row of at most 32 KB (372 positions of 88 bytes) is not split
     q = gd.plan(1, 32, 8, 128, 372, -1, gd.KIND_TQ, num_sms=152)
     assert q.n_split == 1 and q.merge == 0 and q.ws_bytes == 0
