@@ -214,11 +214,11 @@ def _device_inputs(case, torch):
 
 
 def _rows_fused_merge(plan, kind="f16"):
-    """Grouped f16 rows on the tcgen05 kernel merge their own partials when the grid fits one
-    CTA per SM (the library's rule); TurboQuant row groups are always followed by merge_kernel."""
-    if not (plan.merge and not plan.streamk and plan.row_group > 1) or kind == "tq":
+    """Grouped rows on the tcgen05 f16 kernel and on the TurboQuant row kernel merge their own
+    partials when the grid fits one CTA per SM (the library's rule)."""
+    if not (plan.merge and not plan.streamk and plan.row_group > 1):
         return False
-    if os.environ.get("GQA_F16_ROWS") == "mma":
+    if kind != "tq" and os.environ.get("GQA_F16_ROWS") == "mma":
         return False
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -250,7 +250,10 @@ def _precision(case, plan):
 def _kernel_name(case, plan):
     if case.kind == "tq":
         if plan.row_group > 1:
-            return "tq_rows_kernel (rows grouped by sequence)" + (" + merge_kernel" if plan.merge else "")
+            if not plan.merge:
+                return "tq_rows_kernel (rows grouped by sequence)"
+            return "tq_rows_kernel (rows grouped by sequence" + (
+                ", merge fused)" if _rows_fused_merge(plan, "tq") else ") + merge_kernel")
         name = "tq_decode_kernel" if os.environ.get("GQA_TQ_KERNEL") == "fma" else "tq_mma_kernel"
         return name + (" (split-KV, merge fused)" if plan.merge else "")
     if plan.streamk:

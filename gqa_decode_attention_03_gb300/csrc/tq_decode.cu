@@ -304,15 +304,35 @@ static gqa_status tq_entry(const float* q_rot, const float* q_jl, const uint32_t
   // head_dim 32 runs on the CUDA cores: a 32-dim polar row is 8 bytes, below the tensor-core
   // kernel's 16-byte staging pieces
   const int nb = G / p.head_split <= 4 ? 1 : 2;  // n-blocks of 4 heads per CTA
-  if (plan.row_group > 1)  // rows sharing a sequence: one decoded tile for up to 64 pairs
-    (void)gqa::launch_tq_rows(head_dim, grid, tp, stream);
+  if (plan.row_group > 1 && plan.merge) {
+    // rows sharing a sequence: their chunk CTAs merge the group's partials themselves when the
+    // whole grid fits one CTA per SM (a cooperative launch); otherwise merge_kernel follows
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+      const long long ctas = (long long)plan.grid_x * plan.grid_y * plan.grid_z;
+      tp.base.fused_merge = ctas <= sms ? 1 : 0;
+    }
+    (void)cudaGetLastError();
+    // polls of the fused merge's wait before it gives up; GQA_MERGE_SPIN (tests) sets fewer
+    const char* spin = std::getenv("GQA_MERGE_SPIN");
+    tp.base.merge_spin = spin ? (unsigned)std::strtoul(spin, nullptr, 10) : gqa::kSpinLimit;
+  }
+  if (plan.row_group > 1) {  // rows sharing a sequence: one decoded tile for up to 64 pairs
+    cudaError_t el = gqa::launch_tq_rows(head_dim, grid, tp, stream);
+    if (el == cudaErrorCooperativeLaunchTooLarge && tp.base.fused_merge) {  // not all resident
+      (void)cudaGetLastError();
+      tp.base.fused_merge = 0;
+      (void)gqa::launch_tq_rows(head_dim, grid, tp, stream);
+    }
+  }
   else if (head_dim == 32 || (kern && std::strcmp(kern, "fma") == 0))
     (void)gqa::launch_tq_fma(head_dim, grid, tp, stream);
   else
     (void)gqa::launch_tq_mma(head_dim, nb, grid, tp, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));
-  if (plan.row_group > 1 && plan.merge) {  // the row kernel's partials: merged, rotated back
+  if (plan.row_group > 1 && plan.merge && !tp.base.fused_merge) {  // merged, rotated back
     e = gqa::launch_merge(head_dim, p.part, p.n_valid, plan.n_split, n_tok, n_heads, out, stream,
                           gate, gate ? gate_stride : 0, /*after_partials=*/true, signs);
     if (e != cudaSuccess) return tq_fail(GQA_ECUDA, cudaGetErrorString(e));

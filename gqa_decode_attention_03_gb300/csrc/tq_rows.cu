@@ -23,10 +23,13 @@
 //      A = the V planes (ldmatrix.trans), B = the weights in hi and lo parts.
 // Decoding stage k + 1 overlaps the contractions of stage k (two decoded buffers, one CTA
 // barrier per stage).  At the end of the chunk each warp holds its pairs' complete states: it
-// normalises, rotates back and writes them, or writes rotated partials that merge_kernel,
-// launched next as a programmatic dependent, merges and rotates back -- one warp per (row,
-// head), all rows at once.  (A merge by each row's last chunk CTA left the rows' merges queued
-// behind one another in whichever CTA finished last.)
+// normalises, rotates back and writes them, or writes rotated partials.  When the whole grid
+// fits one CTA per SM (a cooperative launch) the group's chunk CTAs then merge those partials
+// themselves: they meet on a counter in the workspace, and CTA c merges, rotates back and
+// writes the group's pairs c NW + w, ... (tq_rows_fused_merge); otherwise merge_kernel,
+// launched next as a programmatic dependent, does it, one warp per (row, head).  (A merge by
+// each row's last chunk CTA left the rows' merges queued behind one another in whichever CTA
+// finished last.)
 #include <cuda_runtime_api.h>
 
 #include "rows_mma.cuh"
@@ -66,6 +69,100 @@ struct TqRowsCfg {
 // Dim of slot s of a 16-slot polar block, and of slot s of a 32-slot sign block.
 __host__ __device__ constexpr int polar_dim(int s) { return 4 * (s % 4) + s / 4; }
 __host__ __device__ constexpr int sign_dim(int s) { return s / 2 + 16 * (s % 2); }
+
+// The fused merge of one group, run by every thread of every chunk CTA of the group (all
+// resident under a cooperative launch), with the counter protocol of the tcgen05 row kernel's
+// fused merge: each CTA stores and fences its partials and counts itself in on the group's
+// counter, thread 0 waits (at most p.merge_spin polls) until all gridDim.x chunk CTAs are in,
+// counts in a second time whatever happened (the CTA whose second count-in takes the counter
+// to 2 gridDim.x resets it), and then warp w of CTA c merges the group's pairs c NW + w,
+// c NW + w + gridDim.x NW, ... with merge_kernel's arithmetic, rotates them back and writes
+// them.  A wait that runs out flags GQA_ERR_TIMEOUT and skips this CTA's share of the merge.
+template <int D>
+__device__ void tq_rows_fused_merge(const TqParams& tp, const RowGroup& gr, int k, int c,
+                                    int Gc, int head0, bool seq_ok) {
+  constexpr int DPL = D / 32, NW = TqRowsCfg<D>::NW;
+  const PartialParams& p = tp.base;
+  __shared__ int merge_ok;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned int nctas = gridDim.x;
+  unsigned int* cnt = p.counters + (size_t)k * gridDim.y + blockIdx.y;
+  __threadfence();  // this thread's partial stores, device-wide
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(cnt, 1u);
+    int ok = 0;
+    for (uint32_t i = 0; i < p.merge_spin; ++i) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= nctas) {
+        ok = 1;
+        break;
+      }
+    }
+    if (atomicAdd(cnt, 1u) == 2 * nctas - 1) atomicExch(cnt, 0u);
+    if (!ok) flag_error(p.err, GQA_ERR_TIMEOUT);
+    merge_ok = ok;
+  }
+  __syncthreads();
+  if (merge_ok) {
+    const size_t rec = (size_t)p.n_heads * (D + 2);  // floats between consecutive chunks
+    const TqRotateBack<D> rot{tp.signs};
+    for (int q = c * NW + warp; q < gr.nr * Gc; q += static_cast<int>(nctas) * NW) {
+      const int t = gr.t0 + q / Gc, head = head0 + q % Gc;
+      int dummy = 0;
+      const int L = rows_len(p, t, seq_ok, &dummy);
+      if (L == 0) continue;  // zeroed by the bookkeeping
+      const int nv = min((L + p.chunk - 1) / p.chunk, p.n_split);
+      const float* base = p.part + ((size_t)t * p.n_split * p.n_heads + head) * (D + 2);
+      float a[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) a[e] = 0.f;
+      float M = -INFINITY, Ls = 0.f;  // Ls: this lane's share of the sum
+      for (int cb = 0; cb < nv; cb += 32) {
+        const int nb = min(32, nv - cb);
+        float m = -INFINITY, l = 0.f;
+        if (lane < nb) {
+          m = __ldcg(base + (cb + lane) * rec + D);
+          l = __ldcg(base + (cb + lane) * rec + D + 1);
+        }
+        float mb = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        const float M_new = fmaxf(M, mb);
+        if (M_new == -INFINITY) continue;
+        const float corr = M == -INFINITY ? 0.f : __expf(M - M_new);
+        M = M_new;
+        Ls *= corr;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) a[e] *= corr;
+        const float w = m == -INFINITY ? 0.f : __expf(m - M);
+        Ls = fmaf(l, w, Ls);
+        const float* ac = base + cb * rec + lane * DPL;
+#pragma unroll 4
+        for (int j = 0; j < nb; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+          for (int e = 0; e < DPL; e += 2) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(ac + j * rec + e));
+            a[e] = fmaf(wj, v.x, a[e]);
+            a[e + 1] = fmaf(wj, v.y, a[e + 1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) a[e] *= inv;
+      rot(a, head, lane);
+      float* o = p.out + ((size_t)t * p.n_heads + head) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[e] = gated(p, t, head, lane * DPL + e, a[e]);
+    }
+  }
+  __syncthreads();  // merge_ok is read before a later group's merge writes it
+}
 
 template <int D>
 __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const TqParams tp) {
@@ -124,7 +221,10 @@ __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const
       }
     }
     const int c1 = min(c0 + p.chunk, gr.lmax);
-    if (c1 <= c0) continue;  // the same for every warp
+    if (c1 <= c0) {  // the same for every warp
+      if (p.merge && p.fused_merge) tq_rows_fused_merge<D>(tp, gr, k, c, Gc, cta.head0, seq_ok);
+      continue;
+    }
     const int nst = (c1 - c0 + TPOS - 1) / TPOS;
     const size_t hrow0 = ((size_t)(seq_ok ? gr.s : 0) * p.n_kv_heads + g) * p.cache_cap;
 
@@ -455,6 +555,7 @@ __global__ void __launch_bounds__(32 * TqRowsCfg<D>::NW, 1) tq_rows_kernel(const
       }
     }
     __syncthreads();  // the state area is read before the next group decodes into it
+    if (p.merge && p.fused_merge) tq_rows_fused_merge<D>(tp, gr, k, c, Gc, cta.head0, seq_ok);
   }
   if (!ok && lane == 0) flag_error(p.err, GQA_ERR_TIMEOUT);
   // this CTA's partials are written: the merge kernel launched after this one may be scheduled
@@ -467,8 +568,19 @@ static cudaError_t launch_rows(dim3 grid, const TqParams& tp, cudaStream_t strea
   const void* fn = reinterpret_cast<const void*>(&tq_rows_kernel<D>);
   cudaError_t e = ensure_smem(fn, C::SMEM);
   if (e != cudaSuccess) return e;
-  tq_rows_kernel<D><<<grid, 32 * C::NW, C::SMEM, stream>>>(tp);
-  return cudaGetLastError();
+  // with the fused merge the chunk CTAs of a group wait for one another: a cooperative launch
+  // guarantees they are all resident
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(32 * C::NW);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = tp.base.fused_merge ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tq_rows_kernel<D>, tp);
 }
 
 cudaError_t launch_tq_rows(int head_dim, dim3 grid, const TqParams& tp, cudaStream_t stream) {

@@ -80,3 +80,45 @@ def test_merge_timeout_leaves_other_rows_alone():
     assert int(err.item()) == 0
     assert_close(got.cpu().numpy(), oracle_ref(case), TOL_F16, "per-row split")
     assert np.isfinite(got.cpu().numpy()).all()
+
+
+def test_tq_rows_fused_merge_wait_runs_out_then_next_call_is_exact():
+    """The TurboQuant row kernel's fused merge (16 causal rows of one sequence on a compressed
+    cache) under GQA_MERGE_SPIN=0: the call flags GQA_ERR_TIMEOUT and leaves the arrival
+    counters at zero, and the next call on the same workspace matches the oracle."""
+    import oracle
+    gd = _gd()
+    L = [1800 + 13 * r for r in range(16)]
+    c = W.make_tq_case(964, 16, 32, 8, 128, L, cache_cap=2000, seq_of=[0] * 16, n_seq=1)
+    T, H, Hk, D, Lm = 16, 32, 8, 128, max(L)
+    plan = gd.plan(T, H, Hk, D, Lm, -1, gd.KIND_TQ, n_seq=1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan.row_group > 1 and plan.merge == 1
+    assert plan.grid_x * plan.grid_y * plan.grid_z <= sms  # the fused merge, not merge_kernel
+    ws = gd.alloc_workspace(T, H, Hk, D, Lm, -1, gd.KIND_TQ, n_seq=1)
+    cnt = _counter_bytes(T, plan.grid_y)
+    i32 = lambda a: dev(np.ascontiguousarray(a).view(np.int32))  # noqa: E731
+    args = (dev(c.q_rot), dev(c.q_jl), i32(c.k_polar), i32(c.k_jl), i32(c.k_norms),
+            i32(c.v_polar), i32(c.v_norms), c.centroids, dev(c.signs), c.qjl_scale,
+            dev(c.kv_len))
+
+    def call(err):
+        return gd.attn_decode_tq(*args, scale=c.scale, seq_of=dev(c.seq_of), max_kv_len=Lm,
+                                 ws=ws, err=err)
+
+    for attempt in range(2):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        with _env(GQA_MERGE_SPIN=0):
+            call(err)
+        torch.cuda.synchronize()
+        assert int(err.item()) & gd.ERR_TIMEOUT, f"attempt {attempt}: no timeout flagged"
+        assert int(ws[:cnt].count_nonzero().item()) == 0, "arrival counters left non-zero"
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = call(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert int(ws[:cnt].count_nonzero().item()) == 0
+    ref = oracle.decode_tq(c.q_rot, c.q_jl, c.k_polar, c.k_jl, c.k_norms, c.v_polar, c.v_norms,
+                           c.centroids, c.signs, c.qjl_scale, c.scale, c.kv_len, c.seq_of)
+    g = got.cpu().numpy().astype(np.float64)
+    assert (np.abs(g - ref) / np.maximum(1.0, np.abs(ref))).max() <= 1e-4  # the TurboQuant bound
