@@ -18,7 +18,11 @@
 //      the digit is the one whose suffix still holds budget cells while the next one's does
 //      not.  After the last step the next suffix is ge(T + 1), the cells strictly above T; the
 //      remaining need = budget - ge(T + 1) cells come from blocks whose key equals T, lowest
-//      cells first.
+//      cells first.  When a step leaves at most kSelFinishCells cells in the chosen digit's bin
+//      (at most 32 blocks: scores spread over a range end there after two steps), those blocks
+//      are gathered and one warp ranks them directly: T is the key of the candidate whose
+//      cells above it fall short of the need while its own reach it, the same T and ge(T + 1)
+//      the remaining steps would find.
 //   2. The list.  Blocks are visited in ascending order in rounds of 4 kSelThreads blocks,
 //      four consecutive blocks a thread.  Exclusive scans (within the thread, then over the
 //      CTA) of the cells at key T give each block the number of such cells before it, hence how
@@ -39,6 +43,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelStageBlocks = 46080;  // 180 KB of staged keys: rows of up to 184,319 cells
 constexpr int kSelBins = 257;           // digits 0..255 of a step, and "above every candidate"
 constexpr int kSelSpecBlocks = 4096;    // block scores read before the row length is known
+constexpr uint32_t kSelFinishCells = 124;  // candidates ranked by one warp: <= 32 blocks
 
 // fp32 bit pattern -> uint32 whose unsigned order is the float order (-0 below +0; NaNs at the
 // ends): negative values have every bit flipped, the others get the sign bit set.
@@ -114,7 +119,8 @@ __global__ void __launch_bounds__(kSelThreads)
   int sn = 0;  // alternates the reduction slots
 
   // ---- 1. the threshold key, eight bits a step (ge(T) >= budget holds throughout: ge(0) = n)
-  __shared__ uint32_t pick[2];  // the step's digit and the cells above T + 2^sh
+  __shared__ uint32_t pick[3];  // the step's digit, the cells above T + 2^sh, the digit's cells
+  __shared__ uint32_t cand_key[32], cand_cells[32], cand_n;  // the direct finish's candidates
   const uint32_t want = static_cast<uint32_t>(budget);
   uint32_t T = 0, above = 0;
   for (int step = 0, sh = 24; sh >= 0; ++step, sh -= 8) {
@@ -142,7 +148,9 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid < 256 && suf >= want && suf - bin < want) {
       pick[0] = tid;
       pick[1] = suf - bin;
+      pick[2] = bin;
     }
+    if (tid == 0) cand_n = 0u;
     __syncthreads();
     T |= pick[0] << sh;
     above = pick[1];  // cells at or above T + 2^sh
@@ -150,6 +158,41 @@ __global__ void __launch_bounds__(kSelThreads)
     // (this warp's own rows) for the next step
     for (int i = lane; i < kSelBins; i += 32) hist[(step + 1) & 1][warp][i] = 0u;
     __syncwarp();
+    if (sh > 0 && pick[2] <= kSelFinishCells) {  // the same for every thread
+      // ---- the direct finish: the blocks of the chosen digit's bin (keys agreeing with T
+      //      from bit sh up), then warp 0 ranks them
+      for (int b = tid; b < nb; b += kSelThreads) {
+        const uint32_t k = key(b);
+        if ((k >> sh) == (T >> sh)) {
+          const uint32_t at = atomicAdd(&cand_n, 1u);
+          cand_key[at] = k;
+          cand_cells[at] = cells(b);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t nc = cand_n, need_c = want - above;  // 1 <= need_c <= the bin's cells
+        const uint32_t kl = lane < nc ? cand_key[lane] : 0u;
+        const uint32_t wl = lane < nc ? cand_cells[lane] : 0u;
+        uint32_t gt = 0, eq = 0;  // cells of the candidates above / at this lane's key
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t kj = __shfl_sync(0xffffffffu, kl, j);
+          const uint32_t wj = __shfl_sync(0xffffffffu, wl, j);
+          gt += kj > kl ? wj : 0u;
+          eq += kj == kl ? wj : 0u;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < nc && gt < need_c && need_c <= gt + eq);
+        if (lane == (hit ? __ffs(hit) - 1 : 0)) {
+          pick[0] = kl;
+          pick[1] = above + gt;
+        }
+      }
+      __syncthreads();
+      T = pick[0];
+      above = pick[1];  // cells above T
+      break;
+    }
   }
   const uint32_t need = want - above;  // cells taken from blocks at the threshold, >= 1
 

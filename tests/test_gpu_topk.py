@@ -40,6 +40,27 @@ def test_topk_bit_exact(levels, budget):
     assert np.array_equal(got, _oracle_ids(scores, kv_len, budget))
 
 
+@pytest.mark.parametrize("dist", ["spread", "clustered", "clustered_ties"])
+@pytest.mark.parametrize("budget", [7, 300, 4000])
+def test_topk_few_candidates_after_any_step(dist, budget):
+    """Score sets whose threshold bin holds only a few blocks after the first 8-bit step (scores
+    spread over many binades), or only after the third (scores sharing their top 16 key bits),
+    with equal scores among those blocks: the selection ranks them directly, bit-exact."""
+    rng = np.random.default_rng(1200 + budget + len(dist))
+    nb = 2049
+    if dist == "spread":
+        s = np.ldexp(rng.choice([-1.0, 1.0], nb) * (1.0 + rng.random(nb)), rng.integers(-60, 60, nb))
+    elif dist == "clustered":
+        s = 1.0 + rng.random(nb) * 2.0 ** -9
+    else:
+        s = 1.0 + rng.integers(0, 600, nb) * 2.0 ** -20
+    scores = s.astype(np.float32).reshape(1, nb)
+    kv_len = np.array([4 * nb - 3], np.int32)  # the last block holds one cell
+    got = _gd().attn_select_topk(dev(scores), dev(kv_len), budget,
+                                 max_kv_len=int(kv_len[0])).cpu().numpy()
+    assert np.array_equal(got, _oracle_ids(scores, kv_len, budget))
+
+
 def test_topk_signed_zero_and_infinities():
     s = np.array([[0.0, -0.0, np.inf, -np.inf, 1.0, -1.0, 0.0, -0.0]], np.float32)
     kv_len = np.array([30], np.int32)
