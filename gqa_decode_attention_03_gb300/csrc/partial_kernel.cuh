@@ -57,8 +57,9 @@ struct PartialParams {
   int n_split;             // chunks per row in the grid (grid.x)
   float scale_log2;        // scale * log2(e)
   int merge;
-  int fused_merge;         // tcgen05 row kernel: the chunk CTAs of a group merge its partials
-                           // themselves (cooperative launch; counters [groups][n_kv_heads])
+  int fused_merge;         // row kernels (tcgen05 f16, TurboQuant): the chunk CTAs of a group
+                           // merge its partials themselves (cooperative launch; counters
+                           // [groups][n_kv_heads], [groups][grid.y] for TurboQuant)
   unsigned int merge_spin; // polls of the fused merge's wait for the group's other chunk CTAs
                            // before it gives up (kSpinLimit unless a test asks for fewer)
   const float* gate;       // sigmoid output gate or null: element (t, h, d) at

@@ -82,13 +82,16 @@ typedef struct gqa_plan {
                                  n_tok, or row-group slots when row_group > 1);
                                  stream-K (CTAs, 1, 1) */
   int merge;         /* 1 when rows may be split: partials go to ws and are merged inside the
-                        same kernel by whichever CTA finishes a row's KV head last, or (rows
-                        grouped by sequence) by a second kernel, one warp per (row, head) */
+                        same kernel by whichever CTA finishes a row's KV head last; rows grouped
+                        by sequence are merged inside the kernel by the group's chunk CTAs when
+                        the grid fits one CTA per SM, else by a second kernel, one warp per
+                        (row, head) */
   int streamk;       /* 1: stream-K split (f16 caches): the (row, KV head, position) stream is
                         cut into equal shares, one per CTA of a persistent grid */
   int row_group;     /* rows one CTA serves from a shared K/V tile: > 1 when rows may share a
-                        sequence (n_seq < n_tok; f16 caches, head_dim 64 or 128, group size
-                        1, 2, 4 or 8), else 1 */
+                        sequence (n_seq < n_tok; f16 caches with head_dim 64 or 128 and group
+                        size 1, 2, 4 or 8, or TurboQuant caches with head_dim 64 or 128), else
+                        1 */
   size_t ws_bytes;   /* workspace the call needs (0 when merge == 0) */
 } gqa_plan;
 
@@ -96,13 +99,14 @@ typedef struct gqa_plan {
  * attn_decode_plan -- the split planner (host only; launches nothing, needs no GPU).
  * Rows are cut into equal chunks (qsa2.metal chunks its id list in fixed 32-cell pieces;
  * FORWARD_MSL's split-T decode uses fixed 512-position partial blocks): enough chunks for about
- * one wave of two CTAs per SM at max_kv_len, none longer than 8192 positions.  With
+ * one wave of two CTAs per SM at max_kv_len, none longer than 8192 positions (4096 for f16
+ * rows longer than 8192; TurboQuant caches: eight CTAs per SM, at most 1792).  With
  * GQA_F16_SPLIT=streamk in the environment, f16 calls with n_tok <= 8192 use the stream-K
  * split instead: a persistent grid of up to two CTAs per SM, each taking an equal share of
  * all rows' KV positions.
- * When rows may share a sequence (n_seq < n_tok) an f16 call groups the rows of each run of
- * equal seq_of[] values (up to 64 / group size rows) into one CTA that reads each K/V tile once
- * for all of them; the chunks are then sized for the groups rather than the rows.
+ * When rows may share a sequence (n_seq < n_tok) an f16 or TurboQuant call groups the rows of
+ * each run of equal seq_of[] values (up to 64 / group size rows) into one CTA that reads each
+ * K/V tile once for all of them; the chunks are then sized for the groups rather than the rows.
  * num_sms <= 0 queries the current CUDA device.  budget < 0 means dense (no id list).  n_seq
  * is the number of sequences in the cache, as passed to the decode call.
  * Returns GQA_EINVAL on bad sizes, GQA_EUNSUPPORTED for group sizes > 16.
@@ -111,10 +115,11 @@ gqa_status attn_decode_plan(int n_tok, int n_seq, int n_heads, int n_kv_heads, i
                             int max_kv_len, int budget, int kind, int num_sms, gqa_plan* plan);
 
 /*
- * attn_decode_workspace_bytes -- bytes of `ws` that attn_decode_f16 (kind GQA_KIND_F16) or
- * attn_decode_q8_sel (GQA_KIND_Q8) needs for these sizes on the current device; 0 when no
- * split is needed or the sizes are invalid.  It is the arrival counters (n_tok * n_kv_heads *
- * 4 bytes, rounded up to 256) followed by the partials: chunked mode n_tok * n_split *
+ * attn_decode_workspace_bytes -- bytes of `ws` that attn_decode_f16 (kind GQA_KIND_F16),
+ * attn_decode_q8_sel (GQA_KIND_Q8) or attn_decode_tq (GQA_KIND_TQ) needs for these sizes on
+ * the current device; 0 when no split is needed or the sizes are invalid.  It is the arrival
+ * counters (n_tok * grid_y * 4 bytes, rounded up to 256; grid_y as attn_decode_plan reports
+ * it: n_kv_heads times the head split) followed by the partials: chunked mode n_tok * n_split *
  * n_heads * (head_dim + 2) * 4 bytes (rounded up to 256) and n_valid (n_tok * 4 bytes);
  * stream-K mode (CTAs + n_tok * n_kv_heads) * group * (head_dim + 2) * 4 bytes.
  */
@@ -134,12 +139,12 @@ size_t attn_decode_workspace_bytes(int n_tok, int n_seq, int n_heads, int n_kv_h
  *   scale         multiplies q.k (finite)
  *   ws, ws_bytes  caller scratch of >= attn_decode_workspace_bytes(..., GQA_KIND_F16) bytes,
  *                 16-byte aligned (may be NULL when that figure is 0).  Its first
- *                 ceil(n_tok * n_kv_heads * 4 / 256) * 256 bytes are per-(row, KV head) arrival
- *                 counters: they must be zero before the first call that uses this ws (zero
- *                 the buffer once after allocating it); every call leaves them zero again, so
- *                 the same ws serves any later call.  The rest holds the split partials
- *                 (see attn_decode_workspace_bytes); it needs no clearing.  Calls sharing a ws
- *                 must not overlap on the GPU.
+ *                 ceil(n_tok * grid_y * 4 / 256) * 256 bytes are arrival counters (per row,
+ *                 or per row group, and KV head): they must be zero before the first call that
+ *                 uses this ws (zero the buffer once after allocating it); every call leaves
+ *                 them zero again, so the same ws serves any later call.  The rest holds the
+ *                 split partials (see attn_decode_workspace_bytes); it needs no clearing.
+ *                 Calls sharing a ws must not overlap on the GPU.
  *   err_word      device int32 or NULL
  */
 gqa_status attn_decode_f16(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -223,7 +228,8 @@ gqa_status attn_select_topk(const float* block_scores, int64_t score_stride,
  *                 low
  *   centroids     HOST fp32 [4]; signs device fp32 [head_dim] (the rotation's sign flips)
  *   head_dim 32, 64 or 128 (the page's set: a power of two, a multiple of 32, at most 128; 32
- *   runs on the CUDA cores), group size <= 8 (else GQA_EUNSUPPORTED).
+ *   runs on the CUDA cores), group size <= 16 (else GQA_EUNSUPPORTED; above 8 heads a KV head's
+ *   group is served by two CTAs of heads).
  *   Other arguments as attn_decode_f16; the workspace is attn_decode_workspace_bytes(...,
  *   GQA_KIND_TQ), zeroed once like attn_decode_f16's.
  */
